@@ -1,0 +1,243 @@
+"""Seeded synthetic workloads for tests and benchmarks.
+
+This module only draws inputs: context lengths, query/key/value values and
+the physical placement of each sequence's logical blocks in the pool.  It
+holds none of the method's arithmetic (no attention, no slot rule, no cache
+layout): both the CUDA path and the fp64 oracle receive what it draws.
+
+Recipe (every config; seed defaults to 0):
+* lengths: numpy PCG64(seed), uniform integers in the config's range
+  (inclusive), or the fixed list of the tiny config;
+* values: torch CPU generator seeded with seed+1, i.i.d. N(0,1), rounded to
+  the config's dtype once (bf16 round-to-nearest-even, or fp32);
+* placement: numpy PCG64(seed+2) permutation of the pool's block ids, handed
+  out to sequences in order; the pool is 1.2x the blocks needed unless the
+  config fixes it (tiny: 32 blocks).  Blocks no sequence owns stay unused.
+
+The K/V histories are LOGICAL: ``k[kv_offsets[s] + j]`` is token j of
+sequence s, shape [sum L][Hkv][d].  The shapes mirror Llama-3-8B/70B GQA
+attention layers (head counts and head dim only; no weights).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+CONFIGS = {
+    # 4 sequences, fp32, MHA, head_dim 64, 16-token blocks in a 32-block pool
+    "tiny": dict(lens=[5, 17, 33, 64], Hq=4, Hkv=4, d=64, bs=16, num_blocks=32,
+                 dtype=torch.float32),
+    # Llama-3-8B-shaped GQA decode
+    "8b": dict(B=64, len_range=(128, 4096), Hq=32, Hkv=8, d=128, bs=16, dtype=torch.bfloat16),
+    # shared system prompt of 1024 tokens + private suffixes, then 64 forks
+    "prefix": dict(B=256, prefix=1024, suffix_range=(1, 512), forks=64, Hq=32, Hkv=8, d=128,
+                   bs=16, dtype=torch.bfloat16),
+    # Llama-3-70B-shaped long-context decode, split into 512-token partitions
+    "70b": dict(B=32, len_range=(16384, 32768), Hq=64, Hkv=8, d=128, bs=32,
+                partition=512, dtype=torch.bfloat16),
+    # continuous batch: 128 decodes + 4 chunked-prefill requests of 512 tokens
+    "mixed": dict(B=128, len_range=(256, 8192), R=4, chunk=512, prior_range=(0, 3584),
+                  Hq=32, Hkv=8, d=128, bs=16, dtype=torch.bfloat16),
+}
+
+
+@dataclass
+class Workload:
+    """Logical inputs of one batch plus the physical placement of its blocks."""
+
+    name: str
+    Hq: int
+    Hkv: int
+    d: int
+    bs: int
+    dtype: torch.dtype
+    lens: np.ndarray            # [B] context length of each sequence (new tokens included)
+    q_counts: np.ndarray        # [B] query rows per sequence (1 for decode)
+    q: torch.Tensor             # [sum q_counts][Hq][d]
+    k: torch.Tensor             # [sum lens][Hkv][d] logical K histories, stacked
+    v: torch.Tensor             # [sum lens][Hkv][d]
+    table: np.ndarray           # [B][max_blocks] int32, physical block of each logical block
+    num_blocks: int
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def B(self) -> int:
+        return len(self.lens)
+
+    @property
+    def kv_offsets(self) -> np.ndarray:
+        off = np.zeros(self.B, dtype=np.int64)
+        off[1:] = np.cumsum(self.lens)[:-1]
+        return off
+
+    @property
+    def max_blocks(self) -> int:
+        return self.table.shape[1]
+
+
+def _values(shape, dtype, gen, device="cpu"):
+    x = torch.randn(*shape, generator=gen, dtype=torch.float32, device="cpu")
+    return x.to(dtype).to(device)
+
+
+def _blocks_of(lens, bs):
+    return [(int(L) + bs - 1) // bs for L in lens]
+
+
+def place(blocks_per_seq, num_blocks, rng, max_blocks=None):
+    """Random physical placement: a permutation of the pool handed out in order."""
+    total = sum(blocks_per_seq)
+    assert total <= num_blocks
+    perm = rng.permutation(num_blocks)
+    mb = max_blocks or max(max(blocks_per_seq), 1)
+    table = np.zeros((len(blocks_per_seq), mb), dtype=np.int32)
+    pos = 0
+    for s, n in enumerate(blocks_per_seq):
+        table[s, :n] = perm[pos:pos + n]
+        pos += n
+    return table
+
+
+def pool_size(blocks_per_seq, factor=1.2):
+    return int(np.ceil(factor * sum(blocks_per_seq)))
+
+
+def decode_workload(name="8b", seed=0, B=None, lens=None, Hq=None, Hkv=None, d=None, bs=None,
+                    dtype=None, num_blocks=None, max_blocks=None, device="cpu"):
+    """Decode batch of config ``name`` (one query per sequence), with overrides."""
+    cfg = dict(CONFIGS[name])
+    Hq = Hq or cfg["Hq"]
+    Hkv = Hkv or cfg["Hkv"]
+    d = d or cfg["d"]
+    bs = bs or cfg["bs"]
+    dtype = dtype or cfg["dtype"]
+    rng_len = np.random.Generator(np.random.PCG64(seed))
+    if lens is None:
+        if "lens" in cfg:
+            lens = cfg["lens"]
+        else:
+            lo, hi = cfg["len_range"]
+            lens = rng_len.integers(lo, hi + 1, size=B or cfg["B"])
+    lens = np.asarray(lens, dtype=np.int64)
+    nblk = _blocks_of(lens, bs)
+    if num_blocks is None:
+        num_blocks = cfg.get("num_blocks") if "lens" in cfg and B is None else None
+        num_blocks = num_blocks or pool_size(nblk)
+    if max_blocks is None:
+        max_blocks = max(nblk) if "len_range" not in cfg else (cfg["len_range"][1] + bs - 1) // bs
+        max_blocks = max(max_blocks, max(nblk))
+    table = place(nblk, num_blocks, np.random.Generator(np.random.PCG64(seed + 2)), max_blocks)
+    gen = torch.Generator().manual_seed(seed + 1)
+    n_kv = int(lens.sum())
+    q = _values((len(lens), Hq, d), dtype, gen, device)
+    k = _values((n_kv, Hkv, d), dtype, gen, device)
+    v = _values((n_kv, Hkv, d), dtype, gen, device)
+    return Workload(name, Hq, Hkv, d, bs, dtype, lens, np.ones(len(lens), np.int64), q, k, v,
+                    table, num_blocks)
+
+
+def prefix_workload(seed=0, B=None, prefix=None, suffix_range=None, device="cpu"):
+    """Shared-prefix decode batch.
+
+    Every sequence starts with the same ``prefix`` tokens (one system prompt)
+    followed by a private suffix.  ``table`` points all sequences at the same
+    physical prefix blocks; ``extra['private_table']`` places a private copy
+    of the prefix for every sequence in a second, larger pool
+    (``extra['private_num_blocks']`` blocks) for the sharing-equivalence check.
+    """
+    cfg = CONFIGS["prefix"]
+    B = B or cfg["B"]
+    P = cfg["prefix"] if prefix is None else prefix
+    lo, hi = suffix_range or cfg["suffix_range"]
+    Hq, Hkv, d, bs, dtype = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["bs"], cfg["dtype"]
+    rng_len = np.random.Generator(np.random.PCG64(seed))
+    suffix = rng_len.integers(lo, hi + 1, size=B).astype(np.int64)
+    lens = P + suffix
+    gen = torch.Generator().manual_seed(seed + 1)
+    q = _values((B, Hq, d), dtype, gen, device)
+    kp = _values((P, Hkv, d), dtype, gen, device)
+    vp = _values((P, Hkv, d), dtype, gen, device)
+    ks = _values((int(suffix.sum()), Hkv, d), dtype, gen, device)
+    vs = _values((int(suffix.sum()), Hkv, d), dtype, gen, device)
+    # logical histories: prefix then the sequence's own suffix
+    k_parts, v_parts, pos = [], [], 0
+    for s in range(B):
+        n = int(suffix[s])
+        k_parts += [kp, ks[pos:pos + n]]
+        v_parts += [vp, vs[pos:pos + n]]
+        pos += n
+    k = torch.cat(k_parts)
+    v = torch.cat(v_parts)
+    # shared placement: prefix blocks once, suffix blocks private
+    n_pre = (P + bs - 1) // bs
+    assert P % bs == 0, "the shared prefix must fill whole blocks"
+    n_suf = [(int(x) + bs - 1) // bs for x in suffix]
+    mb = n_pre + (hi + bs - 1) // bs + 1
+    nb_shared = pool_size([n_pre] + n_suf)
+    perm = np.random.Generator(np.random.PCG64(seed + 2)).permutation(nb_shared)
+    table = np.zeros((B, mb), dtype=np.int32)
+    table[:, :n_pre] = perm[:n_pre]
+    pos = n_pre
+    for s in range(B):
+        table[s, n_pre:n_pre + n_suf[s]] = perm[pos:pos + n_suf[s]]
+        pos += n_suf[s]
+    nb_private = pool_size([n_pre + x for x in n_suf])
+    private = place([n_pre + x for x in n_suf], nb_private,
+                    np.random.Generator(np.random.PCG64(seed + 3)), mb)
+    w = Workload("prefix", Hq, Hkv, d, bs, dtype, lens, np.ones(B, np.int64), q, k, v, table,
+                 nb_shared)
+    w.extra.update(prefix=P, suffix=suffix, private_table=private,
+                   private_num_blocks=nb_private, prefix_blocks=n_pre)
+    return w
+
+
+def mixed_workload(seed=0, B=None, R=None, chunk=None, priors=None, device="cpu"):
+    """Continuous batch: B decode sequences plus R chunked-prefill requests.
+
+    Returns (decode Workload, prefill Workload) sharing one pool of
+    ``num_blocks`` blocks.  Prefill request r has ``extra['prior'][r]`` cached
+    tokens and ``chunk`` new query tokens; its history holds prior+chunk rows.
+    Priors: request 0 has 0, the last has the range maximum, the others are
+    drawn uniformly in between.
+    """
+    cfg = CONFIGS["mixed"]
+    B = B or cfg["B"]
+    R = R or cfg["R"]
+    n = chunk or cfg["chunk"]
+    Hq, Hkv, d, bs, dtype = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["bs"], cfg["dtype"]
+    rng_len = np.random.Generator(np.random.PCG64(seed))
+    lo, hi = cfg["len_range"]
+    lens = rng_len.integers(lo, hi + 1, size=B).astype(np.int64)
+    if priors is None:
+        plo, phi = cfg["prior_range"]
+        mid = rng_len.integers(plo + 1, phi, size=max(R - 2, 0))
+        priors = np.array([plo] + list(mid) + [phi], dtype=np.int64)[:R]
+    priors = np.asarray(priors, dtype=np.int64)
+    plens = priors + n
+    nblk_d = _blocks_of(lens, bs)
+    nblk_p = _blocks_of(plens, bs)
+    num_blocks = pool_size(nblk_d + nblk_p)
+    mb = max(max(nblk_d), max(nblk_p), (hi + bs - 1) // bs)
+    table = place(nblk_d + nblk_p, num_blocks, np.random.Generator(np.random.PCG64(seed + 2)),
+                  mb)
+    gen = torch.Generator().manual_seed(seed + 1)
+    qd = _values((B, Hq, d), dtype, gen, device)
+    kd = _values((int(lens.sum()), Hkv, d), dtype, gen, device)
+    vd = _values((int(lens.sum()), Hkv, d), dtype, gen, device)
+    qp = _values((R * n, Hq, d), dtype, gen, device)
+    kp = _values((int(plens.sum()), Hkv, d), dtype, gen, device)
+    vp = _values((int(plens.sum()), Hkv, d), dtype, gen, device)
+    dec = Workload("mixed-decode", Hq, Hkv, d, bs, dtype, lens, np.ones(B, np.int64), qd, kd, vd,
+                   table[:B], num_blocks)
+    pre = Workload("mixed-prefill", Hq, Hkv, d, bs, dtype, plens, np.full(R, n, np.int64), qp,
+                   kp, vp, table[B:], num_blocks)
+    pre.extra.update(prior=priors, chunk=n)
+    return dec, pre
+
+
+def sample_indices(n, k, seed=0):
+    """k distinct indices of range(n), seeded, sorted."""
+    rng = np.random.Generator(np.random.PCG64(seed + 7))
+    return np.sort(rng.choice(n, size=min(k, n), replace=False))

@@ -1,0 +1,225 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged-attention library.
+ *
+ * PagedAttention keeps each sequence's KV cache in fixed-size physical blocks
+ * and reaches them through a per-sequence block table that maps logical block
+ * i to a physical block anywhere in the pool ("PagedAttention: memetakan blok
+ * KV logis ke memori fisik tidak kontigu", section "Urutan logis dipisahkan
+ * dari penempatan fisik"; "Apa itu PagedAttention?", section "Cara kerja
+ * PagedAttention: Blok halaman non-kontigu").  The attention kernel follows
+ * the block table before it loads K and V (nalar.dev, section "Kernel
+ * attention harus mengikuti block table"); the attention equation itself is
+ * unchanged (same page, opening section).
+ *
+ * Conventions for every call
+ * --------------------------
+ *  - Return value: PA_OK (0) or a PA_ERR_* code; pa_last_error_string()
+ *    gives the message of the last failing call on the calling thread.
+ *  - Tensors are caller-owned DEVICE pointers (unless a parameter says host).
+ *    The library never allocates device memory in an op call and keeps no
+ *    pointer after it returns.
+ *  - Ops are asynchronous on the given stream (a cudaStream_t; NULL = the
+ *    legacy default stream).  The status covers argument checks and launch
+ *    errors only; device-side errors (an out-of-range block id, a pipeline
+ *    wait that ran out) are recorded in a device error word read by
+ *    pa_device_error().
+ *  - dtype: PA_BF16 (bfloat16) or PA_F32 (float32) for q, K/V caches and
+ *    outputs.  Accumulation is always fp32.
+ *  - Cache layout (both K and V): [num_blocks][Hkv][block_size][head_dim],
+ *    contiguous, so one (block, KV head) is block_size*head_dim contiguous
+ *    elements.  Pool base pointers must be 16-byte aligned.
+ *  - GQA: query head h reads KV head h / (Hq / Hkv).
+ *  - Supported shapes: head_dim 64 or 128; Hq/Hkv in {1, 2, 4, 8};
+ *    block_size a power of two in [8, 128].
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *pa_stream_t; /* same type as cudaStream_t */
+
+enum {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,     /* bad argument, shape or (validate mode) metadata */
+    PA_ERR_OOM = 2,         /* block manager: not enough free blocks */
+    PA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    PA_ERR_UNSUPPORTED = 4, /* valid request this build has no kernel for */
+    PA_ERR_DEVICE = 5       /* pa_device_error found a device-side error */
+};
+
+enum { PA_BF16 = 0, PA_F32 = 1 };
+
+/* device error word bits (pa_device_error) */
+enum {
+    PA_DEVERR_BAD_BLOCK = 1, /* a block-table entry was outside [0, num_blocks) */
+    PA_DEVERR_TIMEOUT = 2    /* a bounded pipeline wait ran out; output invalid */
+};
+
+/* Message of the last failing call on this thread ("" if none). */
+const char *pa_last_error_string(void);
+
+/* Library ABI version (incremented on any signature change). */
+int pa_version(void);
+
+/*
+ * Validate mode (off by default).  When on, every op first copies its
+ * metadata (slot_mapping, block_table, context_lens, copy pairs) to the host
+ * and checks it: slots and block ids inside the pool, no duplicate slots in
+ * one reshape call, copy pairs disjoint, context lengths in (0, table
+ * capacity].  It synchronizes the stream, so it is for debugging and tests.
+ */
+int pa_set_validate(int on);
+
+/*
+ * Read (and, if clear != 0, reset) the device error word of the current
+ * device.  Synchronizes the stream.  *bits receives PA_DEVERR_* bits.
+ * Returns PA_ERR_DEVICE if any bit was set, else PA_OK.
+ */
+int pa_device_error(int *bits, int clear, pa_stream_t stream);
+
+/*
+ * pa_reshape_and_cache -- store the new tokens' K and V into their slots.
+ * Only the new token's K/V is computed and stored; earlier tokens are read
+ * back from the cache ("KV Cache dan PagedAttention: Apa Fungsinya dan
+ * Mengapa Itu Penting", section "Apa itu KV Cache?").
+ *   k_new, v_new  [T][Hkv][head_dim]               (dtype)
+ *   k_cache, v_cache  pool as above, written in place
+ *   slot_mapping  int64 [T]: slot = physical_block * block_size + offset;
+ *                 a negative slot is padding and is skipped
+ * Effect: k_cache[slot/bs][h][slot%bs][:] = k_new[t][h][:] (same for V), bit
+ * exact.  Duplicate slots in one call are a caller error (undefined which
+ * token wins; PA_ERR_INVALID in validate mode).
+ */
+int pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                         const int64_t *slot_mapping, int64_t T, int64_t num_blocks, int Hkv,
+                         int block_size, int head_dim, int dtype, pa_stream_t stream);
+
+/*
+ * pa_copy_blocks -- copy-on-write support: for each pair (src, dst), physical
+ * block dst of BOTH caches becomes a byte copy of block src ("Apa itu
+ * PagedAttention?", section "Cara kerja PagedAttention", item 3; nalar.dev,
+ * section "Sharing blok dapat menghindari duplikasi state KV").
+ *   pairs  int64 [n][2] device array of (src, dst) block ids
+ * No dst may equal any src or another dst in the same call (PA_ERR_INVALID in
+ * validate mode).  Bit exact.
+ */
+int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int64_t n,
+                   int64_t num_blocks, int Hkv, int block_size, int head_dim, int dtype,
+                   pa_stream_t stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of fp32 workspace pa_decode needs for
+ * split-KV partials (0 when no sequence can span more than one partition).
+ * partition_tokens as for pa_decode (0 = library default).
+ */
+int pa_decode_workspace_size(int B, int Hq, int head_dim, int max_blocks_per_seq,
+                             int block_size, int partition_tokens, size_t *bytes);
+
+/*
+ * pa_decode -- paged decode attention: one query token per sequence.
+ * For sequence b with context length L = context_lens[b] (the newest token,
+ * already stored by pa_reshape_and_cache, included) and query head h:
+ *   o[b][h] = sum_{j<L} exp(s_j - max s) V_b[j][h/g] / sum_j exp(s_j - max s),
+ *   s_j = scale * (q[b][h] . K_b[j][h/g])
+ * where token j of sequence b lives in physical block
+ * block_table[b][j / block_size] at offset j % block_size.  The sum over j
+ * is split into partitions of partition_tokens tokens whose partial
+ * (max, sum, weighted values) are merged by log-sum-exp when L exceeds one
+ * partition.  The result depends only on the logical token order, never on
+ * where blocks sit in the pool (bit-identical under any placement).
+ *   out, q        [B][Hq][head_dim]                    (dtype)
+ *   block_table   int32 [B][max_blocks_per_seq]
+ *   context_lens  int32 [B], each in [1, max_blocks_per_seq*block_size]
+ *   partition_tokens  0 = default (512), or a positive multiple of both 32
+ *                 and block_size
+ *   workspace     device buffer of at least pa_decode_workspace_size bytes
+ *                 (may be NULL when that size is 0)
+ */
+int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_table, int max_blocks_per_seq, const int32_t *context_lens,
+              int B, int Hq, int Hkv, int head_dim, int block_size, int64_t num_blocks,
+              float scale, int partition_tokens, void *workspace, size_t workspace_bytes,
+              int dtype, pa_stream_t stream);
+
+/*
+ * pa_prefill_chunk -- chunked prefill over paged context ("Melihat Lebih
+ * Dalam vLLM v0.7", section "Blueprint Arsitektur 3: Chunked Prefill": a long
+ * prompt is cut into chunks of e.g. 512 tokens and run next to decode).
+ * Request r has n_r = query_start[r+1]-query_start[r] new query tokens whose
+ * K/V are already in the cache; its context length is L_r = context_lens[r]
+ * (prior tokens plus the chunk), so new token i sits at absolute position
+ * P_r + i with P_r = L_r - n_r and attends to positions 0..P_r+i (causal).
+ *   out, q        [query_start[R]][Hq][head_dim]       (bf16 only)
+ *   query_start   int32 [R+1] prefix sum of new-token counts
+ *   context_lens  int32 [R]
+ *   max_query_len host int >= every n_r (sizes the grid)
+ */
+int pa_prefill_chunk(void *out, const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_table, int max_blocks_per_seq,
+                     const int32_t *query_start, const int32_t *context_lens, int R,
+                     int max_query_len, int Hq, int Hkv, int head_dim, int block_size,
+                     int64_t num_blocks, float scale, int dtype, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Host block manager (opaque handle; C++ behind the C ABI).
+ *
+ * Free list, per-block reference counts, sequences as lists of physical
+ * blocks, fork (prefix sharing), append with copy-on-write.  A new block is
+ * taken only when a sequence crosses a block boundary ("Melihat Lebih Dalam
+ * vLLM v0.7", section "Blueprint Arsitektur 2", item "Alokasi On-Demand");
+ * shared blocks stay shared while unchanged and the branch that writes into a
+ * shared, partly filled last block gets a copy first (copy-on-write).  A full
+ * shared block needs no copy.  Sharing is explicit (fork), never by content.
+ *
+ * Free-list order: a stack; initially 0..num_blocks-1, or a Fisher-Yates
+ * shuffle driven by SplitMix64(seed) when seed != 0; allocation takes the next
+ * block of that order and freed blocks are reused first.
+ * Every failing call leaves the manager unchanged.  Not thread safe.
+ * ---------------------------------------------------------------------- */
+typedef struct pa_bm pa_bm;
+
+int pa_bm_create(int64_t num_blocks, int block_size, uint64_t seed, pa_bm **out);
+void pa_bm_destroy(pa_bm *bm);
+
+/* New sequence seq holding n_tokens prompt tokens; slots (host int64
+ * [n_tokens], may be NULL) receives their slots.  PA_ERR_INVALID if seq
+ * exists, PA_ERR_OOM if too few free blocks. */
+int pa_bm_add_seq(pa_bm *bm, int64_t seq, int64_t n_tokens, int64_t *slots);
+
+/* child shares all of parent's blocks (refcount + 1 each). */
+int pa_bm_fork(pa_bm *bm, int64_t parent, int64_t child);
+
+/* One new token for seq: *slot receives its slot; (*cow_src, *cow_dst) the
+ * block copy to run before writing it, or (-1, -1). */
+int pa_bm_append(pa_bm *bm, int64_t seq, int64_t *slot, int64_t *cow_src, int64_t *cow_dst);
+
+/* n new tokens (host int64 slots[n]); at most one copy-on-write pair (only
+ * the first new token can hit a shared block). */
+int pa_bm_append_n(pa_bm *bm, int64_t seq, int64_t n, int64_t *slots, int64_t *cow_src,
+                   int64_t *cow_dst);
+
+/* Drop seq; blocks whose refcount reaches 0 return to the free list. */
+int pa_bm_free_seq(pa_bm *bm, int64_t seq);
+
+/* Host int32 out[n][max_blocks]: the block table rows of seqs[0..n), padded
+ * with 0.  PA_ERR_INVALID if a sequence is unknown or has more blocks. */
+int pa_bm_block_table(const pa_bm *bm, const int64_t *seqs, int n, int32_t *out,
+                      int max_blocks);
+
+int pa_bm_seq_len(const pa_bm *bm, int64_t seq, int64_t *len);
+/* Physical blocks of seq in logical order: out[cap], *n = number of blocks. */
+int pa_bm_seq_blocks(const pa_bm *bm, int64_t seq, int32_t *out, int64_t cap, int64_t *n);
+int pa_bm_refcount(const pa_bm *bm, int64_t block, int *refcount);
+int64_t pa_bm_num_free(const pa_bm *bm);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

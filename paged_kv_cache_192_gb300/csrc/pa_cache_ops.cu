@@ -1,0 +1,155 @@
+// reshape_and_cache and copy_blocks: the bit-exact data movement of the
+// paged KV cache.  Both are HBM-bound copies done in 16-byte vectors.
+#include <algorithm>
+#include <unordered_set>
+#include <vector>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace {
+
+// One thread per 16-byte chunk of one (token, KV head) row.  Source rows are
+// contiguous ([T][Hkv][row]); the destination of row (t, h) is
+// [slot / bs][h][slot % bs] in the pool.  Negative slots are padding.
+__global__ void __launch_bounds__(256) reshape_and_cache_kernel(
+    const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, uint4 *__restrict__ k_cache,
+    uint4 *__restrict__ v_cache, const int64_t *__restrict__ slots, int64_t total, int Hkv,
+    int bs_log2, int chunks, int64_t num_blocks, int *err) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += stride) {
+        const int64_t row = i / chunks;
+        const int c = static_cast<int>(i - row * chunks);
+        const int64_t t = row / Hkv;
+        const int h = static_cast<int>(row - t * Hkv);
+        const int64_t slot = __ldg(slots + t);
+        if (slot < 0) continue;
+        const int64_t blk = slot >> bs_log2;
+        const int64_t off = slot & ((1ll << bs_log2) - 1);
+        if (blk >= num_blocks) {
+            pa::record_error(err, PA_DEVERR_BAD_BLOCK);
+            continue;
+        }
+        const int64_t dst = (((blk * Hkv + h) << bs_log2) + off) * chunks + c;
+        k_cache[dst] = __ldg(k_new + i);
+        v_cache[dst] = __ldg(v_new + i);
+    }
+}
+
+// blockIdx.x = pair, blockIdx.y = cache (0: K, 1: V).  Each CTA copies one
+// whole physical block of one cache.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ k_cache,
+                                                          uint4 *__restrict__ v_cache,
+                                                          const int64_t *__restrict__ pairs,
+                                                          int64_t chunks_per_block,
+                                                          int64_t num_blocks, int *err) {
+    const int64_t p = blockIdx.x;
+    const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+    if (src < 0 || dst < 0 || src >= num_blocks || dst >= num_blocks) {
+        if (threadIdx.x == 0) pa::record_error(err, PA_DEVERR_BAD_BLOCK);
+        return;
+    }
+    uint4 *base = blockIdx.y ? v_cache : k_cache;
+    const uint4 *s = base + src * chunks_per_block;
+    uint4 *d = base + dst * chunks_per_block;
+    for (int64_t i = threadIdx.x; i < chunks_per_block; i += blockDim.x) d[i] = s[i];
+}
+
+int log2_int(int x) {
+    int l = 0;
+    while ((1 << l) < x) ++l;
+    return l;
+}
+
+int grid_for(int64_t work, int threads) {
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t want = (work + threads - 1) / threads;
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sms) * 16)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                         const int64_t *slot_mapping, int64_t T, int64_t num_blocks, int Hkv,
+                         int block_size, int head_dim, int dtype, pa_stream_t stream) {
+    pa::clear_error();
+    const size_t es = pa::dtype_size(dtype);
+    if (!es) return pa::fail(PA_ERR_INVALID, "reshape_and_cache: bad dtype %d", dtype);
+    if (T < 0 || num_blocks <= 0 || Hkv <= 0 || head_dim <= 0)
+        return pa::fail(PA_ERR_INVALID, "reshape_and_cache: bad sizes");
+    if (!pa::pow2_in(block_size, 1, 1024))
+        return pa::fail(PA_ERR_INVALID, "reshape_and_cache: block_size must be a power of two");
+    if ((head_dim * es) % 16)
+        return pa::fail(PA_ERR_INVALID, "reshape_and_cache: row bytes must be a multiple of 16");
+    if (T == 0) return PA_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping)
+        return pa::fail(PA_ERR_INVALID, "reshape_and_cache: NULL pointer");
+    if (!pa::aligned16(k_new) || !pa::aligned16(v_new) || !pa::aligned16(k_cache) ||
+        !pa::aligned16(v_cache))
+        return pa::fail(PA_ERR_INVALID, "reshape_and_cache: pointers must be 16-byte aligned");
+    if (pa::validate_on()) {
+        std::vector<int64_t> s(T);
+        if (int rc = pa::fetch(s.data(), slot_mapping, T * sizeof(int64_t), stream)) return rc;
+        std::unordered_set<int64_t> seen;
+        for (int64_t t = 0; t < T; ++t) {
+            if (s[t] < 0) continue;
+            if (s[t] >= num_blocks * block_size)
+                return pa::fail(PA_ERR_INVALID, "validate: slot %lld of token %lld out of pool",
+                                (long long)s[t], (long long)t);
+            if (!seen.insert(s[t]).second)
+                return pa::fail(PA_ERR_INVALID, "validate: duplicate slot %lld", (long long)s[t]);
+        }
+    }
+    const int chunks = static_cast<int>(head_dim * es / 16);
+    const int64_t total = T * Hkv * chunks;
+    reshape_and_cache_kernel<<<grid_for(total, 256), 256, 0, stream>>>(
+        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, total, Hkv,
+        log2_int(block_size), chunks, num_blocks, pa::device_error_word());
+    return pa::check_launch("reshape_and_cache launch");
+}
+
+int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int64_t n,
+                   int64_t num_blocks, int Hkv, int block_size, int head_dim, int dtype,
+                   pa_stream_t stream) {
+    pa::clear_error();
+    const size_t es = pa::dtype_size(dtype);
+    if (!es) return pa::fail(PA_ERR_INVALID, "copy_blocks: bad dtype %d", dtype);
+    if (n < 0 || num_blocks <= 0 || Hkv <= 0 || block_size <= 0 || head_dim <= 0)
+        return pa::fail(PA_ERR_INVALID, "copy_blocks: bad sizes");
+    const size_t block_bytes = size_t(Hkv) * block_size * head_dim * es;
+    if (block_bytes % 16) return pa::fail(PA_ERR_INVALID, "copy_blocks: block bytes % 16 != 0");
+    if (n == 0) return PA_OK;
+    if (!k_cache || !v_cache || !pairs) return pa::fail(PA_ERR_INVALID, "copy_blocks: NULL");
+    if (!pa::aligned16(k_cache) || !pa::aligned16(v_cache))
+        return pa::fail(PA_ERR_INVALID, "copy_blocks: pools must be 16-byte aligned");
+    if (n > 0x7fffffff) return pa::fail(PA_ERR_INVALID, "copy_blocks: too many pairs");
+    if (pa::validate_on()) {
+        std::vector<int64_t> p(2 * n);
+        if (int rc = pa::fetch(p.data(), pairs, 2 * n * sizeof(int64_t), stream)) return rc;
+        std::unordered_set<int64_t> srcs, dsts;
+        for (int64_t i = 0; i < n; ++i) {
+            for (int j = 0; j < 2; ++j)
+                if (p[2 * i + j] < 0 || p[2 * i + j] >= num_blocks)
+                    return pa::fail(PA_ERR_INVALID, "validate: pair %lld outside the pool",
+                                    (long long)i);
+            srcs.insert(p[2 * i]);
+            if (!dsts.insert(p[2 * i + 1]).second)
+                return pa::fail(PA_ERR_INVALID, "validate: duplicate destination block");
+        }
+        for (int64_t d : dsts)
+            if (srcs.count(d)) return pa::fail(PA_ERR_INVALID, "validate: dst is also a src");
+    }
+    dim3 grid(static_cast<unsigned>(n), 2);
+    copy_blocks_kernel<<<grid, 256, 0, stream>>>(
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), pairs,
+        static_cast<int64_t>(block_bytes / 16), num_blocks, pa::device_error_word());
+    return pa::check_launch("copy_blocks launch");
+}
+
+}  // extern "C"

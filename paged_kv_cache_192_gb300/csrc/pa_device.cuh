@@ -1,0 +1,132 @@
+// Device-side helpers: bf16 unpacking, packed fp32 FMA, mbarriers and
+// bulk (TMA) copies, written as inline PTX for sm_103a.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pa.h"
+
+namespace pa {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---- bf16 <-> fp32 -------------------------------------------------------
+// A 32-bit word holds two bf16 values, element 0 in the low half.  Widening a
+// bf16 to fp32 is a 16-bit left shift of its bit pattern (exact).
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+template <typename T> struct Elem;
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int kPerChunk = 8;  // elements per 16-byte chunk
+    // Unpack one 16-byte chunk into 8 floats (as 4 pairs).
+    __device__ __forceinline__ static void unpack(const uint4 &c, float2 (&f)[4]) {
+        f[0] = bf16x2_to_float2(c.x);
+        f[1] = bf16x2_to_float2(c.y);
+        f[2] = bf16x2_to_float2(c.z);
+        f[3] = bf16x2_to_float2(c.w);
+    }
+    __device__ __forceinline__ static void store(__nv_bfloat16 *p, float x) {
+        *p = __float2bfloat16_rn(x);
+    }
+};
+template <> struct Elem<float> {
+    static constexpr int kPerChunk = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &c, float2 (&f)[2]) {
+        f[0] = make_float2(__uint_as_float(c.x), __uint_as_float(c.y));
+        f[1] = make_float2(__uint_as_float(c.z), __uint_as_float(c.w));
+    }
+    __device__ __forceinline__ static void store(float *p, float x) { *p = x; }
+};
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    return __ffma2_rn(a, b, c);
+}
+
+// ---- shared-memory addressing --------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// ---- mbarrier ----------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) writes to the same buffer.
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of `bar` to complete, for at most ~kWaitNs.
+// Returns false when the limit ran out (the caller records an error and
+// stops).  No wait in this library is unbounded.
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitNs) return false;
+    }
+}
+
+// Bulk global->shared copy (non-tensor TMA) completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void record_error(int *word, int bits) {
+    if (word) atomicOr(word, bits);
+}
+
+}  // namespace pa

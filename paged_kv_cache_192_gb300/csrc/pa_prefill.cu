@@ -1,0 +1,392 @@
+// Chunked prefill over a paged KV cache (bf16), tensor-core tiles.
+//
+// What it computes ("Melihat Lebih Dalam vLLM v0.7", section "Blueprint
+// Arsitektur 3: Chunked Prefill"): a prompt is cut into chunks (e.g. 512
+// tokens) that run in the same step as decodes.  New token i of request r sits
+// at absolute position P_r + i and attends causally to positions 0..P_r+i of
+// its request, the prior context and the chunk itself, all read through the
+// block table (nalar.dev, section "Kernel attention harus mengikuti block
+// table").  Prefill is the compute-bound phase (same page), so QK^T and PV run
+// as dense bf16 tiles on the tensor cores with fp32 accumulation.
+//
+// Layout of the work: one CTA of 4 warps per (request, KV head, 64-row query
+// tile); a row is one (query token, query head) pair, so the GQ heads that
+// share a KV head share every K/V tile (GQA packed into M).  K/V tiles of 64
+// tokens are gathered block by block into swizzled shared memory with
+// cp.async (double-buffered); online softmax in the log2 domain.
+#include <cmath>
+#include <vector>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace {
+
+constexpr int kRows = 64;   // query rows (token, head) per CTA
+constexpr int kKT = 64;     // KV tokens per tile
+constexpr int kThreads = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct PrefillParams {
+    __nv_bfloat16 *out;
+    const __nv_bfloat16 *q;
+    const uint8_t *k_cache;
+    const uint8_t *v_cache;
+    const int32_t *block_table;
+    const int32_t *query_start;
+    const int32_t *context_lens;
+    int *err;
+    int64_t num_blocks;
+    int R, Hq, Hkv, bs, bs_log2, MB;
+    float qscale;
+};
+
+// Swizzled address of 16-byte chunk `c` of row `r` in a tile of rows of
+// `CH` chunks: chunk positions are XORed with the row's low 3 bits so that
+// ldmatrix reads of 8 consecutive rows hit 8 different bank groups.
+template <int CH>
+__device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c) {
+    return base + r * (CH * 16) + ((c ^ (r & 7)) * 16);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
+    const int n = valid ? 16 : 0;  // 0: zero-fill without reading
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                          uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col)
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int D, int GQ>
+__global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParams p) {
+    constexpr int CH = D * 2 / 16;  // 16-byte chunks per row
+    constexpr int KS = D / 16;      // k-steps over head_dim
+    constexpr int NT = kKT / 8;     // score n-tiles per KV tile
+    constexpr int OT = D / 8;       // output n-tiles
+    constexpr int QTOK = kRows / GQ;
+    constexpr int TILE_BYTES = kKT * D * 2;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t sq = pa::smem_u32(smem);
+    const uint32_t sk = sq + kRows * D * 2;       // [2][kKT][D]
+    const uint32_t sv = sk + 2 * TILE_BYTES;      // [2][kKT][D]
+
+    const int qt = blockIdx.x, hk = blockIdx.y, r = blockIdx.z;
+    const int qs = p.query_start[r];
+    const int n = p.query_start[r + 1] - qs;
+    const int t0 = qt * QTOK;
+    if (t0 >= n) return;
+    const int cap = p.MB << p.bs_log2;
+    int L = p.context_lens[r];
+    if (L > cap || L < n) {
+        if (threadIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+        return;
+    }
+    const int P = L - n;
+    const int kv_end = min(L, P + t0 + QTOK);  // last position of this tile + 1
+    const int ntiles = (kv_end + kKT - 1) / kKT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---- Q tile: row m = token (m / GQ), head (m % GQ) ----------------------
+    for (int idx = tid; idx < kRows * CH; idx += kThreads) {
+        const int m = idx / CH, c = idx % CH;
+        const int t = t0 + m / GQ;
+        const bool valid = t < n;
+        const __nv_bfloat16 *src =
+            p.q + (static_cast<size_t>(qs + (valid ? t : 0)) * p.Hq + hk * GQ + m % GQ) * D + c * 8;
+        cp_async16(swz<CH>(sq, m, c), src, valid);
+    }
+    const int32_t *bt = p.block_table + static_cast<size_t>(r) * p.MB;
+    auto load_tile = [&](int it, int buf) {
+        const int j0 = it * kKT;
+        for (int idx = tid; idx < kKT * CH; idx += kThreads) {
+            const int row = idx / CH, c = idx % CH;
+            const int j = j0 + row;
+            const bool valid = j < kv_end;
+            size_t off = 0;
+            if (valid) {
+                int blk = bt[j >> p.bs_log2];
+                if (blk < 0 || blk >= p.num_blocks) {
+                    pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+                    blk = 0;
+                }
+                off = ((static_cast<size_t>(blk) * p.Hkv + hk) * p.bs + (j & (p.bs - 1))) * D * 2 +
+                      c * 16;
+            }
+            cp_async16(swz<CH>(sk + buf * TILE_BYTES, row, c), p.k_cache + off, valid);
+            cp_async16(swz<CH>(sv + buf * TILE_BYTES, row, c), p.v_cache + off, valid);
+        }
+    };
+    load_tile(0, 0);
+    cp_async_commit();
+
+    // This thread's two rows of the warp's 16: g and g+8.
+    const int g = lane >> 2, cq = lane & 3;
+    int pos[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int m = warp * 16 + g + 8 * i;
+        const int t = min(t0 + m / GQ, n - 1);  // rows past the chunk reuse the last row
+        pos[i] = P + t;
+    }
+
+    uint32_t qf[KS][4];
+    float o[OT][4];
+#pragma unroll
+    for (int j = 0; j < OT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+
+    for (int it = 0; it < ntiles; ++it) {
+        const int buf = it & 1;
+        if (it + 1 < ntiles) load_tile(it + 1, buf ^ 1);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        if (it == 0) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int row = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+                const int c = ks * 2 + (lane >> 4);
+                ldsm_x4(swz<CH>(sq, row, c), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+            }
+        }
+        const uint32_t kb = sk + buf * TILE_BYTES, vb = sv + buf * TILE_BYTES;
+        // ---- S = Q K^T (16 x 64 per warp) ----------------------------------------
+        float s[NT][4];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+            for (int j = 0; j < NT; j += 2) {
+                const int row = j * 8 + (lane & 7) + 8 * (lane >> 4);
+                const int c = ks * 2 + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(swz<CH>(kb, row, c), b0, b1, b2, b3);
+                mma_bf16(s[j], qf[ks], b0, b1);
+                mma_bf16(s[j + 1], qf[ks], b2, b3);
+            }
+        }
+        // ---- scale, causal mask, online softmax ---------------------------------
+        const int j0 = it * kKT;
+        float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int col = j0 + j * 8 + cq * 2 + (e & 1);
+                const int ri = e >> 1;
+                float v = s[j][e] * p.qscale;
+                v = col <= pos[ri] ? v : -INFINITY;
+                s[j][e] = v;
+                tmax[ri] = fmaxf(tmax[ri], v);
+            }
+        float alpha[2];
+#pragma unroll
+        for (int ri = 0; ri < 2; ++ri) {
+            tmax[ri] = fmaxf(tmax[ri], __shfl_xor_sync(pa::kFull, tmax[ri], 1));
+            tmax[ri] = fmaxf(tmax[ri], __shfl_xor_sync(pa::kFull, tmax[ri], 2));
+            const float mnew = fmaxf(mrow[ri], tmax[ri]);
+            alpha[ri] = mrow[ri] == -INFINITY ? 0.f : fast_exp2(mrow[ri] - mnew);
+            mrow[ri] = mnew;
+        }
+        float rsum[2] = {0.f, 0.f};
+        uint32_t pf[NT / 2][4];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const float p0 = fast_exp2(s[j][0] - mrow[0]);
+            const float p1 = fast_exp2(s[j][1] - mrow[0]);
+            const float p2 = fast_exp2(s[j][2] - mrow[1]);
+            const float p3 = fast_exp2(s[j][3] - mrow[1]);
+            rsum[0] += p0 + p1;
+            rsum[1] += p2 + p3;
+            pf[j / 2][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
+            pf[j / 2][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
+        }
+#pragma unroll
+        for (int ri = 0; ri < 2; ++ri) lrow[ri] = lrow[ri] * alpha[ri] + rsum[ri];
+#pragma unroll
+        for (int j = 0; j < OT; ++j) {
+            o[j][0] *= alpha[0];
+            o[j][1] *= alpha[0];
+            o[j][2] *= alpha[1];
+            o[j][3] *= alpha[1];
+        }
+        // ---- O += P V --------------------------------------------------------------
+#pragma unroll
+        for (int kk = 0; kk < kKT / 16; ++kk) {
+#pragma unroll
+            for (int j = 0; j < OT; j += 2) {
+                const int row = kk * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+                const int c = j + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(swz<CH>(vb, row, c), b0, b1, b2, b3);
+                mma_bf16(o[j], pf[kk], b0, b1);
+                mma_bf16(o[j + 1], pf[kk], b2, b3);
+            }
+        }
+        __syncthreads();  // buffer `buf` is refilled two iterations on
+    }
+    cp_async_wait<0>();
+
+    // ---- normalise and store ------------------------------------------------------
+#pragma unroll
+    for (int ri = 0; ri < 2; ++ri) {
+        lrow[ri] += __shfl_xor_sync(pa::kFull, lrow[ri], 1);
+        lrow[ri] += __shfl_xor_sync(pa::kFull, lrow[ri], 2);
+    }
+#pragma unroll
+    for (int ri = 0; ri < 2; ++ri) {
+        const int m = warp * 16 + g + 8 * ri;
+        const int t = t0 + m / GQ;
+        if (t >= n) continue;
+        const float inv = 1.f / lrow[ri];
+        __nv_bfloat16 *dst = p.out + (static_cast<size_t>(qs + t) * p.Hq + hk * GQ + m % GQ) * D;
+#pragma unroll
+        for (int j = 0; j < OT; ++j) {
+            const uint32_t v = pack_bf16(o[j][2 * ri] * inv, o[j][2 * ri + 1] * inv);
+            *reinterpret_cast<uint32_t *>(dst + j * 8 + cq * 2) = v;
+        }
+    }
+}
+
+int log2_int(int x) {
+    int l = 0;
+    while ((1 << l) < x) ++l;
+    return l;
+}
+
+template <int D, int GQ>
+int launch(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
+    const size_t smem = kRows * D * 2 + 4 * kKT * D * 2;
+    auto kern = prefill_kernel<D, GQ>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return pa::cuda_fail(e, "prefill: shared memory attribute");
+    constexpr int qtok = kRows / GQ;
+    dim3 grid((max_query_len + qtok - 1) / qtok, p.Hkv, p.R);
+    kern<<<grid, kThreads, smem, stream>>>(p);
+    return pa::check_launch("prefill launch");
+}
+
+template <int D>
+int dispatch_gq(int gq, const PrefillParams &p, int mq, cudaStream_t s) {
+    switch (gq) {
+        case 1: return launch<D, 1>(p, mq, s);
+        case 2: return launch<D, 2>(p, mq, s);
+        case 4: return launch<D, 4>(p, mq, s);
+        case 8: return launch<D, 8>(p, mq, s);
+        default: return pa::fail(PA_ERR_UNSUPPORTED, "prefill: Hq/Hkv=%d unsupported", gq);
+    }
+}
+
+}  // namespace
+
+extern "C" int pa_prefill_chunk(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *block_table, int max_blocks_per_seq,
+                                const int32_t *query_start, const int32_t *context_lens, int R,
+                                int max_query_len, int Hq, int Hkv, int head_dim, int block_size,
+                                int64_t num_blocks, float scale, int dtype, pa_stream_t stream) {
+    pa::clear_error();
+    if (dtype != PA_BF16)
+        return pa::fail(PA_ERR_UNSUPPORTED, "prefill: only bf16 is supported (dtype %d)", dtype);
+    if (R < 0 || R > 65535 || Hq <= 0 || Hkv <= 0 || Hkv > 65535 || Hq % Hkv ||
+        max_query_len < 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
+        return pa::fail(PA_ERR_INVALID, "prefill: bad sizes");
+    if (head_dim != 64 && head_dim != 128)
+        return pa::fail(PA_ERR_UNSUPPORTED, "prefill: head_dim %d unsupported", head_dim);
+    if (Hq / Hkv != 1 && Hq / Hkv != 2 && Hq / Hkv != 4 && Hq / Hkv != 8)
+        return pa::fail(PA_ERR_UNSUPPORTED, "prefill: Hq/Hkv=%d unsupported", Hq / Hkv);
+    if (!pa::pow2_in(block_size, 8, 128))
+        return pa::fail(PA_ERR_UNSUPPORTED, "prefill: block_size %d unsupported", block_size);
+    if (int64_t(max_blocks_per_seq) * block_size > (int64_t(1) << 30))
+        return pa::fail(PA_ERR_INVALID, "prefill: table capacity too large");
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return pa::fail(PA_ERR_INVALID, "prefill: scale must be positive and finite");
+    if (R == 0 || max_query_len == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_table || !query_start || !context_lens)
+        return pa::fail(PA_ERR_INVALID, "prefill: NULL pointer");
+    if (!pa::aligned16(q) || !pa::aligned16(out) || !pa::aligned16(k_cache) ||
+        !pa::aligned16(v_cache))
+        return pa::fail(PA_ERR_INVALID, "prefill: tensors must be 16-byte aligned");
+    if (pa::validate_on()) {
+        std::vector<int32_t> qsv(R + 1), lens(R), table(size_t(R) * max_blocks_per_seq);
+        if (int rc = pa::fetch(qsv.data(), query_start, (R + 1) * sizeof(int32_t), stream))
+            return rc;
+        if (int rc = pa::fetch(lens.data(), context_lens, R * sizeof(int32_t), stream)) return rc;
+        if (int rc = pa::fetch(table.data(), block_table, table.size() * sizeof(int32_t), stream))
+            return rc;
+        const int64_t cap = int64_t(max_blocks_per_seq) * block_size;
+        for (int r = 0; r < R; ++r) {
+            const int nr = qsv[r + 1] - qsv[r];
+            if (nr < 0 || nr > max_query_len)
+                return pa::fail(PA_ERR_INVALID, "validate: request %d has %d new tokens", r, nr);
+            if (lens[r] < nr || lens[r] > cap)
+                return pa::fail(PA_ERR_INVALID, "validate: context_lens[%d]=%d", r, lens[r]);
+            const int nb = (lens[r] + block_size - 1) / block_size;
+            for (int i = 0; i < nb; ++i) {
+                const int32_t v = table[size_t(r) * max_blocks_per_seq + i];
+                if (v < 0 || v >= num_blocks)
+                    return pa::fail(PA_ERR_INVALID, "validate: block_table[%d][%d]=%d", r, i, v);
+            }
+        }
+    }
+    PrefillParams p{};
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k_cache = static_cast<const uint8_t *>(k_cache);
+    p.v_cache = static_cast<const uint8_t *>(v_cache);
+    p.block_table = block_table;
+    p.query_start = query_start;
+    p.context_lens = context_lens;
+    p.err = pa::device_error_word();
+    p.num_blocks = num_blocks;
+    p.R = R;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.bs = block_size;
+    p.bs_log2 = log2_int(block_size);
+    p.MB = max_blocks_per_seq;
+    p.qscale = scale * kLog2e;
+    const int gq = Hq / Hkv;
+    return head_dim == 128 ? dispatch_gq<128>(gq, p, max_query_len, stream)
+                           : dispatch_gq<64>(gq, p, max_query_len, stream);
+}

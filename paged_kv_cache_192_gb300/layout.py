@@ -1,0 +1,57 @@
+"""Host-side helpers around the paged layout: slot arithmetic, KV sizing and
+setting up device pools from logical K/V through the library's own
+reshape_and_cache.
+
+Pool layout (both K and V): [num_blocks][Hkv][block_size][head_dim].
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import ops
+
+
+def slots_for(table_row, positions, block_size):
+    """Slots of the given logical positions of one sequence:
+    physical block table_row[j // bs] times bs, plus j % bs ("PagedAttention:
+    memetakan blok KV logis ke memori fisik tidak kontigu", section "Urutan
+    logis dipisahkan dari penempatan fisik")."""
+    pos = np.asarray(positions, dtype=np.int64)
+    row = np.asarray(table_row, dtype=np.int64)
+    return row[pos // block_size] * block_size + pos % block_size
+
+
+def kv_bytes_per_token(layers, kv_heads, head_dim, elem_bytes):
+    """Bytes of K and V one token keeps across all layers."""
+    return 2 * layers * kv_heads * head_dim * elem_bytes
+
+
+def alloc_pools(num_blocks, Hkv, block_size, head_dim, dtype, device="cuda", poison=True):
+    """K and V pools; poisoned with NaN so that any read of a slot nobody
+    wrote shows up in the output."""
+    shape = (num_blocks, Hkv, block_size, head_dim)
+    if poison:
+        k = torch.full(shape, float("nan"), dtype=dtype, device=device)
+        v = torch.full(shape, float("nan"), dtype=dtype, device=device)
+    else:
+        k = torch.empty(shape, dtype=dtype, device=device)
+        v = torch.empty(shape, dtype=dtype, device=device)
+    return k, v
+
+
+def all_slots(table, lens, block_size):
+    """Slots of every token of every sequence, stacked in logical order."""
+    parts = [slots_for(table[s], np.arange(int(L)), block_size) for s, L in enumerate(lens)]
+    return np.concatenate(parts) if parts else np.zeros(0, np.int64)
+
+
+def fill_pools(k_cache, v_cache, k_logical, v_logical, table, lens, block_size, chunk=1 << 20):
+    """Write stacked logical K/V [sum L][Hkv][d] into the pools at the slots the
+    block table gives, with pa_reshape_and_cache."""
+    slots = torch.from_numpy(all_slots(table, lens, block_size)).to(k_cache.device)
+    for i in range(0, slots.numel(), chunk):
+        sl = slice(i, i + chunk)
+        ops.reshape_and_cache(k_logical[sl].to(k_cache.device).contiguous(),
+                              v_logical[sl].to(k_cache.device).contiguous(), k_cache, v_cache,
+                              slots[sl].contiguous())

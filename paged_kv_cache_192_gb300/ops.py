@@ -1,0 +1,125 @@
+"""Torch-facing binding of the paged-attention ops (argument marshalling only).
+
+Every function passes device pointers, sizes and the current CUDA stream to
+the C ABI of include/pa.h; all work runs in the library's sm_103a kernels.
+Tensors must be contiguous CUDA tensors.  Outputs and workspaces that the
+caller does not pass are allocated here with torch (the library itself never
+allocates).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+from ._lib import PA_BF16, PA_F32, check, lib
+
+_DTYPES = {torch.bfloat16: PA_BF16, torch.float32: PA_F32}
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return _DTYPES[t.dtype]
+
+
+def _cuda(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def set_validate(on: bool):
+    check(lib().pa_set_validate(int(bool(on))))
+
+
+def device_error(clear: bool = True, stream=None) -> int:
+    """Device error bits (PA_DEVERR_*) recorded by kernels; 0 if none."""
+    bits = ctypes.c_int(0)
+    rc = lib().pa_device_error(ctypes.byref(bits), int(clear), _stream(stream))
+    if rc not in (_lib.PA_OK, _lib.PA_ERR_DEVICE):
+        check(rc)
+    return bits.value
+
+
+def reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None):
+    """Store new K/V rows [T][Hkv][d] into their slots of the [NB][Hkv][bs][d] pools."""
+    NB, Hkv, bs, d = k_cache.shape
+    T = k_new.shape[0]
+    assert k_new.shape == (T, Hkv, d) and v_new.shape == k_new.shape
+    assert v_cache.shape == k_cache.shape and slot_mapping.shape == (T,)
+    check(lib().pa_reshape_and_cache(
+        _cuda(k_new, "k_new", k_cache.dtype), _cuda(v_new, "v_new", k_cache.dtype),
+        _cuda(k_cache, "k_cache"), _cuda(v_cache, "v_cache", k_cache.dtype),
+        _cuda(slot_mapping, "slot_mapping", torch.int64), T, NB, Hkv, bs, d, _dt(k_cache),
+        _stream(stream)))
+
+
+def copy_blocks(k_cache, v_cache, pairs, stream=None):
+    """Copy physical blocks pairs[i][0] -> pairs[i][1] of both pools."""
+    NB, Hkv, bs, d = k_cache.shape
+    n = pairs.shape[0] if pairs.numel() else 0
+    check(lib().pa_copy_blocks(
+        _cuda(k_cache, "k_cache"), _cuda(v_cache, "v_cache", k_cache.dtype),
+        _cuda(pairs, "pairs", torch.int64) if n else None, n, NB, Hkv, bs, d, _dt(k_cache),
+        _stream(stream)))
+
+
+def decode_workspace_size(B, Hq, head_dim, max_blocks_per_seq, block_size, partition_tokens=0):
+    out = ctypes.c_size_t(0)
+    check(lib().pa_decode_workspace_size(B, Hq, head_dim, max_blocks_per_seq, block_size,
+                                         partition_tokens, ctypes.byref(out)))
+    return out.value
+
+
+def decode(q, k_cache, v_cache, block_table, context_lens, scale=None, partition_tokens=0,
+           workspace=None, out=None, stream=None):
+    """Paged decode attention; q [B][Hq][d] -> out [B][Hq][d]."""
+    B, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    assert d2 == d and block_table.shape[0] == B and context_lens.shape == (B,)
+    MB = block_table.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    ws_bytes = decode_workspace_size(B, Hq, d, MB, bs, partition_tokens)
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes // 4, dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(lib().pa_decode(
+        _cuda(out, "out", q.dtype), _cuda(q, "q", k_cache.dtype), _cuda(k_cache, "k_cache"),
+        _cuda(v_cache, "v_cache", k_cache.dtype), _cuda(block_table, "block_table", torch.int32),
+        MB, _cuda(context_lens, "context_lens", torch.int32), B, Hq, Hkv, d, bs, NB, scale,
+        partition_tokens, ws_ptr, ws_len, _dt(q), _stream(stream)))
+    return out
+
+
+def prefill_chunk(q, k_cache, v_cache, block_table, query_start, context_lens, max_query_len,
+                  scale=None, out=None, stream=None):
+    """Causal chunked prefill; q [sum n][Hq][d] -> out [sum n][Hq][d] (bf16)."""
+    Tq, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    R = context_lens.shape[0]
+    assert d2 == d and query_start.shape == (R + 1,) and block_table.shape[0] == R
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    check(lib().pa_prefill_chunk(
+        _cuda(out, "out", q.dtype), _cuda(q, "q", k_cache.dtype), _cuda(k_cache, "k_cache"),
+        _cuda(v_cache, "v_cache", k_cache.dtype), _cuda(block_table, "block_table", torch.int32),
+        block_table.shape[1], _cuda(query_start, "query_start", torch.int32),
+        _cuda(context_lens, "context_lens", torch.int32), R, int(max_query_len), Hq, Hkv, d, bs,
+        NB, scale, _dt(q), _stream(stream)))
+    return out

@@ -1,0 +1,100 @@
+"""The C ABI library builds, loads without a GPU, exports every symbol
+include/pa.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_192_gb300 import build
+    build.build()
+    from paged_kv_cache_192_gb300 import _lib
+    return _lib.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path_calls():
+    names = declared_functions()
+    for n in ("pa_reshape_and_cache", "pa_decode", "pa_prefill_chunk", "pa_copy_blocks",
+              "pa_decode_workspace_size", "pa_bm_create", "pa_bm_append", "pa_bm_fork"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from paged_kv_cache_192_gb300._lib import SIGNATURES
+    names = declared_functions()
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in pa.h but not exported"
+    assert set(names) == set(SIGNATURES), "binding signatures must mirror pa.h"
+
+
+def test_version(lib):
+    assert lib.pa_version() == 1
+
+
+def test_workspace_size_host_only(lib):
+    from paged_kv_cache_192_gb300 import ops
+    # 8B-shaped: 64 seqs, 32 heads, d 128, 256 blocks of 16 -> 8 partitions of 512
+    assert ops.decode_workspace_size(64, 32, 128, 256, 16, 512) == 64 * 32 * 8 * 130 * 4
+    # one partition covers every sequence: no workspace
+    assert ops.decode_workspace_size(4, 4, 64, 4, 16, 0) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=7), 1),               # bad dtype
+    (dict(head_dim=96), 4),           # unsupported head_dim
+    (dict(Hq=12, Hkv=8), 1),          # Hq not a multiple of Hkv
+    (dict(Hq=32, Hkv=2), 4),          # group of 16 unsupported
+    (dict(block_size=24), 4),         # not a power of two
+    (dict(partition_tokens=48), 1),   # not a multiple of 32
+    (dict(scale=-1.0), 1),
+])
+def test_decode_rejects_bad_arguments(lib, kw, code):
+    args = dict(out=None, q=None, k=None, v=None, bt=None, MB=4, lens=None, B=1, Hq=4, Hkv=4,
+                head_dim=64, block_size=16, NB=8, scale=0.125, partition_tokens=0, ws=None,
+                ws_bytes=0, dtype=1, stream=None)
+    args.update(kw)
+    rc = lib.pa_decode(args["out"], args["q"], args["k"], args["v"], args["bt"], args["MB"],
+                       args["lens"], args["B"], args["Hq"], args["Hkv"], args["head_dim"],
+                       args["block_size"], args["NB"], args["scale"], args["partition_tokens"],
+                       args["ws"], args["ws_bytes"], args["dtype"], args["stream"])
+    assert rc == code
+    assert lib.pa_last_error_string()
+
+
+def test_null_pointers_rejected(lib):
+    rc = lib.pa_decode(None, None, None, None, None, 4, None, 2, 4, 4, 64, 16, 8, 0.125, 0, None,
+                       0, 1, None)
+    assert rc == 1 and b"NULL" in lib.pa_last_error_string()
+    rc = lib.pa_reshape_and_cache(None, None, None, None, None, 3, 8, 4, 16, 64, 0, None)
+    assert rc == 1
+
+
+def test_empty_calls_are_noops(lib):
+    assert lib.pa_reshape_and_cache(None, None, None, None, None, 0, 8, 4, 16, 64, 0, None) == 0
+    assert lib.pa_copy_blocks(None, None, None, 0, 8, 4, 16, 64, 0, None) == 0
+    assert lib.pa_decode(None, None, None, None, None, 4, None, 0, 4, 4, 64, 16, 8, 0.125, 0,
+                         None, 0, 1, None) == 0
+
+
+def test_prefill_rejects_fp32(lib):
+    rc = lib.pa_prefill_chunk(None, None, None, None, None, 4, None, None, 1, 8, 4, 4, 64, 16, 8,
+                              0.125, 1, None)
+    assert rc == 4
+
+
+def test_misaligned_pool_rejected(lib):
+    rc = lib.pa_reshape_and_cache(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(8),
+                                  ctypes.c_void_p(16), ctypes.c_void_p(16), 1, 8, 4, 16, 64, 0,
+                                  None)
+    assert rc == 1 and b"aligned" in lib.pa_last_error_string()

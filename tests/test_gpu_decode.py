@@ -1,0 +1,181 @@
+"""Paged decode on the GPU against the fp64 oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import compare, device_inputs, oracle_decode
+from paged_kv_cache_192_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_192_gb300 import build
+    build.build()
+
+
+def ops():
+    from paged_kv_cache_192_gb300 import ops as o
+    return o
+
+
+def run(w, partition_tokens=0, seqs=None, poison=True):
+    k_cache, v_cache, table, lens = device_inputs(w, DEV, poison)
+    out = ops().decode(w.q.to(DEV), k_cache, v_cache, table, lens,
+                       partition_tokens=partition_tokens)
+    torch.cuda.synchronize()
+    assert ops().device_error() == 0
+    got = out.double().cpu().numpy()
+    ref = oracle_decode(w, seqs)
+    if seqs is not None:
+        got = got[np.asarray(seqs)]
+    return got, ref, out
+
+
+def test_tiny_fp32_config():
+    """4 sequences {5,17,33,64}, MHA 4 heads, d 64, 16-token blocks, 32-block pool, fp32."""
+    w = synth.decode_workload("tiny", seed=0)
+    assert w.num_blocks == 32 and list(w.lens) == [5, 17, 33, 64]
+    got, ref, _ = run(w)
+    compare(got, ref, torch.float32, "tiny")
+
+
+def test_8b_config_full_size():
+    """Llama-3-8B-shaped: 64 sequences, L ~ U[128,4096], 32/8 heads, d 128, bf16,
+    shuffled 1.2x pool; every output element against the oracle."""
+    w = synth.decode_workload("8b", seed=0)
+    got, ref, _ = run(w)
+    compare(got, ref, torch.bfloat16, "8b")
+
+
+def test_70b_config_full_size_sampled():
+    """Llama-3-70B-shaped long context (L ~ U[16k,32k], 64/8 heads, 32-token
+    blocks, 512-token partitions); the GPU runs the full batch, the oracle
+    checks 3 seeded sequences element by element."""
+    w = synth.decode_workload("70b", seed=0)
+    seqs = synth.sample_indices(w.B, 3, seed=0)
+    got, ref, _ = run(w, partition_tokens=512, seqs=seqs)
+    compare(got, ref, torch.bfloat16, "70b")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4), (8, 2), (16, 2)])
+@pytest.mark.parametrize("bs", [8, 16, 32, 64])
+def test_shapes_ragged(dtype, d, Hq, Hkv, bs):
+    """Ragged lengths around tile, block and partition edges; 64-token
+    partitions so that long sequences split and merge."""
+    lens = [1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 300]
+    w = synth.decode_workload("8b", seed=3, lens=lens, Hq=Hq, Hkv=Hkv, d=d, bs=bs, dtype=dtype)
+    got, ref, _ = run(w, partition_tokens=max(64, bs))
+    compare(got, ref, dtype, f"ragged d{d} {Hq}/{Hkv} bs{bs}")
+
+
+def test_placement_invariance_bit_identical():
+    """Two different physical placements of the same logical K/V give
+    bit-identical outputs (the reduction order follows logical positions)."""
+    w1 = synth.decode_workload("8b", seed=5, B=16)
+    w2 = synth.decode_workload("8b", seed=5, B=16)
+    rng = np.random.default_rng(99)
+    perm = rng.permutation(w2.num_blocks).astype(np.int32)
+    w2.table = perm[w1.table]
+    _, _, o1 = run(w1, seqs=[0])
+    _, _, o2 = run(w2, seqs=[0])
+    assert torch.equal(o1, o2)
+
+
+def test_split_matches_unsplit():
+    w = synth.decode_workload("8b", seed=6, B=8)
+    _, ref, o_split = run(w, partition_tokens=128)
+    _, _, o_whole = run(w, partition_tokens=4096)
+    compare(o_split.double().cpu().numpy(), ref, torch.bfloat16, "split")
+    compare(o_whole.double().cpu().numpy(), ref, torch.bfloat16, "whole")
+
+
+def test_single_token_returns_v0_exactly():
+    w = synth.decode_workload("8b", seed=7, lens=[1, 1, 1])
+    _, _, out = run(w)
+    offs = w.kv_offsets
+    g = w.Hq // w.Hkv
+    for s in range(3):
+        v0 = w.v[offs[s]].repeat_interleave(g, dim=0)
+        assert torch.equal(out[s].cpu(), v0)
+
+
+def test_zero_query_is_mean_of_values():
+    w = synth.decode_workload("8b", seed=8, lens=[700, 33])
+    w.q.zero_()
+    got, ref, _ = run(w)
+    compare(got, ref, torch.bfloat16, "q=0")
+    offs = w.kv_offsets
+    mean = w.v[offs[1]:offs[1] + 33].double().mean(0).repeat_interleave(4, 0).numpy()
+    compare(got[1], mean, torch.bfloat16, "q=0 mean")
+
+
+def test_dominant_key_selects_its_value():
+    """A key with a score far above the rest (also forces the lazy rescale path
+    mid-sequence)."""
+    w = synth.decode_workload("8b", seed=9, lens=[1000])
+    w.k[600] = w.q[0, :: w.Hq // w.Hkv].to(w.k.dtype) * 40.0
+    got, ref, _ = run(w)
+    compare(got, ref, torch.bfloat16, "dominant")
+
+
+def test_bad_block_id_is_recorded_not_faulted():
+    """An out-of-pool table entry is replaced by block 0 in the kernel and
+    reported in the device error word (no out-of-bounds access)."""
+    from paged_kv_cache_192_gb300._lib import PA_DEVERR_BAD_BLOCK
+    w = synth.decode_workload("8b", seed=10, lens=[40])
+    k_cache, v_cache, table, lens = device_inputs(w, DEV)
+    table[0, 1] = w.num_blocks + 5
+    ops().device_error(clear=True)
+    ops().decode(w.q.to(DEV), k_cache, v_cache, table, lens)
+    torch.cuda.synchronize()
+    assert ops().device_error(clear=True) & PA_DEVERR_BAD_BLOCK
+
+
+def test_validate_mode_rejects_bad_metadata():
+    from paged_kv_cache_192_gb300._lib import PAError
+    w = synth.decode_workload("8b", seed=10, lens=[40, 20])
+    k_cache, v_cache, table, lens = device_inputs(w, DEV)
+    ops().set_validate(True)
+    try:
+        bad = table.clone()
+        bad[1, 0] = -3
+        with pytest.raises(PAError):
+            ops().decode(w.q.to(DEV), k_cache, v_cache, bad, lens)
+        bad_lens = lens.clone()
+        bad_lens[0] = 0
+        with pytest.raises(PAError):
+            ops().decode(w.q.to(DEV), k_cache, v_cache, table, bad_lens)
+        ops().decode(w.q.to(DEV), k_cache, v_cache, table, lens)  # valid passes
+    finally:
+        ops().set_validate(False)
+
+
+def test_shared_prefix_equals_private_copies():
+    """Sequences pointing at one physical copy of a 1024-token prefix give the
+    same bits as the same sequences with private prefix copies (nalar.dev,
+    'Sharing blok dapat menghindari duplikasi state KV'); both match the
+    oracle."""
+    w = synth.prefix_workload(seed=0, B=64)
+    _, ref, o_shared = run(w, seqs=np.arange(8))
+    w_priv = synth.prefix_workload(seed=0, B=64)
+    w_priv.table = w_priv.extra["private_table"]
+    w_priv.num_blocks = w_priv.extra["private_num_blocks"]
+    _, _, o_private = run(w_priv, seqs=[0])
+    assert torch.equal(o_shared, o_private)
+    compare(o_shared.double().cpu().numpy()[:8], ref, torch.bfloat16, "shared prefix")
+
+
+def test_prefix_config_full_size():
+    """Shared-prefix config: 256 sequences, 1024 shared tokens, suffix ~U[1,512];
+    oracle on 16 sampled sequences."""
+    w = synth.prefix_workload(seed=0)
+    seqs = synth.sample_indices(w.B, 16, seed=1)
+    got, ref, _ = run(w, seqs=seqs)
+    compare(got, ref, torch.bfloat16, "prefix")

@@ -1,0 +1,94 @@
+"""Chunked prefill (causal, over paged context) on the GPU against the fp64
+oracle, and the mixed continuous batch (decodes + prefill chunks)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import compare, device_inputs, oracle_decode
+from paged_kv_cache_192_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_192_gb300 import build
+    build.build()
+
+
+def ops():
+    from paged_kv_cache_192_gb300 import ops as o
+    return o
+
+
+def _prefill_workload(priors, n_new, Hq=32, Hkv=8, d=128, bs=16, seed=0):
+    lens = [p + n for p, n in zip(priors, n_new)]
+    w = synth.decode_workload("8b", seed=seed, lens=lens, Hq=Hq, Hkv=Hkv, d=d, bs=bs)
+    g = torch.Generator().manual_seed(seed + 100)
+    q = torch.randn(sum(n_new), Hq, d, generator=g).to(w.dtype)
+    return w, q
+
+
+def _run(w, q, priors, n_new):
+    k_cache, v_cache, table, lens = device_inputs(w, DEV)
+    qs = torch.tensor(np.concatenate([[0], np.cumsum(n_new)]), dtype=torch.int32, device=DEV)
+    out = ops().prefill_chunk(q.to(DEV), k_cache, v_cache, table, qs, lens, max(n_new))
+    torch.cuda.synchronize()
+    assert ops().device_error() == 0
+    ref = oracle.prefill_chunk(q.double().numpy(), w.k.double().numpy(), w.v.double().numpy(),
+                               n_new, priors, 1.0 / np.sqrt(w.d))
+    return out.double().cpu().numpy(), ref
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4), (8, 2), (32, 4)])
+@pytest.mark.parametrize("d,bs", [(128, 16), (64, 32), (128, 8)])
+def test_prefill_shapes(Hq, Hkv, d, bs):
+    priors = [0, 13, 64, 100, 5]
+    n_new = [7, 1, 65, 130, 64]
+    w, q = _prefill_workload(priors, n_new, Hq, Hkv, d, bs, seed=1)
+    got, ref = _run(w, q, priors, n_new)
+    compare(got, ref, torch.bfloat16, f"prefill {Hq}/{Hkv} d{d} bs{bs}")
+
+
+def test_prefill_first_query_sees_only_itself():
+    w, q = _prefill_workload([0], [48], seed=2)
+    got, _ = _run(w, q, [0], [48])
+    v0 = w.v[0].repeat_interleave(w.Hq // w.Hkv, 0).double().numpy()
+    assert np.array_equal(got[0], v0)
+
+
+def test_mixed_config_full_size():
+    """Mixed continuous batch: 128 decodes with L ~ U[256,8192] and 4 chunks of
+    512 new tokens over 0..3584 prior tokens, one pool; all new K/V stored by
+    reshape_and_cache first.  Decode checked on 16 sampled sequences, prefill
+    on the first and last 64 queries of every chunk."""
+    dec, pre = synth.mixed_workload(seed=0)
+    from paged_kv_cache_192_gb300 import layout
+    k_cache, v_cache = layout.alloc_pools(dec.num_blocks, dec.Hkv, dec.bs, dec.d, dec.dtype, DEV)
+    layout.fill_pools(k_cache, v_cache, dec.k, dec.v, dec.table, dec.lens, dec.bs)
+    layout.fill_pools(k_cache, v_cache, pre.k, pre.v, pre.table, pre.lens, pre.bs)
+    t_dec = torch.from_numpy(dec.table).to(DEV)
+    l_dec = torch.from_numpy(dec.lens.astype(np.int32)).to(DEV)
+    out_d = ops().decode(dec.q.to(DEV), k_cache, v_cache, t_dec, l_dec)
+    n = pre.extra["chunk"]
+    R = pre.B
+    qs = torch.arange(0, (R + 1) * n, n, dtype=torch.int32, device=DEV)
+    out_p = ops().prefill_chunk(pre.q.to(DEV), k_cache, v_cache, torch.from_numpy(pre.table).to(DEV),
+                                qs, torch.from_numpy(pre.lens.astype(np.int32)).to(DEV), n)
+    torch.cuda.synchronize()
+    assert ops().device_error() == 0
+    seqs = synth.sample_indices(dec.B, 16, seed=2)
+    compare(out_d.double().cpu().numpy()[seqs], oracle_decode(dec, seqs), torch.bfloat16,
+            "mixed decode")
+    got = out_p.double().cpu().numpy()
+    offs = pre.kv_offsets
+    for r in range(R):
+        P = int(pre.extra["prior"][r])
+        k = pre.k[offs[r]:offs[r] + pre.lens[r]].double().numpy()
+        v = pre.v[offs[r]:offs[r] + pre.lens[r]].double().numpy()
+        for lo in (0, n - 64):
+            q = pre.q[r * n + lo:r * n + lo + 64].double().numpy()
+            ref = oracle.attention(q, k, v, [64], [P + lo], [pre.lens[r]], 1.0 / np.sqrt(pre.d))
+            compare(got[r * n + lo:r * n + lo + 64], ref, torch.bfloat16, f"chunk {r} @{lo}")

@@ -204,7 +204,7 @@ def run_gpu(args, world, rank, local):
 
     # resident inputs: N_POOLS independent pools (each 1.2x the batch's blocks)
     pools = []
-    for _ in range(N_POOLS):
+    for _ in range(args.pools):
         kc, vc = layout.alloc_pools(w.num_blocks, Hkv, bs, d, w.dtype, dev, poison=False)
         layout.fill_pools(kc, vc, w.k, w.v, w.table, w.lens, bs)
         pools.append((kc, vc))
@@ -227,7 +227,7 @@ def run_gpu(args, world, rank, local):
     launches_per_step = 2 + (1 if ws_bytes else 0)
 
     def step(i, t_dec=None):
-        kc, vc = pools[i % N_POOLS]
+        kc, vc = pools[i % len(pools)]
         check(L.pa_reshape_and_cache(k_new.data_ptr(), v_new.data_ptr(), kc.data_ptr(),
                                      vc.data_ptr(), slots.data_ptr(), B, w.num_blocks, Hkv, bs, d,
                                      PA_BF16, sp))
@@ -245,7 +245,7 @@ def run_gpu(args, world, rank, local):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
-    t_end = time.time() + 1.0
+    t_end = time.time() + (0.0 if args.quick else 1.0)
     i = 0
     while time.time() < t_end:
         for _ in range(50):
@@ -266,7 +266,7 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     # keep the sampler running a little under load for the clock record
-    t_end = time.time() + 0.5
+    t_end = time.time() + (0.0 if args.quick else 0.5)
     while time.time() < t_end:
         for _ in range(50):
             step(i)
@@ -297,7 +297,7 @@ def run_gpu(args, world, rank, local):
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step(i):
-        kc, vc = pools[i % N_POOLS]
+        kc, vc = pools[i % len(pools)]
         for dst, src in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_slots, h_slots),
                          (d_table, h_table), (d_lens, h_lens)):
             dst.copy_(src, non_blocking=True)
@@ -309,6 +309,9 @@ def run_gpu(args, world, rank, local):
                           w.num_blocks, scale, PT, ws.data_ptr(), ws_bytes, PA_BF16, sp))
         h_out.copy_(out, non_blocking=True)
 
+    if args.quick:
+        print(json.dumps({"quick": True, "ms_per_step": ms_per_step, "value": value}))
+        return
     for i in range(args.warmup):
         e2e_step(i)
     torch.cuda.synchronize()
@@ -338,7 +341,7 @@ def run_gpu(args, world, rank, local):
                    "total_context_tokens": int(w.lens.sum()), "pool_blocks": w.num_blocks,
                    "partition_tokens": PT, "parallelism": f"replicas{world}",
                    "l2": f"inputs larger than L2 ({decode_bytes(w) / 1e6:.0f} MB per step) "
-                         f"and {N_POOLS} pools rotated"},
+                         f"and {len(pools)} pools rotated"},
         "tokens_per_s": round(tok_s, 1),
         "pct_of_hbm_peak": round(100 * value / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
@@ -445,6 +448,9 @@ def main(argv=None):
     ap.add_argument("--partition", type=int, default=512)
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pools", type=int, default=N_POOLS, help="pools rotated between steps")
+    ap.add_argument("--quick", action="store_true",
+                    help="profiling case: no clock warm loop, no e2e, no CPU baseline")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_env()

@@ -107,6 +107,7 @@ int pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cache, vo
     }
     const int chunks = static_cast<int>(head_dim * es / 16);
     const int64_t total = T * Hkv * chunks;
+    (void)cudaGetLastError();  // drop a stale error that is not ours
     reshape_and_cache_kernel<<<grid_for(total, 256), 256, 0, stream>>>(
         static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, total, Hkv,
@@ -146,6 +147,7 @@ int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int64_t n
             if (srcs.count(d)) return pa::fail(PA_ERR_INVALID, "validate: dst is also a src");
     }
     dim3 grid(static_cast<unsigned>(n), 2);
+    (void)cudaGetLastError();
     copy_blocks_kernel<<<grid, 256, 0, stream>>>(
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), pairs,
         static_cast<int64_t>(block_bytes / 16), num_blocks, pa::device_error_word());

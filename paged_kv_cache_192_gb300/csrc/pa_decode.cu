@@ -63,7 +63,10 @@ struct Cfg {
     static constexpr int VPL = V / G;                    // scores per lane after reduction
     static constexpr int TILE = TT * ROW;                // bytes per tile per cache
     static constexpr int STAGE = 2 * TILE;               // K then V
-    static constexpr int NST = kRingBytes / STAGE >= 2 ? kRingBytes / STAGE : 2;
+    // stages per warp: as many as fit the ring, at least 2 when 2 fit in
+    // 160 KB per CTA, else 1 (the warp then refills a stage after using it)
+    static constexpr int NST = kRingBytes / STAGE >= 2 ? kRingBytes / STAGE
+                               : (kWarps * 2 * STAGE <= 160 * 1024 ? 2 : 1);
     static constexpr int WARP_SMEM = NST * STAGE;
     static constexpr int OFF_P = kWarps * WARP_SMEM;                  // p and score buffers
     static constexpr int OFF_BAR = OFF_P + kWarps * 2 * TT * GQ * 4;  // mbarriers
@@ -500,6 +503,7 @@ int launch(const DecodeParams &p, cudaStream_t stream) {
     using C = Cfg<T, D, GQ>;
     const size_t smem = C::OFF_BT + sizeof(int32_t) * (p.PT / p.bs + 1);
     auto kern = decode_kernel<T, D, GQ>;
+    (void)cudaGetLastError();  // drop a stale error that is not ours
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return pa::cuda_fail(e, "decode: shared memory attribute");

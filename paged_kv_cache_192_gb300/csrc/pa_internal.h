@@ -21,6 +21,7 @@ bool validate_on();
 int *device_error_word();
 
 inline int cuda_fail(cudaError_t e, const char *what) {
+    (void)cudaGetLastError();  // do not leave the error for the next call to find
     return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 

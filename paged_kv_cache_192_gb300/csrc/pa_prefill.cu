@@ -228,8 +228,12 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
             alpha[ri] = mrow[ri] == -INFINITY ? 0.f : fast_exp2(mrow[ri] - mnew);
             mrow[ri] = mnew;
         }
+        // P enters the tensor cores as bf16; a single bf16 rounding of the
+        // softmax weights (2^-9 relative) is too coarse for short contexts,
+        // so P = hi + lo with both parts bf16 (2^-17 relative) and PV runs
+        // twice into the same fp32 accumulators.
         float rsum[2] = {0.f, 0.f};
-        uint32_t pf[NT / 2][4];
+        uint32_t pf[NT / 2][4], pl[NT / 2][4];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             const float p0 = fast_exp2(s[j][0] - mrow[0]);
@@ -238,8 +242,12 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
             const float p3 = fast_exp2(s[j][3] - mrow[1]);
             rsum[0] += p0 + p1;
             rsum[1] += p2 + p3;
-            pf[j / 2][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
-            pf[j / 2][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
+            const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
+            const float2 r01 = pa::bf16x2_to_float2(h01), r23 = pa::bf16x2_to_float2(h23);
+            pf[j / 2][(j & 1) * 2 + 0] = h01;
+            pf[j / 2][(j & 1) * 2 + 1] = h23;
+            pl[j / 2][(j & 1) * 2 + 0] = pack_bf16(p0 - r01.x, p1 - r01.y);
+            pl[j / 2][(j & 1) * 2 + 1] = pack_bf16(p2 - r23.x, p3 - r23.y);
         }
 #pragma unroll
         for (int ri = 0; ri < 2; ++ri) lrow[ri] = lrow[ri] * alpha[ri] + rsum[ri];
@@ -261,6 +269,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
                 ldsm_x4_t(swz<CH>(vb, row, c), b0, b1, b2, b3);
                 mma_bf16(o[j], pf[kk], b0, b1);
                 mma_bf16(o[j + 1], pf[kk], b2, b3);
+                mma_bf16(o[j], pl[kk], b0, b1);
+                mma_bf16(o[j + 1], pl[kk], b2, b3);
             }
         }
         __syncthreads();  // buffer `buf` is refilled two iterations on
@@ -298,6 +308,7 @@ template <int D, int GQ>
 int launch(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
     const size_t smem = kRows * D * 2 + 4 * kKT * D * 2;
     auto kern = prefill_kernel<D, GQ>;
+    (void)cudaGetLastError();
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return pa::cuda_fail(e, "prefill: shared memory attribute");

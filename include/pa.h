@@ -148,6 +148,30 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               int dtype, pa_stream_t stream);
 
 /*
+ * pa_decode_noalloc -- pa_decode for callers that cannot allocate device
+ * memory (for example a plug-in whose host program owns all device memory
+ * through its own pool, or a latency-critical loop where cudaMalloc, which
+ * may synchronize the device, is not allowed).  The pages have no
+ * counterpart to this entry point; it only changes where the split-KV
+ * workspace comes from.
+ * Same arguments and result as pa_decode, without workspace: the library
+ * uses a fixed device array of pa_decode_noalloc_capacity() bytes (16 MiB)
+ * that every GPU loading the library holds until the process exits.  A
+ * batch whose pa_decode_workspace_size exceeds it is rejected with
+ * PA_ERR_INVALID.  The first call on a device (with that device current)
+ * looks up the array's device address; make it before any stream capture.
+ * All calls on a device share the array: calls that overlap on the GPU race
+ * and must be serialized by the caller.  Nothing is allocated, no
+ * cudaMalloc/cudaFree is called.
+ */
+size_t pa_decode_noalloc_capacity(void);
+int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_table, int max_blocks_per_seq,
+                      const int32_t *context_lens, int B, int Hq, int Hkv, int head_dim,
+                      int block_size, int64_t num_blocks, float scale, int partition_tokens,
+                      int dtype, pa_stream_t stream);
+
+/*
  * pa_prefill_chunk -- chunked prefill over paged context ("Melihat Lebih
  * Dalam vLLM v0.7", section "Blueprint Arsitektur 3: Chunked Prefill": a long
  * prompt is cut into chunks of e.g. 512 tokens and run next to decode).

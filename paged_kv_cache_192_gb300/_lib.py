@@ -34,6 +34,9 @@ SIGNATURES = {
     "pa_decode": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_int,
                            _c_int, _c_int, _c_int, _c_i64, _c_f, _c_int, _c_vp, _c_sz, _c_int,
                            _c_vp]),
+    "pa_decode_noalloc_capacity": (_c_sz, []),
+    "pa_decode_noalloc": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_int,
+                                   _c_int, _c_int, _c_int, _c_i64, _c_f, _c_int, _c_int, _c_vp]),
     "pa_prefill_chunk": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_vp, _c_int,
                                   _c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_f, _c_int,
                                   _c_vp]),

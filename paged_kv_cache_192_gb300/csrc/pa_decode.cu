@@ -30,6 +30,7 @@
 //    placement of blocks.
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 #include <vector>
 
 #include "pa_device.cuh"
@@ -636,6 +637,87 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
                                : dispatch_gq<__nv_bfloat16, 64>(gq, p, stream);
     return head_dim == 128 ? dispatch_gq<float, 128>(gq, p, stream)
                            : dispatch_gq<float, 64>(gq, p, stream);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of pa_decode.
+//
+// Some callers cannot allocate device memory: a plug-in whose host program
+// owns every device allocation through its own pool, or a latency-critical
+// loop where cudaMalloc (which can synchronize the device) is not allowed.
+// pa_decode_noalloc takes the split-KV workspace from a fixed array that the
+// library itself holds in device memory, so such a caller passes only inputs
+// and outputs.
+//
+// The array is a file-scope __device__ object of kNoAllocScratchBytes; every
+// GPU that loads the library keeps it until the process exits.  Host code may
+// not use the array's name as a device address, so the first call on each
+// device (with that device current) looks up its address with
+// cudaGetSymbolAddress and caches it; make that first call before any stream
+// capture.  All calls on a device share the array and it keeps the contents
+// of the last call; nothing in it needs to start at zero (every partial is
+// written before it is read in the same call).  Calls that overlap on the GPU
+// (different streams, or host threads racing) race on the array: serialize
+// them.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+void *g_noalloc_ptr[kNoAllocMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of this device's scratch array (looked up once per device).
+int noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return pa::cuda_fail(e, "decode_noalloc: cudaGetDevice");
+    if (dev < 0 || dev >= kNoAllocMaxDevices)
+        return pa::fail(PA_ERR_UNSUPPORTED, "decode_noalloc: device %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return pa::cuda_fail(e, "decode_noalloc: cudaGetSymbolAddress");
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_decode_noalloc_capacity(void) { return kNoAllocScratchBytes; }
+
+int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_table, int max_blocks_per_seq,
+                      const int32_t *context_lens, int B, int Hq, int Hkv, int head_dim,
+                      int block_size, int64_t num_blocks, float scale, int partition_tokens,
+                      int dtype, pa_stream_t stream) {
+    pa::clear_error();
+    size_t need = 0;
+    if (int rc = pa_decode_workspace_size(B, Hq, head_dim, max_blocks_per_seq, block_size,
+                                          partition_tokens, &need))
+        return rc;
+    if (need > kNoAllocScratchBytes)
+        return pa::fail(PA_ERR_INVALID,
+                        "decode_noalloc: this batch needs %zu bytes of split-KV workspace, more "
+                        "than the library's fixed %zu-byte scratch; use pa_decode with a caller "
+                        "workspace, fewer sequences or longer partitions",
+                        need, kNoAllocScratchBytes);
+    void *scratch = nullptr;
+    if (need) {
+        if (int rc = noalloc_scratch(&scratch)) return rc;
+    }
+    return pa_decode(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, B,
+                     Hq, Hkv, head_dim, block_size, num_blocks, scale, partition_tokens, scratch,
+                     need ? kNoAllocScratchBytes : 0, dtype, stream);
 }
 
 }  // extern "C"

@@ -224,7 +224,7 @@ def run_gpu(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     L = lib()
-    launches_per_step = 2 + (1 if ws_bytes else 0)
+    launches_per_step = 2  # reshape_and_cache + the persistent decode kernel (B <= 1024)
 
     def step(i, t_dec=None):
         kc, vc = pools[i % len(pools)]
@@ -346,7 +346,7 @@ def run_gpu(args, world, rank, local):
         "pct_of_hbm_peak": round(100 * value / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "pa_decode (decode_kernel + merge_kernel)",
+                     "kernel": "pa_decode (decode_persistent_kernel, split-KV merge inside)",
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "avg_launch_us": round(dec_avg_ms * 1e3, 2),
                      "algorithmic_bytes": decode_bytes(w)},

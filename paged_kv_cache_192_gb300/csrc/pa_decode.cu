@@ -9,26 +9,31 @@
 //
 // How (decode is HBM-bound: "Melihat Lebih Dalam vLLM v0.7", section
 // "Blueprint Arsitektur 3", the decode phase is memory-bandwidth intensive):
-//  * One CTA of kWarps warps per work item (sequence b, KV head, partition of
-//    PT tokens).  Partitions are merged by log-sum-exp in a second kernel
-//    when a sequence spans more than one (split-KV).
-//  * Each warp takes every kWarps-th tile of TT tokens of the partition and
-//    streams it through its own ring of NST shared-memory stages.  One lane
-//    issues a bulk copy (cp.async.bulk, non-tensor TMA) per contiguous
-//    (block, KV head) piece of K and of V, completing on an mbarrier.
-//  * All GQ query heads of a KV head share one K/V load.  A token row is split
-//    over G lanes in 16-byte chunks (conflict-free shared loads); QK partial
-//    dots of the S steps x GQ heads are reduced across the G lanes by a
-//    transpose-reduce (each round halves the values a lane carries), which
-//    leaves every (token, head) score in exactly one lane.
-//  * Online softmax in the log2 domain (q pre-scaled by scale*log2(e)) with a
-//    lazy rescale: the running max only moves when a score exceeds it by more
-//    than kTau; the result is exact whatever max is used.
-//  * PV accumulates in fp32 with packed fp32 FMAs; the partial sums of the
-//    token groups, then of the warps, are combined in a fixed order, so the
-//    result depends only on the logical token order, never on the physical
-//    placement of blocks.
+//  * Work unit: one tile of TT tokens of one (sequence, KV head) item.  All
+//    GQ query heads of a KV head share one K/V load.
+//  * Default kernel (decode_persistent_kernel): a persistent grid of ~3 CTAs
+//    per SM; every warp owns an equal, contiguous range of units across all
+//    items (perfect balance) and streams its tiles through its own ring of NST
+//    shared-memory stages.  One lane issues a bulk copy (cp.async.bulk,
+//    non-tensor TMA) per contiguous (block, KV head) piece of K and of V,
+//    completing on an mbarrier; the block-table entry of the next tile is
+//    loaded one tile ahead.  When a warp's range ends inside an item, the
+//    item's ranges (segments) write partial (max, sum, acc) to the workspace
+//    and the last one to arrive (an atomic ticket; nobody waits) merges them
+//    by log-sum-exp: split-KV without a second launch.
+//  * Fallback kernel for very large batches (decode_kernel): one CTA per
+//    (sequence, KV head, partition), merged by merge_kernel.
+//  * Per tile: a token row is split over G lanes in 16-byte chunks
+//    (conflict-free shared loads); QK partial dots of S steps x GQ heads are
+//    reduced across the G lanes by a transpose-reduce (each round halves the
+//    values a lane carries), leaving each (token, head) score in one lane;
+//    online softmax in the log2 domain (q pre-scaled by scale*log2(e)) with a
+//    lazy rescale (the running max moves only when a score exceeds it by more
+//    than kTau; exact whatever max is used); PV with packed fp32 FMAs.
+//  * Every sum runs in an order fixed by logical token positions and the
+//    batch's lengths, never by where blocks sit in the pool.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 #include <vector>
@@ -38,19 +43,41 @@
 
 namespace {
 
+// Tuning knobs (compile-time): CTAs per SM the register budget targets, the
+// per-warp staging ring, and lanes per token row for groups of <= 4 heads.
+#ifndef PA_DECODE_MIN_CTAS
+#define PA_DECODE_MIN_CTAS 2
+#endif
+#ifndef PA_DECODE_RING_KB
+#define PA_DECODE_RING_KB 16
+#endif
+#ifndef PA_DECODE_LANES_SMALL_GROUP
+#define PA_DECODE_LANES_SMALL_GROUP 8
+#endif
+#ifndef PA_DECODE_MIN_STEPS
+#define PA_DECODE_MIN_STEPS 4  // token-row steps per tile (tile = steps x 32/G tokens)
+#endif
+#ifndef PA_DECODE_LOADER
+#define PA_DECODE_LOADER 0  // 0: one bulk (TMA) copy per block piece; 1: per-lane cp.async
+#endif
+#ifndef PA_DECODE_Q_SMEM
+#define PA_DECODE_Q_SMEM 0  // 1: keep the scaled q in shared memory, not registers
+#endif
 constexpr int kWarps = 4;              // warps per CTA
-constexpr int kRingBytes = 16 * 1024;  // per-warp K+V staging ring
+constexpr int kMinCtas = PA_DECODE_MIN_CTAS;
+constexpr int kRingBytes = PA_DECODE_RING_KB * 1024;  // per-warp K+V staging ring
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTau = 8.0f;           // lazy-rescale headroom (log2 units)
 constexpr int kDefaultPartition = 512;
 constexpr int kMaxPartition = 8192;
+constexpr int kPersistentMaxB = 1024;  // the persistent kernel keeps [B] tables in smem
 
 template <typename T, int D, int GQ>
 struct Cfg {
     static constexpr int ES = sizeof(T);
     static constexpr int ROW = D * ES;       // bytes of one token row of one KV head
     static constexpr int CHUNKS = ROW / 16;  // 16-byte chunks per row
-    static constexpr int G0 = GQ >= 8 ? 16 : 8;
+    static constexpr int G0 = GQ >= 8 ? 16 : PA_DECODE_LANES_SMALL_GROUP;
     static constexpr int G = G0 < CHUNKS ? G0 : CHUNKS;  // lanes per token
     static constexpr int CPL = CHUNKS / G;               // chunks per lane
     static constexpr int EPC = 16 / ES;                  // elements per chunk
@@ -58,7 +85,7 @@ struct Cfg {
     static constexpr int P = E / 2;                      // float2 pairs per lane
     static constexpr int TPS = 32 / G;                   // tokens per step
     static constexpr int SMIN = (G + GQ - 1) / GQ;
-    static constexpr int S = SMIN > 4 ? SMIN : 4;        // steps per tile
+    static constexpr int S = SMIN > PA_DECODE_MIN_STEPS ? SMIN : PA_DECODE_MIN_STEPS;
     static constexpr int TT = S * TPS;                   // tokens per tile
     static constexpr int V = S * GQ;                     // partial dots per lane
     static constexpr int VPL = V / G;                    // scores per lane after reduction
@@ -69,14 +96,20 @@ struct Cfg {
     static constexpr int NST = kRingBytes / STAGE >= 2 ? kRingBytes / STAGE
                                : (kWarps * 2 * STAGE <= 160 * 1024 ? 2 : 1);
     static constexpr int WARP_SMEM = NST * STAGE;
+    // CTAs per SM the register budget targets (groups of 8 heads need ~220
+    // registers per thread, so they run at 2)
+    static constexpr int MINB = GQ >= 8 ? 2 : kMinCtas;
     static constexpr int OFF_P = kWarps * WARP_SMEM;                  // p and score buffers
-    static constexpr int OFF_BAR = OFF_P + kWarps * 2 * TT * GQ * 4;  // mbarriers
-    static constexpr int OFF_FLAG = OFF_BAR + kWarps * NST * 8;       // failure flag
-    static constexpr int OFF_BT = OFF_FLAG + 16;                      // block-table slice
+    static constexpr bool QS = PA_DECODE_Q_SMEM != 0;
+    static constexpr int OFF_Q = OFF_P + kWarps * 2 * TT * GQ * 4;    // scaled q (QS)
+    static constexpr int OFF_BAR = OFF_Q + (QS ? kWarps * GQ * D * 4 : 0);  // mbarriers
+    static constexpr int OFF_FLAG = OFF_BAR + kWarps * NST * 8;       // flag / scan scratch
+    static constexpr int OFF_BT = OFF_FLAG + 16;                      // per-batch tables
     static_assert(G * CPL == CHUNKS, "row must split evenly over the lanes of a token");
     static_assert(V % G == 0 && VPL <= GQ && GQ % VPL == 0, "bad reduction shape");
     static_assert(E % 2 == 0 && TT <= 32, "bad tile");
     static_assert(GQ * D * 4 + 2 * GQ * 4 <= WARP_SMEM, "merge buffer must fit the ring");
+    static_assert(kWarps * 4 <= 16, "scan scratch");
 };
 
 struct DecodeParams {
@@ -86,12 +119,14 @@ struct DecodeParams {
     const uint8_t *v_cache;
     const int32_t *block_table;
     const int32_t *context_lens;
-    float *ws_acc;  // [B][Hq][max_parts][D]
-    float *ws_ml;   // [B][Hq][max_parts][2] (max, sum)
+    float *ws_acc;               // [B][Hq][maxseg][D]
+    float *ws_ml;                // [B][Hq][maxseg][2] (max, sum)
+    unsigned long long *ctr;     // [B][Hkv] tickets (persistent kernel)
     int *err;
     int64_t num_blocks;
-    int B, Hq, Hkv, bs, bs_log2, MB, PT, max_parts;
-    float qscale;  // scale * log2(e)
+    int B, Hq, Hkv, bs, bs_log2, MB, PT, max_parts, maxseg;
+    unsigned epoch;              // nonzero, new for every launch
+    float qscale;                // scale * log2(e)
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -117,8 +152,642 @@ __device__ __forceinline__ void transpose_reduce(float (&v)[V], int lane) {
     }
 }
 
+// One warp's attention state for one (sequence, KV head) item: q of the GQ
+// heads (this lane's elements), running max, per-lane partial sums, and the
+// PV accumulators of this lane's elements.
 template <typename T, int D, int GQ>
-__global__ void __launch_bounds__(kWarps * 32, 3) decode_kernel(const DecodeParams p) {
+struct WarpAttn {
+    using C = Cfg<T, D, GQ>;
+    int lane, gl, grp, h0, row_mine;
+    float *qs;  // per-warp scaled q [GQ][D] in shared memory (QS)
+    float2 q2[C::QS ? 1 : GQ][C::QS ? 1 : C::P];
+    float m_run[GQ];
+    float2 acc[GQ][C::P];
+    float lsum[C::VPL], mh[C::VPL];
+    float mhh;  // running max of head lane % GQ
+
+    __device__ __forceinline__ void init(int lane_) {
+        lane = lane_;
+        gl = lane % C::G;
+        grp = lane / C::G;
+        // after the transpose-reduce this lane holds the scores of heads
+        // h0 .. h0+VPL-1 of token row row_mine of the tile
+        h0 = (gl * C::VPL) % GQ;
+        row_mine = ((gl * C::VPL) / GQ) * C::TPS + grp;
+    }
+
+    // element index of pair j of chunk c of this lane
+    __device__ __forceinline__ int dim_of(int c, int j) const {
+        return (c * C::G + gl) * C::EPC + 2 * j;
+    }
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+            m_run[h] = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < C::P; ++j) acc[h][j] = make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < C::VPL; ++k) {
+            lsum[k] = 0.f;
+            mh[k] = -INFINITY;
+        }
+        mhh = -INFINITY;
+    }
+
+    // qb points at q[b][first head of the group][0]
+    __device__ __forceinline__ void load_q(const T *qb, float qscale) {
+        if constexpr (C::QS) __syncwarp();  // the previous item's reads are done
+#pragma unroll
+        for (int h = 0; h < GQ; ++h)
+#pragma unroll
+            for (int c = 0; c < C::CPL; ++c) {
+                const uint4 raw =
+                    *reinterpret_cast<const uint4 *>(qb + h * D + (c * C::G + gl) * C::EPC);
+                float2 f[C::EPC / 2];
+                pa::Elem<T>::unpack(raw, f);
+#pragma unroll
+                for (int i = 0; i < C::EPC / 2; ++i) {
+                    const float2 v = make_float2(f[i].x * qscale, f[i].y * qscale);
+                    if constexpr (C::QS) {
+                        if (grp == 0)
+                            *reinterpret_cast<float2 *>(qs + h * D + (c * C::G + gl) * C::EPC +
+                                                        2 * i) = v;
+                    } else {
+                        q2[h][c * C::EPC / 2 + i] = v;
+                    }
+                }
+            }
+        if constexpr (C::QS) __syncwarp();
+    }
+
+    __device__ __forceinline__ float2 qpair(int h, int j) const {
+        if constexpr (C::QS) {
+            const int c = j / (C::EPC / 2), i = j % (C::EPC / 2);
+            return *reinterpret_cast<const float2 *>(qs + h * D + (c * C::G + gl) * C::EPC + 2 * i);
+        } else {
+            return q2[h][j];
+        }
+    }
+
+    // One staged tile: K rows at kaddr, V rows at vaddr (shared), nvalid rows valid.
+    __device__ __forceinline__ void tile(uint32_t kaddr, uint32_t vaddr, int nvalid, float *pbuf,
+                                         float *sbuf) {
+        const bool masked = nvalid < C::TT;
+        // ---- QK: partial dots of S token rows x GQ heads -----------------
+        float part_[C::V];
+#pragma unroll
+        for (int s = 0; s < C::S; ++s) {
+            const int row = s * C::TPS + grp;
+            float2 kf[C::P];
+#pragma unroll
+            for (int c = 0; c < C::CPL; ++c) {
+                const uint4 raw = pa::lds128(kaddr + row * C::ROW + (c * C::G + gl) * 16);
+                float2 f[C::EPC / 2];
+                pa::Elem<T>::unpack(raw, f);
+#pragma unroll
+                for (int j = 0; j < C::EPC / 2; ++j) kf[c * C::EPC / 2 + j] = f[j];
+            }
+#pragma unroll
+            for (int h = 0; h < GQ; ++h) {
+                float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < C::P; ++j) a = pa::ffma2(qpair(h, j), kf[j], a);
+                part_[s * GQ + h] = a.x + a.y;
+            }
+        }
+        transpose_reduce<C::V, C::G>(part_, lane);
+
+        float sc[C::VPL];
+        const bool row_valid = row_mine < nvalid;
+#pragma unroll
+        for (int k = 0; k < C::VPL; ++k) sc[k] = row_valid ? part_[k] : -INFINITY;
+
+        // ---- online softmax with lazy rescale -------------------------------
+        bool need = false;
+#pragma unroll
+        for (int k = 0; k < C::VPL; ++k) need |= sc[k] > mh[k] + kTau;
+        if (__any_sync(pa::kFull, need)) {
+#pragma unroll
+            for (int k = 0; k < C::VPL; ++k) sbuf[row_mine * GQ + h0 + k] = sc[k];
+            __syncwarp();
+            // Lane l computes head (l % GQ)'s new max and rescale factor;
+            // every other value travels by shuffle (no per-lane indexing of
+            // the per-head arrays, which would push them to local memory).
+            const int hh = lane % GQ;
+            float tmax = -INFINITY;
+            for (int r = 0; r < C::TT; ++r) tmax = fmaxf(tmax, sbuf[r * GQ + hh]);
+            const float mnew_l = fmaxf(mhh, tmax);
+            const float alpha_l = (mhh == -INFINITY) ? 0.f : exp2f(mhh - mnew_l);
+            mhh = mnew_l;
+#pragma unroll
+            for (int h = 0; h < GQ; ++h) {
+                const float alpha = __shfl_sync(pa::kFull, alpha_l, h);
+                const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+                for (int j = 0; j < C::P; ++j) acc[h][j] = __fmul2_rn(acc[h][j], a2);
+                m_run[h] = __shfl_sync(pa::kFull, mnew_l, h);
+            }
+#pragma unroll
+            for (int k = 0; k < C::VPL; ++k) {
+                lsum[k] *= __shfl_sync(pa::kFull, alpha_l, h0 + k);
+                mh[k] = __shfl_sync(pa::kFull, mnew_l, h0 + k);
+            }
+            __syncwarp();
+        }
+#pragma unroll
+        for (int k = 0; k < C::VPL; ++k) {
+            const float pk = fast_exp2(sc[k] - mh[k]);
+            lsum[k] += pk;
+            pbuf[row_mine * GQ + h0 + k] = pk;
+        }
+        __syncwarp();
+
+        // ---- PV ---------------------------------------------------------------
+#pragma unroll
+        for (int s = 0; s < C::S; ++s) {
+            const int row = s * C::TPS + grp;
+            float prow[GQ];
+            if constexpr (GQ % 4 == 0) {
+#pragma unroll
+                for (int h = 0; h < GQ; h += 4) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(pbuf + row * GQ + h);
+                    prow[h] = t4.x;
+                    prow[h + 1] = t4.y;
+                    prow[h + 2] = t4.z;
+                    prow[h + 3] = t4.w;
+                }
+            } else {
+#pragma unroll
+                for (int h = 0; h < GQ; ++h) prow[h] = pbuf[row * GQ + h];
+            }
+            float2 vf[C::P];
+#pragma unroll
+            for (int c = 0; c < C::CPL; ++c) {
+                const uint4 raw = pa::lds128(vaddr + row * C::ROW + (c * C::G + gl) * 16);
+                float2 f[C::EPC / 2];
+                pa::Elem<T>::unpack(raw, f);
+#pragma unroll
+                for (int j = 0; j < C::EPC / 2; ++j) vf[c * C::EPC / 2 + j] = f[j];
+            }
+            if (masked && row >= nvalid) {
+                // p is 0 there, but the stale row may hold NaN: 0 * NaN = NaN
+#pragma unroll
+                for (int j = 0; j < C::P; ++j) vf[j] = make_float2(0.f, 0.f);
+            }
+#pragma unroll
+            for (int h = 0; h < GQ; ++h) {
+                const float2 pp = make_float2(prow[h], prow[h]);
+#pragma unroll
+                for (int j = 0; j < C::P; ++j) acc[h][j] = pa::ffma2(pp, vf[j], acc[h][j]);
+            }
+        }
+    }
+
+    // Sum acc over the token groups (every lane ends with the totals of its
+    // elements) and the per-head softmax denominators over all lanes.
+    __device__ __forceinline__ void reduce(float (&lh)[GQ]) {
+#pragma unroll
+        for (int off = C::G; off < 32; off <<= 1)
+#pragma unroll
+            for (int h = 0; h < GQ; ++h)
+#pragma unroll
+                for (int j = 0; j < C::P; ++j) {
+                    acc[h][j].x += __shfl_xor_sync(pa::kFull, acc[h][j].x, off);
+                    acc[h][j].y += __shfl_xor_sync(pa::kFull, acc[h][j].y, off);
+                }
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+            float t = 0.f;
+#pragma unroll
+            for (int k = 0; k < C::VPL; ++k) t += (h == h0 + k) ? lsum[k] : 0.f;
+            lh[h] = t;
+        }
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1)
+#pragma unroll
+            for (int h = 0; h < GQ; ++h) lh[h] += __shfl_xor_sync(pa::kFull, lh[h], off);
+    }
+};
+
+template <typename T>
+__device__ __forceinline__ void store_pair(T *dst, float a, float b);
+template <>
+__device__ __forceinline__ void store_pair<__nv_bfloat16>(__nv_bfloat16 *dst, float a, float b) {
+    *reinterpret_cast<__nv_bfloat162 *>(dst) = __floats2bfloat162_rn(a, b);
+}
+template <>
+__device__ __forceinline__ void store_pair<float>(float *dst, float a, float b) {
+    *reinterpret_cast<float2 *>(dst) = make_float2(a, b);
+}
+
+// ---------------------------------------------------------------------------
+// Persistent kernel (default)
+// ---------------------------------------------------------------------------
+struct Cursor {
+    int b, hk, t, nt, L;  // item (b, hk), tile t of nt tiles, context length L
+};
+
+// Tables of the persistent kernel in shared memory: tile prefix over the
+// sequences ([B+1]) and clamped context lengths ([B]).
+struct BatchTables {
+    const int32_t *pre;
+    const int32_t *lens;
+};
+
+// Cursor at unit u: the largest b with Hkv*pre[b] <= u, then (hk, t).
+__device__ __forceinline__ Cursor locate_unit(int64_t u, const BatchTables &bt, int B, int Hkv) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (int64_t(Hkv) * bt.pre[mid] <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    Cursor c;
+    c.b = lo;
+    c.nt = bt.pre[lo + 1] - bt.pre[lo];
+    c.L = bt.lens[lo];
+    const int64_t rem = u - int64_t(Hkv) * bt.pre[lo];
+    c.hk = static_cast<int>(rem / c.nt);
+    c.t = static_cast<int>(rem - int64_t(c.hk) * c.nt);
+    return c;
+}
+
+// Next unit: next tile, else next KV head, else next sequence with tiles.
+__device__ __forceinline__ Cursor next_unit(Cursor c, const BatchTables &bt, int B, int Hkv) {
+    if (++c.t == c.nt) {
+        c.t = 0;
+        if (++c.hk == Hkv) {
+            c.hk = 0;
+            do {
+                ++c.b;
+            } while (c.b < B && bt.pre[c.b + 1] == bt.pre[c.b]);
+            if (c.b < B) {
+                c.nt = bt.pre[c.b + 1] - bt.pre[c.b];
+                c.L = bt.lens[c.b];
+            }
+        }
+    }
+    return c;
+}
+
+template <int TT>
+__device__ __forceinline__ int block_entry(const DecodeParams &p, const Cursor &c, int j) {
+    return __ldg(p.block_table + static_cast<size_t>(c.b) * p.MB + ((c.t * TT) >> p.bs_log2) + j);
+}
+
+__device__ __forceinline__ int checked_block(const DecodeParams &p, int v) {
+    if (v < 0 || v >= p.num_blocks) {
+        pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+        v = 0;
+    }
+    return v;
+}
+
+// Producer (one lane): bulk-copy the K and V rows of tile c into the stage.
+template <typename T, int D, int GQ>
+__device__ __forceinline__ void produce_tile(const DecodeParams &p, const Cursor &c, int blk,
+                                             uint8_t *stage, uint64_t *bar) {
+    using C = Cfg<T, D, GQ>;
+    uint8_t *dk = stage;
+    uint8_t *dv = stage + C::TILE;
+    const int tok = c.t * C::TT;
+    if (C::TT <= p.bs) {
+        const int r0 = tok & (p.bs - 1);
+        const size_t off = ((static_cast<size_t>(blk) * p.Hkv + c.hk) * p.bs + r0) * C::ROW;
+        pa::mbar_arrive_expect_tx(bar, 2 * C::TILE);
+        pa::bulk_g2s(dk, p.k_cache + off, C::TILE, bar);
+        pa::bulk_g2s(dv, p.v_cache + off, C::TILE, bar);
+    } else {
+        const int nb = C::TT >> p.bs_log2;  // blocks per tile
+        const uint32_t bytes = static_cast<uint32_t>(p.bs) * C::ROW;
+        int avail = 0;
+        for (int j = 0; j < nb; ++j) avail += (tok + j * p.bs < c.L) ? 1 : 0;
+        pa::mbar_arrive_expect_tx(bar, 2u * avail * bytes);
+        for (int j = 0; j < avail; ++j) {
+            const int id = j == 0 ? blk : checked_block(p, block_entry<C::TT>(p, c, j));
+            const size_t off = (static_cast<size_t>(id) * p.Hkv + c.hk) * p.bs * C::ROW;
+            pa::bulk_g2s(dk + j * bytes, p.k_cache + off, bytes, bar);
+            pa::bulk_g2s(dv + j * bytes, p.v_cache + off, bytes, bar);
+        }
+    }
+}
+
+// Producer (whole warp): 16-byte cp.async copies of tile c's K and V rows,
+// lane l taking chunks l, l+32, ...; each lane's completions arrive on the
+// stage's mbarrier (initialised with one arrival per lane).
+template <typename T, int D, int GQ>
+__device__ __forceinline__ void produce_tile_lanes(const DecodeParams &p, const Cursor &c, int blk,
+                                                   uint8_t *stage, uint64_t *bar, int lane) {
+    using C = Cfg<T, D, GQ>;
+    const int tok = c.t * C::TT;
+    const uint32_t sk = pa::smem_u32(stage);
+#pragma unroll
+    for (int k = 0; k < C::TILE / 16 / 32; ++k) {
+        const int ch = lane + 32 * k;
+        const int row = ch / C::CHUNKS, within = ch % C::CHUNKS;
+        const int t = tok + row;
+        if (t >= c.L) continue;  // rows past the end stay stale and are masked
+        int id = blk;
+        if (C::TT > p.bs && (t >> p.bs_log2) != (tok >> p.bs_log2))
+            id = checked_block(p, __ldg(p.block_table + static_cast<size_t>(c.b) * p.MB +
+                                        (t >> p.bs_log2)));
+        const size_t off =
+            ((static_cast<size_t>(id) * p.Hkv + c.hk) * p.bs + (t & (p.bs - 1))) * C::ROW +
+            within * 16;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sk + ch * 16),
+                     "l"(p.k_cache + off)
+                     : "memory");
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sk + C::TILE + ch * 16),
+                     "l"(p.v_cache + off)
+                     : "memory");
+    }
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(pa::smem_u32(bar))
+                 : "memory");
+}
+
+// Bring an item's q into L1 ahead of its first tile (lanes < q lines).
+template <typename T, int D, int GQ>
+__device__ __forceinline__ void prefetch_q(const DecodeParams &p, const Cursor &c, int lane) {
+    constexpr int kLines = GQ * D * int(sizeof(T)) / 128;
+    const char *qa = reinterpret_cast<const char *>(
+        static_cast<const T *>(p.q) + (static_cast<size_t>(c.b) * p.Hq + c.hk * GQ) * D);
+    if (lane < kLines) asm volatile("prefetch.global.L1 [%0];" ::"l"(qa + lane * 128));
+}
+
+// End of this warp's segment of item c: write the output (the whole item is
+// in this warp's range) or a partial, and merge the item's partials if this
+// segment is the last of them to finish.
+template <typename T, int D, int GQ>
+__device__ __forceinline__ void finish_segment(WarpAttn<T, D, GQ> &st, const DecodeParams &p,
+                                               const BatchTables &bt, const Cursor &c,
+                                               int64_t per, int64_t w, int lane) {
+    using C = Cfg<T, D, GQ>;
+    float lh[GQ];
+    st.reduce(lh);
+    const int64_t ia = int64_t(p.Hkv) * bt.pre[c.b] + int64_t(c.hk) * c.nt;
+    const int64_t wa = ia / per, wb = (ia + c.nt - 1) / per;
+    const int nseg = static_cast<int>(wb - wa + 1), seg = static_cast<int>(w - wa);
+    const size_t hq0 = static_cast<size_t>(c.b) * p.Hq + c.hk * GQ;
+    T *out = static_cast<T *>(p.out);
+    if (nseg == 1) {
+        if (st.grp == 0) {
+#pragma unroll
+            for (int h = 0; h < GQ; ++h) {
+                const float inv = 1.f / lh[h];
+#pragma unroll
+                for (int cc = 0; cc < C::CPL; ++cc)
+#pragma unroll
+                    for (int j = 0; j < C::EPC / 2; ++j) {
+                        const float2 a = st.acc[h][cc * C::EPC / 2 + j];
+                        store_pair<T>(out + (hq0 + h) * D + st.dim_of(cc, j), a.x * inv, a.y * inv);
+                    }
+            }
+        }
+        return;
+    }
+    if (seg < 0 || seg >= p.maxseg) {  // cannot happen with maxseg from the host
+        if (lane == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+        return;
+    }
+    if (st.grp == 0) {
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+            float *dst = p.ws_acc + ((hq0 + h) * p.maxseg + seg) * D;
+#pragma unroll
+            for (int cc = 0; cc < C::CPL; ++cc)
+#pragma unroll
+                for (int j = 0; j < C::EPC / 2; ++j)
+                    *reinterpret_cast<float2 *>(dst + st.dim_of(cc, j)) =
+                        st.acc[h][cc * C::EPC / 2 + j];
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < GQ; ++h)
+            *reinterpret_cast<float2 *>(p.ws_ml + 2 * ((hq0 + h) * p.maxseg + seg)) =
+                make_float2(st.m_run[h], lh[h]);
+    }
+    // Release this warp's partial, take a ticket; the segment that completes
+    // the item merges it.  The warp barrier orders every lane's stores before
+    // lane 0's (cumulative) release fence; nobody waits on anybody.
+    __syncwarp();
+    int last = 0;
+    unsigned long long *ctr = p.ctr + static_cast<size_t>(c.b) * p.Hkv + c.hk;
+    if (lane == 0) {
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        // ticket = (epoch << 32) | count; a stale epoch counts as zero.  Start
+        // from the value the previous launch leaves behind (0).
+        // A failed CAS means another segment's CAS succeeded, so at most
+        // nseg attempts are needed; the bound only guards against corruption.
+        unsigned long long assumed = 0ull;
+        unsigned cnt = 0;
+        bool done = false;
+        for (int tries = 0; tries < 4 * p.maxseg + 8 && !done; ++tries) {
+            const unsigned ep = static_cast<unsigned>(assumed >> 32);
+            cnt = ep == p.epoch ? static_cast<unsigned>(assumed) + 1u : 1u;
+            const unsigned long long old =
+                atomicCAS(ctr, assumed, (static_cast<unsigned long long>(p.epoch) << 32) | cnt);
+            done = old == assumed;
+            assumed = old;
+        }
+        if (!done) pa::record_error(p.err, PA_DEVERR_TIMEOUT);
+        last = done && cnt == static_cast<unsigned>(nseg);
+        if (last) asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    }
+    last = __shfl_sync(pa::kFull, last, 0);
+    if (!last) return;
+    __syncwarp();
+    // Merge: lane s < nseg holds segment s's (max, sum) per head; every lane
+    // owns D/32 output elements; all loads are independent (issued ahead).
+    constexpr int EL = D / 32;
+    float wsh[GQ], inv[GQ];
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) {
+        const size_t sb = (hq0 + h) * p.maxseg;
+        float2 ml = make_float2(-INFINITY, 0.f);
+        if (lane < nseg) ml = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + 2 * (sb + lane)));
+        float M = ml.x;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(pa::kFull, M, o));
+        wsh[h] = lane < nseg ? exp2f(ml.x - M) : 0.f;
+        float den = wsh[h] * ml.y;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(pa::kFull, den, o);
+        inv[h] = 1.f / den;
+    }
+    float accm[GQ][EL];
+#pragma unroll
+    for (int h = 0; h < GQ; ++h)
+#pragma unroll
+        for (int e = 0; e < EL; ++e) accm[h][e] = 0.f;
+#pragma unroll 4
+    for (int sgi = 0; sgi < nseg; ++sgi) {
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+            const float wv = __shfl_sync(pa::kFull, wsh[h], sgi);
+            const float *src = p.ws_acc + ((hq0 + h) * p.maxseg + sgi) * D + EL * lane;
+            if constexpr (EL == 4) {
+                const float4 a = __ldcg(reinterpret_cast<const float4 *>(src));
+                accm[h][0] += wv * a.x;
+                accm[h][1] += wv * a.y;
+                accm[h][2] += wv * a.z;
+                accm[h][3] += wv * a.w;
+            } else {
+                const float2 a = __ldcg(reinterpret_cast<const float2 *>(src));
+                accm[h][0] += wv * a.x;
+                accm[h][1] += wv * a.y;
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < GQ; ++h)
+#pragma unroll
+        for (int e = 0; e < EL; e += 2)
+            store_pair<T>(out + (hq0 + h) * D + EL * lane + e, accm[h][e] * inv[h],
+                          accm[h][e + 1] * inv[h]);
+    if (lane == 0) atomicExch(ctr, 0ull);
+}
+
+template <typename T, int D, int GQ>
+__global__ void __launch_bounds__(kWarps * 32, (Cfg<T, D, GQ>::MINB))
+    decode_persistent_kernel(const DecodeParams p) {
+    using C = Cfg<T, D, GQ>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t *ring = smem + warp * C::WARP_SMEM;
+    float *pbuf = reinterpret_cast<float *>(smem + C::OFF_P) + warp * 2 * C::TT * GQ;
+    float *sbuf = pbuf + C::TT * GQ;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR) + warp * C::NST;
+    int *scan = reinterpret_cast<int *>(smem + C::OFF_FLAG);
+    int32_t *pre = reinterpret_cast<int32_t *>(smem + C::OFF_BT);  // [B+1] tile prefix
+    int32_t *lens = pre + p.B + 1;                                  // [B]
+
+    // ---- tiles per sequence and their prefix sums (whole CTA) ---------------
+    const int cap = p.MB << p.bs_log2;
+    int carry = 0;
+    for (int base = 0; base < p.B; base += blockDim.x) {
+        const int b = base + threadIdx.x;
+        int nt = 0;
+        if (b < p.B) {
+            int L = p.context_lens[b];
+            if (L < 1 || L > cap) {
+                if (blockIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+                L = L < 1 ? 0 : cap;
+            }
+            lens[b] = L;
+            nt = (L + C::TT - 1) / C::TT;
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(pa::kFull, nt, o);
+            if (lane >= o) nt += y;
+        }
+        if (lane == 31) scan[warp] = nt;
+        __syncthreads();
+        int off = carry, total = 0;
+        for (int w2 = 0; w2 < kWarps; ++w2) {
+            off += w2 < warp ? scan[w2] : 0;
+            total += scan[w2];
+        }
+        if (b < p.B) pre[b + 1] = off + nt;
+        carry += total;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) pre[0] = 0;
+    if (lane == 0) {
+        for (int s = 0; s < C::NST; ++s) pa::mbar_init(&bars[s], PA_DECODE_LOADER ? 32 : 1);
+        pa::fence_barrier_init();
+    }
+    __syncthreads();
+    const BatchTables bt{pre, lens};
+
+    // ---- this warp's range of units ------------------------------------------
+    const int64_t U = int64_t(p.Hkv) * pre[p.B];
+    const int64_t W = int64_t(gridDim.x) * kWarps;
+    int64_t per = (U + W - 1) / W;
+    const int64_t pmin = p.PT / C::TT;
+    if (per < pmin) per = pmin;
+    const int64_t w = int64_t(blockIdx.x) * kWarps + warp;
+    const int64_t u0 = w * per;
+    if (u0 >= U) return;  // warp-uniform; no CTA barrier follows
+    const int my_n = static_cast<int>(min(per, U - u0));
+
+    WarpAttn<T, D, GQ> st;
+    st.init(lane);
+    st.qs = reinterpret_cast<float *>(smem + C::OFF_Q) + warp * GQ * D;
+    const T *qbase = static_cast<const T *>(p.q);
+
+    // ---- pipeline prologue ----------------------------------------------------
+    Cursor pc = locate_unit(u0, bt, p.B, p.Hkv);  // next tile to produce
+    Cursor cc = pc;                               // next tile to consume
+    constexpr bool kLanes = PA_DECODE_LOADER != 0;
+    int pend = 0;  // raw block-table entry of pc's tile (lane 0, or every lane)
+    if (kLanes || lane == 0) pend = block_entry<C::TT>(p, pc, 0);
+    const int npro = min(C::NST, my_n);
+    for (int i = 0; i < npro; ++i) {
+        if (kLanes)
+            produce_tile_lanes<T, D, GQ>(p, pc, checked_block(p, pend), ring + i * C::STAGE,
+                                         &bars[i], lane);
+        else if (lane == 0)
+            produce_tile<T, D, GQ>(p, pc, checked_block(p, pend), ring + i * C::STAGE, &bars[i]);
+        if (i > 0 && pc.t == 0) prefetch_q<T, D, GQ>(p, pc, lane);
+        pc = next_unit(pc, bt, p.B, p.Hkv);
+        if ((kLanes || lane == 0) && i + 1 < my_n) pend = block_entry<C::TT>(p, pc, 0);
+    }
+
+    int failed_at = -1;
+    for (int i = 0; i < my_n; ++i) {
+        const int s = i % C::NST;
+        const bool ok = __all_sync(pa::kFull, pa::mbar_wait(&bars[s], (i / C::NST) & 1));
+        if (!ok) {
+            failed_at = i;
+            break;
+        }
+        if (i == 0 || cc.t == 0) {
+            st.reset();
+            st.load_q(qbase + (static_cast<size_t>(cc.b) * p.Hq + cc.hk * GQ) * D, p.qscale);
+        }
+        const uint32_t kaddr = pa::smem_u32(ring + s * C::STAGE);
+        st.tile(kaddr, kaddr + C::TILE, min(C::TT, cc.L - cc.t * C::TT), pbuf, sbuf);
+        __syncwarp();
+        if (i + C::NST < my_n) {
+            if (kLanes) {
+                produce_tile_lanes<T, D, GQ>(p, pc, checked_block(p, pend), ring + s * C::STAGE,
+                                             &bars[s], lane);
+            } else if (lane == 0) {
+                pa::fence_proxy_async();
+                produce_tile<T, D, GQ>(p, pc, checked_block(p, pend), ring + s * C::STAGE,
+                                       &bars[s]);
+            }
+            if (pc.t == 0) prefetch_q<T, D, GQ>(p, pc, lane);
+            pc = next_unit(pc, bt, p.B, p.Hkv);
+            if ((kLanes || lane == 0) && i + C::NST + 1 < my_n)
+                pend = block_entry<C::TT>(p, pc, 0);
+        }
+        if (cc.t == cc.nt - 1 || i == my_n - 1) finish_segment<T, D, GQ>(st, p, bt, cc, per, w, lane);
+        cc = next_unit(cc, bt, p.B, p.Hkv);
+    }
+    if (failed_at >= 0) {
+        // A copy never completed: record it and wait (bounded) for this warp's
+        // other copies in flight so none lands after the CTA exits.
+        if (lane == 0) {
+            pa::record_error(p.err, PA_DEVERR_TIMEOUT);
+            const int last = min(failed_at + C::NST, my_n);
+            for (int i = failed_at + 1; i < last; ++i)
+                (void)pa::mbar_wait(&bars[i % C::NST], (i / C::NST) & 1);
+        }
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Grid kernel for batches too large for the persistent kernel's tables:
+// one CTA of kWarps warps per (sequence, KV head, partition of PT tokens).
+// ---------------------------------------------------------------------------
+template <typename T, int D, int GQ>
+__global__ void __launch_bounds__(kWarps * 32, (Cfg<T, D, GQ>::MINB)) decode_kernel(const DecodeParams p) {
     using C = Cfg<T, D, GQ>;
     extern __shared__ __align__(128) uint8_t smem[];
 
@@ -135,7 +804,6 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_kernel(const DecodePara
     const int ntok = min(L - tok0, p.PT);
     const int ntiles = (ntok + C::TT - 1) / C::TT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gl = lane % C::G, grp = lane / C::G;
 
     uint8_t *ring = smem + warp * C::WARP_SMEM;
     float *pbuf = reinterpret_cast<float *>(smem + C::OFF_P) + warp * 2 * C::TT * GQ;
@@ -195,172 +863,27 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_kernel(const DecodePara
         }
     };
 
-    // q of the GQ heads of this KV head, this lane's elements, pre-scaled.
-    float2 q2[GQ][C::P];
-    {
-        const T *qb = static_cast<const T *>(p.q) + (static_cast<size_t>(b) * p.Hq + hk * GQ) * D;
-#pragma unroll
-        for (int h = 0; h < GQ; ++h)
-#pragma unroll
-            for (int c = 0; c < C::CPL; ++c) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(
-                    qb + h * D + (c * C::G + gl) * C::EPC);
-                float2 f[C::EPC / 2];
-                pa::Elem<T>::unpack(raw, f);
-#pragma unroll
-                for (int i = 0; i < C::EPC / 2; ++i)
-                    q2[h][c * C::EPC / 2 + i] =
-                        make_float2(f[i].x * p.qscale, f[i].y * p.qscale);
-            }
-    }
+    WarpAttn<T, D, GQ> st;
+    st.init(lane);
+    st.qs = reinterpret_cast<float *>(smem + C::OFF_Q) + warp * GQ * D;
+    st.reset();
+    st.load_q(static_cast<const T *>(p.q) + (static_cast<size_t>(b) * p.Hq + hk * GQ) * D,
+              p.qscale);
 
     if (lane == 0)
         for (int i = 0; i < min(C::NST, my_ntiles); ++i) issue(i);
 
-    float m_run[GQ];
-    float2 acc[GQ][C::P];
-#pragma unroll
-    for (int h = 0; h < GQ; ++h) {
-        m_run[h] = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < C::P; ++j) acc[h][j] = make_float2(0.f, 0.f);
-    }
-    // After the transpose-reduce this lane holds the scores of step s_mine,
-    // heads h0 .. h0+VPL-1, i.e. token row row_mine of the tile.
-    const int h0 = (gl * C::VPL) % GQ;
-    const int row_mine = ((gl * C::VPL) / GQ) * C::TPS + grp;
-    float lsum[C::VPL], mh[C::VPL];
-#pragma unroll
-    for (int k = 0; k < C::VPL; ++k) {
-        lsum[k] = 0.f;
-        mh[k] = -INFINITY;
-    }
-
     int failed_at = -1;
     for (int i = 0; i < my_ntiles; ++i) {
-        const int st = i % C::NST;
-        const bool ok = __all_sync(pa::kFull, pa::mbar_wait(&bars[st], (i / C::NST) & 1));
+        const int s = i % C::NST;
+        const bool ok = __all_sync(pa::kFull, pa::mbar_wait(&bars[s], (i / C::NST) & 1));
         if (!ok) {
             failed_at = i;
             break;
         }
         const int nvalid = min(C::TT, ntok - (warp + i * kWarps) * C::TT);
-        const uint32_t kaddr = pa::smem_u32(ring + st * C::STAGE);
-        const uint32_t vaddr = kaddr + C::TILE;
-        const bool masked = nvalid < C::TT;
-
-        // ---- QK: partial dots of S token rows x GQ heads -----------------
-        float part_[C::V];
-#pragma unroll
-        for (int s = 0; s < C::S; ++s) {
-            const int row = s * C::TPS + grp;
-            float2 kf[C::P];
-#pragma unroll
-            for (int c = 0; c < C::CPL; ++c) {
-                const uint4 raw = pa::lds128(kaddr + row * C::ROW + (c * C::G + gl) * 16);
-                float2 f[C::EPC / 2];
-                pa::Elem<T>::unpack(raw, f);
-#pragma unroll
-                for (int j = 0; j < C::EPC / 2; ++j) kf[c * C::EPC / 2 + j] = f[j];
-            }
-#pragma unroll
-            for (int h = 0; h < GQ; ++h) {
-                float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int j = 0; j < C::P; ++j) a = pa::ffma2(q2[h][j], kf[j], a);
-                part_[s * GQ + h] = a.x + a.y;
-            }
-        }
-        transpose_reduce<C::V, C::G>(part_, lane);
-
-        float sc[C::VPL];
-        const bool row_valid = row_mine < nvalid;
-#pragma unroll
-        for (int k = 0; k < C::VPL; ++k) sc[k] = row_valid ? part_[k] : -INFINITY;
-
-        // ---- online softmax with lazy rescale -------------------------------
-        bool need = false;
-#pragma unroll
-        for (int k = 0; k < C::VPL; ++k) need |= sc[k] > mh[k] + kTau;
-        if (__any_sync(pa::kFull, need)) {
-#pragma unroll
-            for (int k = 0; k < C::VPL; ++k) sbuf[row_mine * GQ + h0 + k] = sc[k];
-            __syncwarp();
-            const int hh = lane % GQ;
-            float tmax = -INFINITY;
-            for (int r = 0; r < C::TT; ++r) tmax = fmaxf(tmax, sbuf[r * GQ + hh]);
-            float mold = m_run[0];
-#pragma unroll
-            for (int h = 1; h < GQ; ++h) mold = (hh == h) ? m_run[h] : mold;
-            const float mnew_l = fmaxf(mold, tmax);
-#pragma unroll
-            for (int h = 0; h < GQ; ++h) {
-                const float mnew = __shfl_sync(pa::kFull, mnew_l, h);
-                const float alpha = (m_run[h] == -INFINITY) ? 0.f : exp2f(m_run[h] - mnew);
-                const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-                for (int j = 0; j < C::P; ++j) acc[h][j] = __fmul2_rn(acc[h][j], a2);
-#pragma unroll
-                for (int k = 0; k < C::VPL; ++k)
-                    if (h == h0 + k) lsum[k] *= alpha;
-                m_run[h] = mnew;
-            }
-#pragma unroll
-            for (int k = 0; k < C::VPL; ++k) {
-                float m = m_run[0];
-#pragma unroll
-                for (int h = 1; h < GQ; ++h) m = (h == h0 + k) ? m_run[h] : m;
-                mh[k] = m;
-            }
-            __syncwarp();
-        }
-#pragma unroll
-        for (int k = 0; k < C::VPL; ++k) {
-            const float pk = fast_exp2(sc[k] - mh[k]);
-            lsum[k] += pk;
-            pbuf[row_mine * GQ + h0 + k] = pk;
-        }
-        __syncwarp();
-
-        // ---- PV ---------------------------------------------------------------
-#pragma unroll
-        for (int s = 0; s < C::S; ++s) {
-            const int row = s * C::TPS + grp;
-            float prow[GQ];
-            if constexpr (GQ % 4 == 0) {
-#pragma unroll
-                for (int h = 0; h < GQ; h += 4) {
-                    const float4 t4 = *reinterpret_cast<const float4 *>(pbuf + row * GQ + h);
-                    prow[h] = t4.x;
-                    prow[h + 1] = t4.y;
-                    prow[h + 2] = t4.z;
-                    prow[h + 3] = t4.w;
-                }
-            } else {
-#pragma unroll
-                for (int h = 0; h < GQ; ++h) prow[h] = pbuf[row * GQ + h];
-            }
-            float2 vf[C::P];
-#pragma unroll
-            for (int c = 0; c < C::CPL; ++c) {
-                const uint4 raw = pa::lds128(vaddr + row * C::ROW + (c * C::G + gl) * 16);
-                float2 f[C::EPC / 2];
-                pa::Elem<T>::unpack(raw, f);
-#pragma unroll
-                for (int j = 0; j < C::EPC / 2; ++j) vf[c * C::EPC / 2 + j] = f[j];
-            }
-            if (masked && row >= nvalid) {
-                // p is 0 there, but the stale row may hold NaN: 0 * NaN = NaN
-#pragma unroll
-                for (int j = 0; j < C::P; ++j) vf[j] = make_float2(0.f, 0.f);
-            }
-#pragma unroll
-            for (int h = 0; h < GQ; ++h) {
-                const float2 pp = make_float2(prow[h], prow[h]);
-#pragma unroll
-                for (int j = 0; j < C::P; ++j) acc[h][j] = pa::ffma2(pp, vf[j], acc[h][j]);
-            }
-        }
+        const uint32_t kaddr = pa::smem_u32(ring + s * C::STAGE);
+        st.tile(kaddr, kaddr + C::TILE, nvalid, pbuf, sbuf);
         __syncwarp();
         if (lane == 0 && i + C::NST < my_ntiles) {
             pa::fence_proxy_async();
@@ -382,48 +905,27 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_kernel(const DecodePara
         __syncwarp();
     }
 
-    // ---- warp epilogue: sum over token groups, l per head ---------------------
-#pragma unroll
-    for (int off = C::G; off < 32; off <<= 1)
-#pragma unroll
-        for (int h = 0; h < GQ; ++h)
-#pragma unroll
-            for (int j = 0; j < C::P; ++j) {
-                acc[h][j].x += __shfl_xor_sync(pa::kFull, acc[h][j].x, off);
-                acc[h][j].y += __shfl_xor_sync(pa::kFull, acc[h][j].y, off);
-            }
     float lh[GQ];
-#pragma unroll
-    for (int h = 0; h < GQ; ++h) {
-        float t = 0.f;
-#pragma unroll
-        for (int k = 0; k < C::VPL; ++k) t += (h == h0 + k) ? lsum[k] : 0.f;
-        lh[h] = t;
-    }
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1)
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) lh[h] += __shfl_xor_sync(pa::kFull, lh[h], off);
+    st.reduce(lh);
 
     // ---- CTA merge of the warps' (max, sum, acc) ----------------------------
     __syncthreads();  // every ring is drained: reuse it as the merge buffer
     float *wacc = reinterpret_cast<float *>(ring);  // [GQ][D]
     float *wml = wacc + GQ * D;                     // max[GQ], sum[GQ]
-    if (grp == 0) {
+    if (st.grp == 0) {
 #pragma unroll
         for (int h = 0; h < GQ; ++h)
 #pragma unroll
             for (int c = 0; c < C::CPL; ++c)
 #pragma unroll
-                for (int j = 0; j < C::EPC / 2; ++j) {
-                    const int dim = (c * C::G + gl) * C::EPC + 2 * j;
-                    *reinterpret_cast<float2 *>(wacc + h * D + dim) = acc[h][c * C::EPC / 2 + j];
-                }
+                for (int j = 0; j < C::EPC / 2; ++j)
+                    *reinterpret_cast<float2 *>(wacc + h * D + st.dim_of(c, j)) =
+                        st.acc[h][c * C::EPC / 2 + j];
     }
     if (lane == 0)
 #pragma unroll
         for (int h = 0; h < GQ; ++h) {
-            wml[h] = m_run[h];
+            wml[h] = st.m_run[h];
             wml[GQ + h] = lh[h];
         }
     __syncthreads();
@@ -499,8 +1001,46 @@ bool partition_ok(int pt, int bs) {
     return pt > 0 && pt <= kMaxPartition && pt % 32 == 0 && pt % bs == 0;
 }
 
+std::atomic<unsigned> g_epoch{0};
+
+unsigned next_epoch() {
+    unsigned e = ++g_epoch;
+    while (e == 0) e = ++g_epoch;
+    return e;
+}
+
+int sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return sms;
+}
+
 template <typename T, int D, int GQ>
-int launch(const DecodeParams &p, cudaStream_t stream) {
+int launch_persistent(const DecodeParams &p, cudaStream_t stream) {
+    using C = Cfg<T, D, GQ>;
+    const size_t smem = C::OFF_BT + sizeof(int32_t) * (2 * p.B + 1);
+    auto kern = decode_persistent_kernel<T, D, GQ>;
+    (void)cudaGetLastError();  // drop a stale error that is not ours
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return pa::cuda_fail(e, "decode: shared memory attribute");
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, smem);
+    if (e != cudaSuccess) return pa::cuda_fail(e, "decode: occupancy");
+#ifdef PA_DECODE_FORCE_PER_SM
+    per_sm = PA_DECODE_FORCE_PER_SM;
+#endif
+    const int sms = sm_count();
+    if (sms <= 0) return pa::fail(PA_ERR_CUDA, "decode: no SM count");
+    const int grid = sms * std::max(per_sm, 1);
+    kern<<<grid, kWarps * 32, smem, stream>>>(p);
+    return pa::check_launch("decode launch");
+}
+
+template <typename T, int D, int GQ>
+int launch_grid(const DecodeParams &p, cudaStream_t stream) {
     using C = Cfg<T, D, GQ>;
     const size_t smem = C::OFF_BT + sizeof(int32_t) * (p.PT / p.bs + 1);
     auto kern = decode_kernel<T, D, GQ>;
@@ -518,6 +1058,18 @@ int launch(const DecodeParams &p, cudaStream_t stream) {
     return PA_OK;
 }
 
+// The persistent kernel needs the batch's tile counts in shared memory and
+// 32-bit tile prefix sums.
+bool use_persistent(const DecodeParams &p) {
+    return p.B <= kPersistentMaxB && int64_t(p.B) * (int64_t(p.MB) << p.bs_log2) / 8 < (1ll << 31);
+}
+
+template <typename T, int D, int GQ>
+int launch(const DecodeParams &p, cudaStream_t stream) {
+    return use_persistent(p) ? launch_persistent<T, D, GQ>(p, stream)
+                             : launch_grid<T, D, GQ>(p, stream);
+}
+
 template <typename T, int D>
 int dispatch_gq(int gq, const DecodeParams &p, cudaStream_t s) {
     switch (gq) {
@@ -529,9 +1081,14 @@ int dispatch_gq(int gq, const DecodeParams &p, cudaStream_t s) {
     }
 }
 
-size_t workspace_bytes_for(int B, int Hq, int D, int max_parts) {
-    if (max_parts <= 1) return 0;
-    return static_cast<size_t>(B) * Hq * max_parts * (D + 2) * sizeof(float);
+// Workspace: tickets [B][Hq] (u64), then acc [B][Hq][maxseg][D], then
+// (max, sum) [B][Hq][maxseg][2]; maxseg = partitions per sequence + 1 bounds
+// the segments of one item in the persistent kernel and the partitions of the
+// grid kernel.
+size_t workspace_bytes_for(int B, int Hq, int D, int maxseg) {
+    if (B <= 0) return 0;
+    return static_cast<size_t>(B) * Hq *
+           (sizeof(unsigned long long) + static_cast<size_t>(maxseg) * (D + 2) * sizeof(float));
 }
 
 }  // namespace
@@ -549,8 +1106,8 @@ int pa_decode_workspace_size(int B, int Hq, int head_dim, int max_blocks_per_seq
     if (!partition_ok(pt, block_size))
         return pa::fail(PA_ERR_INVALID, "workspace_size: bad partition_tokens %d", pt);
     const int64_t cap = int64_t(max_blocks_per_seq) * block_size;
-    const int max_parts = static_cast<int>((cap + pt - 1) / pt);
-    *bytes = workspace_bytes_for(B, Hq, head_dim, max_parts);
+    const int maxseg = static_cast<int>((cap + pt - 1) / pt) + 1;
+    *bytes = workspace_bytes_for(B, Hq, head_dim, maxseg);
     return PA_OK;
 }
 
@@ -583,15 +1140,16 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     if (B == 0) return PA_OK;
     if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens)
         return pa::fail(PA_ERR_INVALID, "decode: NULL pointer");
-    if (!pa::aligned16(q) || !pa::aligned16(k_cache) || !pa::aligned16(v_cache))
-        return pa::fail(PA_ERR_INVALID, "decode: q and pools must be 16-byte aligned");
+    if (!pa::aligned16(q) || !pa::aligned16(out) || !pa::aligned16(k_cache) ||
+        !pa::aligned16(v_cache))
+        return pa::fail(PA_ERR_INVALID, "decode: q, out and pools must be 16-byte aligned");
     const int64_t cap = int64_t(max_blocks_per_seq) * block_size;
     const int max_parts = static_cast<int>((cap + pt - 1) / pt);
-    const size_t need = workspace_bytes_for(B, Hq, head_dim, max_parts);
-    if (need > workspace_bytes || (need && !workspace))
+    const size_t need = workspace_bytes_for(B, Hq, head_dim, max_parts + 1);
+    if (need > workspace_bytes || !workspace)
         return pa::fail(PA_ERR_INVALID, "decode: workspace needs %zu bytes, got %zu", need,
                         workspace_bytes);
-    if (need && !pa::aligned16(workspace))
+    if (!pa::aligned16(workspace))
         return pa::fail(PA_ERR_INVALID, "decode: workspace must be 16-byte aligned");
     if (pa::validate_on()) {
         std::vector<int32_t> lens(B), table(size_t(B) * max_blocks_per_seq);
@@ -618,8 +1176,9 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     p.v_cache = static_cast<const uint8_t *>(v_cache);
     p.block_table = block_table;
     p.context_lens = context_lens;
-    p.ws_acc = static_cast<float *>(workspace);
-    p.ws_ml = need ? p.ws_acc + size_t(B) * Hq * max_parts * head_dim : nullptr;
+    p.ctr = static_cast<unsigned long long *>(workspace);
+    p.ws_acc = reinterpret_cast<float *>(p.ctr + size_t(B) * Hq);
+    p.ws_ml = p.ws_acc + size_t(B) * Hq * (max_parts + 1) * head_dim;
     p.err = pa::device_error_word();
     p.num_blocks = num_blocks;
     p.B = B;
@@ -629,7 +1188,9 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     p.bs_log2 = log2_int(block_size);
     p.MB = max_blocks_per_seq;
     p.PT = pt;
-    p.max_parts = max_parts;
+    p.max_parts = max_parts + 1;  // slot stride of both kernels
+    p.maxseg = max_parts + 1;
+    p.epoch = next_epoch();
     p.qscale = scale * kLog2e;
     const int gq = Hq / Hkv;
     if (dtype == PA_BF16)
@@ -640,7 +1201,6 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
 }
 
 }  // extern "C"
-
 // ---------------------------------------------------------------------------
 // Allocation-free variant of pa_decode.
 //

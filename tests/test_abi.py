@@ -44,10 +44,11 @@ def test_version(lib):
 
 def test_workspace_size_host_only(lib):
     from paged_kv_cache_192_gb300 import ops
-    # 8B-shaped: 64 seqs, 32 heads, d 128, 256 blocks of 16 -> 8 partitions of 512
-    assert ops.decode_workspace_size(64, 32, 128, 256, 16, 512) == 64 * 32 * 8 * 130 * 4
-    # one partition covers every sequence: no workspace
-    assert ops.decode_workspace_size(4, 4, 64, 4, 16, 0) == 0
+    # 8B-shaped: 64 seqs, 32 heads, d 128, 256 blocks of 16 -> 8 partitions of
+    # 512 + 1 segment slots per (sequence, head), plus one 8-byte ticket each
+    assert ops.decode_workspace_size(64, 32, 128, 256, 16, 512) == 64 * 32 * (8 + 9 * 130 * 4)
+    assert ops.decode_workspace_size(4, 4, 64, 4, 16, 0) == 4 * 4 * (8 + 2 * 66 * 4)
+    assert ops.decode_workspace_size(0, 4, 64, 4, 16, 0) == 0
 
 
 @pytest.mark.parametrize("kw,code", [

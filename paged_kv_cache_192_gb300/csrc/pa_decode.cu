@@ -601,52 +601,56 @@ __device__ __forceinline__ void finish_segment(WarpAttn<T, D, GQ> &st, const Dec
     __syncwarp();
     // Merge: lane s < nseg holds segment s's (max, sum) per head; every lane
     // owns D/32 output elements; all loads are independent (issued ahead).
+    // Heads go in groups of up to 4 so the accumulators stay in registers.
     constexpr int EL = D / 32;
-    float wsh[GQ], inv[GQ];
+    constexpr int HB = GQ < 4 ? GQ : 4;
+#pragma unroll 1
+    for (int hb = 0; hb < GQ; hb += HB) {
+        float wsh[HB], inv[HB], accm[HB][EL];
 #pragma unroll
-    for (int h = 0; h < GQ; ++h) {
-        const size_t sb = (hq0 + h) * p.maxseg;
-        float2 ml = make_float2(-INFINITY, 0.f);
-        if (lane < nseg) ml = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + 2 * (sb + lane)));
-        float M = ml.x;
+        for (int hh = 0; hh < HB; ++hh) {
+            const size_t sb = (hq0 + hb + hh) * p.maxseg;
+            float2 ml = make_float2(-INFINITY, 0.f);
+            if (lane < nseg)
+                ml = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + 2 * (sb + lane)));
+            float M = ml.x;
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(pa::kFull, M, o));
-        wsh[h] = lane < nseg ? exp2f(ml.x - M) : 0.f;
-        float den = wsh[h] * ml.y;
+            for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(pa::kFull, M, o));
+            wsh[hh] = lane < nseg ? exp2f(ml.x - M) : 0.f;
+            float den = wsh[hh] * ml.y;
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(pa::kFull, den, o);
-        inv[h] = 1.f / den;
-    }
-    float accm[GQ][EL];
+            for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(pa::kFull, den, o);
+            inv[hh] = 1.f / den;
 #pragma unroll
-    for (int h = 0; h < GQ; ++h)
+            for (int e = 0; e < EL; ++e) accm[hh][e] = 0.f;
+        }
+        constexpr int kUnr = GQ >= 8 ? 2 : 4;
+#pragma unroll kUnr
+        for (int sgi = 0; sgi < nseg; ++sgi) {
 #pragma unroll
-        for (int e = 0; e < EL; ++e) accm[h][e] = 0.f;
-#pragma unroll 4
-    for (int sgi = 0; sgi < nseg; ++sgi) {
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) {
-            const float wv = __shfl_sync(pa::kFull, wsh[h], sgi);
-            const float *src = p.ws_acc + ((hq0 + h) * p.maxseg + sgi) * D + EL * lane;
-            if constexpr (EL == 4) {
-                const float4 a = __ldcg(reinterpret_cast<const float4 *>(src));
-                accm[h][0] += wv * a.x;
-                accm[h][1] += wv * a.y;
-                accm[h][2] += wv * a.z;
-                accm[h][3] += wv * a.w;
-            } else {
-                const float2 a = __ldcg(reinterpret_cast<const float2 *>(src));
-                accm[h][0] += wv * a.x;
-                accm[h][1] += wv * a.y;
+            for (int hh = 0; hh < HB; ++hh) {
+                const float wv = __shfl_sync(pa::kFull, wsh[hh], sgi);
+                const float *src = p.ws_acc + ((hq0 + hb + hh) * p.maxseg + sgi) * D + EL * lane;
+                if constexpr (EL == 4) {
+                    const float4 a = __ldcg(reinterpret_cast<const float4 *>(src));
+                    accm[hh][0] += wv * a.x;
+                    accm[hh][1] += wv * a.y;
+                    accm[hh][2] += wv * a.z;
+                    accm[hh][3] += wv * a.w;
+                } else {
+                    const float2 a = __ldcg(reinterpret_cast<const float2 *>(src));
+                    accm[hh][0] += wv * a.x;
+                    accm[hh][1] += wv * a.y;
+                }
             }
         }
+#pragma unroll
+        for (int hh = 0; hh < HB; ++hh)
+#pragma unroll
+            for (int e = 0; e < EL; e += 2)
+                store_pair<T>(out + (hq0 + hb + hh) * D + EL * lane + e, accm[hh][e] * inv[hh],
+                              accm[hh][e + 1] * inv[hh]);
     }
-#pragma unroll
-    for (int h = 0; h < GQ; ++h)
-#pragma unroll
-        for (int e = 0; e < EL; e += 2)
-            store_pair<T>(out + (hq0 + h) * D + EL * lane + e, accm[h][e] * inv[h],
-                          accm[h][e + 1] * inv[h]);
     if (lane == 0) atomicExch(ctr, 0ull);
 }
 

@@ -1,13 +1,24 @@
 """Benchmark of the paged-attention hot path on GB300.
 
-One step = one pass of the decode hot path over one batch of the
-Llama-3-8B-shaped workload (64 sequences, L ~ U[128,4096], 32 query / 8 KV
-heads, head_dim 128, bf16, 16-token blocks in a shuffled pool 1.2x the need):
-pa_reshape_and_cache of the 64 new tokens, then pa_decode (split-KV partials
-+ log-sum-exp merge).  Inputs are resident in HBM and larger than L2; three
-independent pools are rotated between steps.
+A step is one pass of the hot path over one batch, every call through the C
+ABI of include/pa.h, inputs resident in HBM:
 
-Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+* 8b (default, the headline): Llama-3-8B-shaped decode batch (64 sequences,
+  L ~ U[128,4096], 32 query / 8 KV heads, head_dim 128, bf16, 16-token blocks
+  shuffled over a pool 1.2x the need): pa_reshape_and_cache of the 64 new
+  tokens, then pa_decode (persistent kernel, split-KV merged inside).
+* 70b: Llama-3-70B-shaped long-context decode (32 sequences, L ~ U[16k,32k],
+  64/8 heads, 32-token blocks, 512-token split-KV partitions).
+* prefix: 256 sequences sharing a 1024-token system prompt plus 64
+  parallel-sampling forks set up through the native block manager; the step
+  runs the fork's copy-on-write block copies, stores the 320 new tokens and
+  decodes all 320 sequences.
+* mixed: continuous batch of 128 decodes (L ~ U[256,8192]) and 4 chunked-prefill
+  requests of 512 tokens over 0..3584 prior tokens in one pool; the step stores
+  all 2176 new tokens, decodes and runs the prefill chunks.
+
+Inputs are larger than L2 and three independent pools are rotated between
+steps.  Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
 oracle on a bounded sample of the same workload instead.
 
 Multi-GPU: sequences are independent, so every rank runs its own replica of
@@ -37,7 +48,8 @@ if ROOT not in sys.path:
 from paged_kv_cache_192_gb300 import synth  # noqa: E402
 
 METRIC = "paged decode attn: KV GB/s (% of GB300 HBM peak) and tokens/s at 1 GPU"
-WORKLOAD = "llama3-8b-gqa-decode"
+WORKLOADS = {"8b": "llama3-8b-gqa-decode", "70b": "llama3-70b-long-decode",
+             "prefix": "shared-prefix-decode-with-forks", "mixed": "mixed-decode-prefill-batch"}
 N_POOLS = 3
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -86,20 +98,27 @@ def reduce_sum(value, world, device="cpu"):
 # workload accounting
 # ----------------------------------------------------------------------------
 
-def decode_bytes(w):
-    """Algorithmic HBM bytes of one pa_decode: every cached token's K and V
-    row once per KV head, q and out once, the block-table entries read, the
+def _es(dtype):
+    return 2 if dtype == torch.bfloat16 else 4
+
+
+def decode_bytes(lens, B, Hq, Hkv, d, bs, dtype):
+    """Algorithmic HBM bytes of one pa_decode: every cached token's K and V row
+    once per KV head, q and out once, the block-table entries read and the
     context lengths.  Split-KV partials are overhead, not counted."""
-    es = 2 if w.dtype == torch.bfloat16 else 4
-    kv = int(w.lens.sum()) * 2 * w.Hkv * w.d * es
-    qo = 2 * w.B * w.Hq * w.d * es
-    tables = int(sum(-(-int(L) // w.bs) for L in w.lens)) * 4 + w.B * 4
-    return kv + qo + tables
+    es = _es(dtype)
+    kv = int(np.sum(lens)) * 2 * Hkv * d * es
+    return kv + 2 * B * Hq * d * es + int(sum(-(-int(L) // bs) for L in lens)) * 4 + B * 4
 
 
-def reshape_bytes(w):
-    es = 2 if w.dtype == torch.bfloat16 else 4
-    return w.B * (2 * 2 * w.Hkv * w.d * es + 8)  # read + write K and V rows, slot
+def store_bytes(T, Hkv, d, dtype):
+    """pa_reshape_and_cache: read and write of T rows of K and V, slots."""
+    return T * (2 * 2 * Hkv * d * _es(dtype) + 8)
+
+
+def prefill_flops(priors, n_new, Hq, d):
+    """QK^T and PV of causal chunks: 4*Hq*d*(n*P + n(n+1)/2) per request."""
+    return int(sum(4 * Hq * d * (n * P + n * (n + 1) // 2) for P, n in zip(priors, n_new)))
 
 
 def peaks():
@@ -107,29 +126,29 @@ def peaks():
     if os.path.exists(path):
         with open(path) as f:
             j = json.load(f)
-        return float(j["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return float(j["hbm_gbs"]), float(j["bf16_tflops_sustained"]), "measured"
+    return 6800.0, 1700.0, "fallback"
 
 
-def kernel_traffic():
-    """ncu DRAM bytes per decode launch, if recorded for the current kernel
+def source_sha1(*names):
+    h = hashlib.sha1()
+    for name in names:
+        with open(os.path.join(ROOT, "paged_kv_cache_192_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def kernel_traffic(record, *sources):
+    """ncu DRAM bytes per launch of a kernel, if recorded for its current
     source (else None)."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    path = os.path.join(ROOT, "profiles", record)
     if not os.path.exists(path):
         return None
     with open(path) as f:
         j = json.load(f)
-    if j.get("source_sha1") != source_sha1():
+    if j.get("source_sha1") != source_sha1(*sources):
         return None
     return j.get("bytes_per_launch")
-
-
-def source_sha1():
-    h = hashlib.sha1()
-    for name in ("pa_decode.cu", "pa_device.cuh"):
-        with open(os.path.join(ROOT, "paged_kv_cache_192_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
-    return h.hexdigest()
 
 
 # ----------------------------------------------------------------------------
@@ -140,7 +159,6 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.proc = None
         self.gpu = gpu_index
-        self.t0 = None
 
     def start(self):
         try:
@@ -183,135 +201,384 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
+# step plans
+# ----------------------------------------------------------------------------
+
+class Plan:
+    """Device-resident inputs of one workload and the calls of one step."""
+
+    def __init__(self, name):
+        self.name = name
+        self.pools = []        # [(k_cache, v_cache)]
+        self.inputs = {}       # name -> device tensor re-sent each e2e step
+        self.outputs = {}      # name -> device tensor read back each e2e step
+        self.config = {}
+        self.extra = {}
+        self.step_bytes = 0    # algorithmic bytes of one step (the metric's unit)
+        self.tokens = 0        # query tokens produced per step
+        self.decode_bytes = 0
+        self.prefill_flops = 0
+        self.launches = 0
+        self.oracle_sample = None  # callable(n_seq, seed) -> (seconds, bytes, n) on the host
+
+    def run(self, i, L, sp, ev=None, src=None):
+        raise NotImplementedError
+
+
+def _slots_last(table, lens, bs):
+    from paged_kv_cache_192_gb300 import layout
+    return np.array([layout.slots_for(table[s], [lens[s] - 1], bs)[0] for s in range(len(lens))],
+                    dtype=np.int64)
+
+
+class DecodePlan(Plan):
+    """Store each sequence's newest token, then decode the batch."""
+
+    def __init__(self, name, dev, args):
+        super().__init__(name)
+        from paged_kv_cache_192_gb300 import layout, ops
+        gen_dev = "cuda" if name == "70b" else "cpu"
+        w = synth.decode_workload(name, seed=args.seed, gen_device=gen_dev)
+        self.w = w
+        for _ in range(args.pools):
+            kc, vc = layout.alloc_pools(w.num_blocks, w.Hkv, w.bs, w.d, w.dtype, dev, poison=False)
+            layout.fill_pools(kc, vc, w.k, w.v, w.table, w.lens, w.bs)
+            self.pools.append((kc, vc))
+        if w.k.is_cuda:  # keep only the pools on the device
+            w.k, w.v, w.q = w.k.cpu(), w.v.cpu(), w.q.cpu()
+        last = torch.from_numpy(w.kv_offsets + w.lens - 1)
+        self.inputs = {
+            "q": w.q.to(dev), "k_new": w.k[last].contiguous().to(dev),
+            "v_new": w.v[last].contiguous().to(dev),
+            "slots": torch.from_numpy(_slots_last(w.table, w.lens, w.bs)).to(dev),
+            "table": torch.from_numpy(w.table).to(dev),
+            "lens": torch.from_numpy(w.lens.astype(np.int32)).to(dev)}
+        self.outputs = {"out": torch.empty_like(self.inputs["q"])}
+        self.PT = args.partition
+        self.ws_bytes = ops.decode_workspace_size(w.B, w.Hq, w.d, w.max_blocks, w.bs, self.PT)
+        self.ws = torch.zeros(max(self.ws_bytes // 4, 1), dtype=torch.float32, device=dev)
+        self.decode_bytes = decode_bytes(w.lens, w.B, w.Hq, w.Hkv, w.d, w.bs, w.dtype)
+        self.step_bytes = self.decode_bytes + store_bytes(w.B, w.Hkv, w.d, w.dtype)
+        self.tokens = w.B
+        self.launches = 2
+        lo, hi = synth.CONFIGS[name]["len_range"]
+        self.config = {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d, "block_size": w.bs,
+                       "context_len": f"U[{lo},{hi}] seed {args.seed}",
+                       "total_context_tokens": int(w.lens.sum()), "pool_blocks": w.num_blocks,
+                       "partition_tokens": self.PT}
+        self.oracle_sample = lambda n, seed: time_oracle_decode(w, n, seed)
+
+    def run(self, i, L, sp, ev=None, src=None):
+        from paged_kv_cache_192_gb300._lib import PA_BF16, check
+        w, x = self.w, (src or self.inputs)
+        kc, vc = self.pools[i % len(self.pools)]
+        check(L.pa_reshape_and_cache(x["k_new"].data_ptr(), x["v_new"].data_ptr(), kc.data_ptr(),
+                                     vc.data_ptr(), x["slots"].data_ptr(), w.B, w.num_blocks,
+                                     w.Hkv, w.bs, w.d, PA_BF16, sp))
+        if ev:
+            ev["decode"][0].record()
+        check(L.pa_decode(self.outputs["out"].data_ptr(), x["q"].data_ptr(), kc.data_ptr(),
+                          vc.data_ptr(), x["table"].data_ptr(), w.max_blocks,
+                          x["lens"].data_ptr(), w.B, w.Hq, w.Hkv, w.d, w.bs, w.num_blocks,
+                          1.0 / math.sqrt(w.d), self.PT, self.ws.data_ptr(), self.ws_bytes,
+                          PA_BF16, sp))
+        if ev:
+            ev["decode"][1].record()
+
+
+class PrefixPlan(Plan):
+    """Shared system prompt + private suffixes + 64 forks, through the native
+    block manager; step = CoW block copies, store 320 new tokens, decode 320."""
+
+    def __init__(self, dev, args):
+        super().__init__("prefix")
+        from paged_kv_cache_192_gb300 import ops
+        from paged_kv_cache_192_gb300.block_manager import BlockManager
+        cfg = synth.CONFIGS["prefix"]
+        w = synth.prefix_workload(seed=args.seed)
+        P, suffix = w.extra["prefix"], w.extra["suffix"]
+        Hkv, d, bs, Hq = w.Hkv, w.d, w.bs, w.Hq
+        B, nf = w.B, cfg["forks"]
+        offs = w.kv_offsets
+        need = P // bs + sum(-(-int(s) // bs) for s in suffix)
+        NB = int(math.ceil(1.2 * need)) + 2 * nf
+        bm = BlockManager(NB, bs, seed=args.seed + 5)
+        SYS = 1 << 40
+        prompt_slots = bm.add_seq(SYS, P)
+        hist_slots = []
+        for s in range(B):
+            bm.fork(SYS, s)
+            sl, _ = bm.append_n(s, int(suffix[s]) - 1)
+            hist_slots.append(sl)
+        rng = np.random.default_rng(args.seed + 6)
+        parents = np.sort(rng.choice(B, size=nf, replace=False))
+        children = [(1 << 41) + i for i in range(nf)]
+        for par, ch in zip(parents, children):
+            bm.fork(int(par), ch)
+        order = list(range(B)) + children
+        new_slots, pairs = [], []
+        for seq in order:  # ascending ids: parents write (and copy) before children
+            slot, a, b = bm.append(seq)
+            new_slots.append(slot)
+            if a >= 0:
+                pairs.append((a, b))
+        MB = max(len(bm.seq_blocks(s)) for s in order)
+        table = bm.block_table(order, MB)
+        lens = np.array([bm.seq_len(s) for s in order], dtype=np.int64)
+        gen = torch.Generator().manual_seed(args.seed + 7)
+        kn_children = torch.randn(nf, Hkv, d, generator=gen).to(w.dtype)
+        vn_children = torch.randn(nf, Hkv, d, generator=gen).to(w.dtype)
+        q_children = torch.randn(nf, Hq, d, generator=gen).to(w.dtype)
+        last = torch.from_numpy(offs + w.lens - 1)
+        k_new = torch.cat([w.k[last], kn_children])
+        v_new = torch.cat([w.v[last], vn_children])
+        hs = np.concatenate(hist_slots)
+        rows = torch.from_numpy(np.concatenate(
+            [np.arange(offs[s] + P, offs[s] + w.lens[s] - 1) for s in range(B)]))
+        for _ in range(args.pools):
+            kc = torch.zeros(NB, Hkv, bs, d, dtype=w.dtype, device=dev)
+            vc = torch.zeros_like(kc)
+            # prompt once, then each sequence's private history (all but its newest token)
+            ops.reshape_and_cache(w.k[:P].to(dev), w.v[:P].to(dev), kc, vc,
+                                  torch.from_numpy(prompt_slots).to(dev))
+            ops.reshape_and_cache(w.k[rows].to(dev), w.v[rows].to(dev), kc, vc,
+                                  torch.from_numpy(hs).to(dev))
+            self.pools.append((kc, vc))
+        self.NB, self.MB, self.Bd = NB, MB, len(order)
+        self.Hq, self.Hkv, self.d, self.bs, self.dtype = Hq, Hkv, d, bs, w.dtype
+        self.npairs = len(pairs)
+        self.inputs = {
+            "q": torch.cat([w.q, q_children]).to(dev), "k_new": k_new.to(dev),
+            "v_new": v_new.to(dev),
+            "slots": torch.tensor(new_slots, dtype=torch.int64, device=dev),
+            "table": torch.from_numpy(table).to(dev),
+            "lens": torch.from_numpy(lens.astype(np.int32)).to(dev),
+            "pairs": torch.tensor(pairs if pairs else [[0, 0]], dtype=torch.int64, device=dev)}
+        self.outputs = {"out": torch.empty_like(self.inputs["q"])}
+        self.PT = args.partition
+        self.ws_bytes = ops.decode_workspace_size(self.Bd, Hq, d, MB, bs, self.PT)
+        self.ws = torch.zeros(max(self.ws_bytes // 4, 1), dtype=torch.float32, device=dev)
+        es = _es(w.dtype)
+        self.decode_bytes = decode_bytes(lens, self.Bd, Hq, Hkv, d, bs, w.dtype)
+        used = set()
+        for r, L in enumerate(lens):
+            used.update(table[r, :-(-int(L) // bs)].tolist())
+        unique = len(used) * Hkv * bs * d * es * 2
+        self.step_bytes = (self.decode_bytes + store_bytes(self.Bd, Hkv, d, w.dtype) +
+                           self.npairs * 2 * 2 * Hkv * bs * d * es)
+        self.tokens = self.Bd
+        self.launches = 3 if self.npairs else 2
+        self.extra = {"unique_kv_bytes": unique, "logical_kv_bytes": self.decode_bytes,
+                      "cow_pairs": self.npairs}
+        self.config = {"B": self.Bd, "sequences": f"{B} sharing a {P}-token prompt + {nf} forks",
+                       "suffix_len": "U[1,512]", "Hq": Hq, "Hkv": Hkv, "head_dim": d,
+                       "block_size": bs, "pool_blocks": NB, "partition_tokens": self.PT,
+                       "cow_pairs": self.npairs}
+        self.oracle_sample = lambda n, seed: time_oracle_decode(w, n, seed)
+
+    def run(self, i, L, sp, ev=None, src=None):
+        from paged_kv_cache_192_gb300._lib import PA_BF16, check
+        x = src or self.inputs
+        kc, vc = self.pools[i % len(self.pools)]
+        if self.npairs:
+            check(L.pa_copy_blocks(kc.data_ptr(), vc.data_ptr(), x["pairs"].data_ptr(),
+                                   self.npairs, self.NB, self.Hkv, self.bs, self.d, PA_BF16, sp))
+        check(L.pa_reshape_and_cache(x["k_new"].data_ptr(), x["v_new"].data_ptr(), kc.data_ptr(),
+                                     vc.data_ptr(), x["slots"].data_ptr(), self.Bd, self.NB,
+                                     self.Hkv, self.bs, self.d, PA_BF16, sp))
+        if ev:
+            ev["decode"][0].record()
+        check(L.pa_decode(self.outputs["out"].data_ptr(), x["q"].data_ptr(), kc.data_ptr(),
+                          vc.data_ptr(), x["table"].data_ptr(), self.MB, x["lens"].data_ptr(),
+                          self.Bd, self.Hq, self.Hkv, self.d, self.bs, self.NB,
+                          1.0 / math.sqrt(self.d), self.PT, self.ws.data_ptr(), self.ws_bytes,
+                          PA_BF16, sp))
+        if ev:
+            ev["decode"][1].record()
+
+
+class MixedPlan(Plan):
+    """128 decodes + 4 chunked-prefill requests sharing one pool."""
+
+    def __init__(self, dev, args):
+        super().__init__("mixed")
+        from paged_kv_cache_192_gb300 import layout, ops
+        dec, pre = synth.mixed_workload(seed=args.seed)
+        self.dec, self.pre = dec, pre
+        n, R = pre.extra["chunk"], pre.B
+        priors = pre.extra["prior"]
+        doffs, poffs = dec.kv_offsets, pre.kv_offsets
+        # history = every decode token but the newest and every prior prefill token
+        hist_rows_d = np.concatenate([np.arange(doffs[s], doffs[s] + dec.lens[s] - 1)
+                                      for s in range(dec.B)])
+        hist_slots_d = np.concatenate([layout.slots_for(dec.table[s], np.arange(dec.lens[s] - 1),
+                                                        dec.bs) for s in range(dec.B)])
+        hist_rows_p = np.concatenate([np.arange(poffs[r], poffs[r] + priors[r]) for r in range(R)])
+        hist_slots_p = np.concatenate([layout.slots_for(pre.table[r], np.arange(priors[r]),
+                                                        pre.bs) for r in range(R)])
+        new_rows_p = np.concatenate([np.arange(poffs[r] + priors[r], poffs[r] + pre.lens[r])
+                                     for r in range(R)])
+        new_slots_p = np.concatenate([layout.slots_for(pre.table[r],
+                                                       np.arange(priors[r], pre.lens[r]), pre.bs)
+                                      for r in range(R)])
+        for _ in range(args.pools):
+            kc, vc = layout.alloc_pools(dec.num_blocks, dec.Hkv, dec.bs, dec.d, dec.dtype, dev,
+                                        poison=False)
+            ops.reshape_and_cache(dec.k[hist_rows_d].to(dev), dec.v[hist_rows_d].to(dev), kc, vc,
+                                  torch.from_numpy(hist_slots_d).to(dev))
+            if len(hist_rows_p):
+                ops.reshape_and_cache(pre.k[hist_rows_p].to(dev), pre.v[hist_rows_p].to(dev), kc,
+                                      vc, torch.from_numpy(hist_slots_p).to(dev))
+            self.pools.append((kc, vc))
+        last = torch.from_numpy(doffs + dec.lens - 1)
+        k_new = torch.cat([dec.k[last], pre.k[new_rows_p]])
+        v_new = torch.cat([dec.v[last], pre.v[new_rows_p]])
+        slots = np.concatenate([_slots_last(dec.table, dec.lens, dec.bs), new_slots_p])
+        self.inputs = {
+            "q": dec.q.to(dev), "qp": pre.q.to(dev), "k_new": k_new.to(dev),
+            "v_new": v_new.to(dev), "slots": torch.from_numpy(slots).to(dev),
+            "table": torch.from_numpy(np.ascontiguousarray(dec.table)).to(dev),
+            "lens": torch.from_numpy(dec.lens.astype(np.int32)).to(dev),
+            "ptable": torch.from_numpy(np.ascontiguousarray(pre.table)).to(dev),
+            "plens": torch.from_numpy(pre.lens.astype(np.int32)).to(dev),
+            "qstart": torch.arange(0, (R + 1) * n, n, dtype=torch.int32, device=dev)}
+        self.outputs = {"out": torch.empty_like(self.inputs["q"]),
+                        "outp": torch.empty_like(self.inputs["qp"])}
+        self.T = len(slots)
+        self.n, self.R = n, R
+        self.PT = args.partition
+        self.ws_bytes = ops.decode_workspace_size(dec.B, dec.Hq, dec.d, dec.max_blocks, dec.bs,
+                                                  self.PT)
+        self.ws = torch.zeros(max(self.ws_bytes // 4, 1), dtype=torch.float32, device=dev)
+        self.decode_bytes = decode_bytes(dec.lens, dec.B, dec.Hq, dec.Hkv, dec.d, dec.bs,
+                                         dec.dtype)
+        es = _es(dec.dtype)
+        prefill_kv = (int(pre.lens.sum()) * 2 * pre.Hkv * pre.d * es +
+                      2 * R * n * pre.Hq * pre.d * es)
+        self.step_bytes = (self.decode_bytes + prefill_kv +
+                           store_bytes(self.T, dec.Hkv, dec.d, dec.dtype))
+        self.prefill_flops = prefill_flops(priors, [n] * R, pre.Hq, pre.d)
+        self.tokens = dec.B + R * n
+        self.launches = 3
+        self.extra = {"prefill_flops": self.prefill_flops, "priors": [int(x) for x in priors]}
+        self.config = {"B_decode": dec.B, "decode_len": "U[256,8192]", "prefill_requests": R,
+                       "chunk": n, "priors": [int(x) for x in priors], "Hq": dec.Hq,
+                       "Hkv": dec.Hkv, "head_dim": dec.d, "block_size": dec.bs,
+                       "pool_blocks": dec.num_blocks, "partition_tokens": self.PT}
+        self.oracle_sample = lambda k, seed: time_oracle_decode(dec, k, seed)
+
+    def run(self, i, L, sp, ev=None, src=None):
+        from paged_kv_cache_192_gb300._lib import PA_BF16, check
+        dec, pre, x = self.dec, self.pre, (src or self.inputs)
+        kc, vc = self.pools[i % len(self.pools)]
+        check(L.pa_reshape_and_cache(x["k_new"].data_ptr(), x["v_new"].data_ptr(), kc.data_ptr(),
+                                     vc.data_ptr(), x["slots"].data_ptr(), self.T, dec.num_blocks,
+                                     dec.Hkv, dec.bs, dec.d, PA_BF16, sp))
+        if ev:
+            ev["decode"][0].record()
+        check(L.pa_decode(self.outputs["out"].data_ptr(), x["q"].data_ptr(), kc.data_ptr(),
+                          vc.data_ptr(), x["table"].data_ptr(), dec.max_blocks,
+                          x["lens"].data_ptr(), dec.B, dec.Hq, dec.Hkv, dec.d, dec.bs,
+                          dec.num_blocks, 1.0 / math.sqrt(dec.d), self.PT, self.ws.data_ptr(),
+                          self.ws_bytes, PA_BF16, sp))
+        if ev:
+            ev["decode"][1].record()
+            ev["prefill"][0].record()
+        check(L.pa_prefill_chunk(self.outputs["outp"].data_ptr(), x["qp"].data_ptr(),
+                                 kc.data_ptr(), vc.data_ptr(), x["ptable"].data_ptr(),
+                                 pre.max_blocks, x["qstart"].data_ptr(), x["plens"].data_ptr(),
+                                 self.R, self.n, pre.Hq, pre.Hkv, pre.d, pre.bs, dec.num_blocks,
+                                 1.0 / math.sqrt(pre.d), PA_BF16, sp))
+        if ev:
+            ev["prefill"][1].record()
+
+
+def make_plan(name, dev, args):
+    if name in ("8b", "70b"):
+        return DecodePlan(name, dev, args)
+    if name == "prefix":
+        return PrefixPlan(dev, args)
+    return MixedPlan(dev, args)
+
+
+# ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
+
+def _events(n, keys):
+    return [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for k in keys} for _ in range(n)]
+
 
 def run_gpu(args, world, rank, local):
     from paged_kv_cache_192_gb300 import build
     build.build()
-    from paged_kv_cache_192_gb300 import layout, ops
-    from paged_kv_cache_192_gb300._lib import PA_BF16, check, lib
+    from paged_kv_cache_192_gb300._lib import lib
 
     assert torch.cuda.is_available(), "the GPU arm needs a CUDA device"
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     init_dist(world, "nccl")
-    w = synth.decode_workload("8b", seed=args.seed)
-    B, Hq, Hkv, d, bs = w.B, w.Hq, w.Hkv, w.d, w.bs
-    MB = w.max_blocks
-    PT = args.partition
-    scale = 1.0 / math.sqrt(d)
-
-    # resident inputs: N_POOLS independent pools (each 1.2x the batch's blocks)
-    pools = []
-    for _ in range(args.pools):
-        kc, vc = layout.alloc_pools(w.num_blocks, Hkv, bs, d, w.dtype, dev, poison=False)
-        layout.fill_pools(kc, vc, w.k, w.v, w.table, w.lens, bs)
-        pools.append((kc, vc))
-    table = torch.from_numpy(w.table).to(dev)
-    lens = torch.from_numpy(w.lens.astype(np.int32)).to(dev)
-    q = w.q.to(dev)
-    offs = w.kv_offsets
-    last = torch.from_numpy(offs + w.lens - 1)
-    k_new = w.k[last].contiguous().to(dev)
-    v_new = w.v[last].contiguous().to(dev)
-    slots = torch.from_numpy(np.array(
-        [layout.slots_for(w.table[s], [w.lens[s] - 1], bs)[0] for s in range(B)],
-        dtype=np.int64)).to(dev)
-    ws_bytes = ops.decode_workspace_size(B, Hq, d, MB, bs, PT)
-    ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device=dev)
-    out = torch.empty_like(q)
+    plan = make_plan(args.workload, dev, args)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     L = lib()
-    launches_per_step = 2  # reshape_and_cache + the persistent decode kernel (B <= 1024)
-
-    def step(i, t_dec=None):
-        kc, vc = pools[i % len(pools)]
-        check(L.pa_reshape_and_cache(k_new.data_ptr(), v_new.data_ptr(), kc.data_ptr(),
-                                     vc.data_ptr(), slots.data_ptr(), B, w.num_blocks, Hkv, bs, d,
-                                     PA_BF16, sp))
-        if t_dec is not None:
-            t_dec[0].record(stream)
-        check(L.pa_decode(out.data_ptr(), q.data_ptr(), kc.data_ptr(), vc.data_ptr(),
-                          table.data_ptr(), MB, lens.data_ptr(), B, Hq, Hkv, d, bs, w.num_blocks,
-                          scale, PT, ws.data_ptr(), ws_bytes, PA_BF16, sp))
-        if t_dec is not None:
-            t_dec[1].record(stream)
+    keys = ["decode"] + (["prefill"] if plan.prefill_flops else [])
 
     # warm-up: W steps, then keep the GPU busy >= 1 s so clocks settle
     clocks = ClockSampler(local)
     clocks.start()
     for i in range(args.warmup):
-        step(i)
+        plan.run(i, L, sp)
     torch.cuda.synchronize()
     t_end = time.time() + (0.0 if args.quick else 1.0)
     i = 0
     while time.time() < t_end:
-        for _ in range(50):
-            step(i)
+        for _ in range(20):
+            plan.run(i, L, sp)
             i += 1
         torch.cuda.synchronize()
 
     # timed region: exactly K steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    ev = _events(args.steps, keys)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     e0.record(stream)
     for i in range(args.steps):
-        step(i, ev[i])
+        plan.run(i, L, sp, ev[i])
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    # keep the sampler running a little under load for the clock record
     t_end = time.time() + (0.0 if args.quick else 0.5)
     while time.time() < t_end:
-        for _ in range(50):
-            step(i)
+        for _ in range(20):
+            plan.run(i, L, sp)
         torch.cuda.synchronize()
     clk = clocks.stop()
-    elapsed_ms = e0.elapsed_time(e1)
-    dec_ms = [a.elapsed_time(b) for a, b in ev]
-    elapsed_ms = reduce_max(elapsed_ms, world, dev)
+    elapsed_ms = reduce_max(e0.elapsed_time(e1), world, dev)
     ms_per_step = elapsed_ms / args.steps
-
-    step_bytes = decode_bytes(w) + reshape_bytes(w)
-    units = reduce_sum(step_bytes * args.steps, world, dev)
-    value = units / (elapsed_ms / 1e3) / 1e9  # GB/s, whole job
-    tokens = reduce_sum(B * args.steps, world, dev)
-    tok_s = tokens / (elapsed_ms / 1e3)
+    value = reduce_sum(plan.step_bytes * args.steps, world, dev) / (elapsed_ms / 1e3) / 1e9
+    tok_s = reduce_sum(plan.tokens * args.steps, world, dev) / (elapsed_ms / 1e3)
+    if args.quick:
+        print(json.dumps({"quick": True, "workload": args.workload, "ms_per_step": ms_per_step,
+                          "value": value}))
+        return
 
     # end to end: host buffers through the C ABI, copies inside the timed region
-    h_q = q.cpu().pin_memory()
-    h_kn, h_vn = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
-    h_slots = slots.cpu().pin_memory()
-    h_table = table.cpu().pin_memory()
-    h_lens = lens.cpu().pin_memory()
-    h_out = torch.empty_like(q, device="cpu").pin_memory()
-    d_q, d_kn, d_vn = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
-    d_slots, d_table, d_lens = torch.empty_like(slots), torch.empty_like(table), torch.empty_like(
-        lens)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_slots, h_table, h_lens))
-    d2h = h_out.numel() * h_out.element_size()
+    h_in = {k: t.cpu().pin_memory() for k, t in plan.inputs.items()}
+    d_in = {k: torch.empty_like(t) for k, t in plan.inputs.items()}
+    h_out = {k: torch.empty_like(t, device="cpu").pin_memory() for k, t in plan.outputs.items()}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
 
     def e2e_step(i):
-        kc, vc = pools[i % len(pools)]
-        for dst, src in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_slots, h_slots),
-                         (d_table, h_table), (d_lens, h_lens)):
-            dst.copy_(src, non_blocking=True)
-        check(L.pa_reshape_and_cache(d_kn.data_ptr(), d_vn.data_ptr(), kc.data_ptr(),
-                                     vc.data_ptr(), d_slots.data_ptr(), B, w.num_blocks, Hkv, bs,
-                                     d, PA_BF16, sp))
-        check(L.pa_decode(out.data_ptr(), d_q.data_ptr(), kc.data_ptr(), vc.data_ptr(),
-                          d_table.data_ptr(), MB, d_lens.data_ptr(), B, Hq, Hkv, d, bs,
-                          w.num_blocks, scale, PT, ws.data_ptr(), ws_bytes, PA_BF16, sp))
-        h_out.copy_(out, non_blocking=True)
+        for k in d_in:
+            d_in[k].copy_(h_in[k], non_blocking=True)
+        plan.run(i, L, sp, src=d_in)
+        for k in h_out:
+            h_out[k].copy_(plan.outputs[k], non_blocking=True)
 
-    if args.quick:
-        print(json.dumps({"quick": True, "ms_per_step": ms_per_step, "value": value}))
-        return
     for i in range(args.warmup):
         e2e_step(i)
     torch.cuda.synchronize()
@@ -324,39 +591,47 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = reduce_max(f0.elapsed_time(f1), world, dev)
-    e2e_value = reduce_sum(step_bytes * args.steps, world, dev) / (e2e_ms / 1e3) / 1e9
+    e2e_value = reduce_sum(plan.step_bytes * args.steps, world, dev) / (e2e_ms / 1e3) / 1e9
 
-    # roofline of the dominant op (pa_decode: partial kernel + merge), timed live
-    peak, peak_kind = peaks()
-    dec_avg_ms = sum(dec_ms) / len(dec_ms)
-    achieved = decode_bytes(w) / (dec_avg_ms / 1e3) / 1e9
-    traffic = kernel_traffic()
+    # roofline of the dominant kernel(s), timed live with events on the stream
+    hbm, bf16_sus, peak_kind = peaks()
+    dec_ms = sum(e["decode"][0].elapsed_time(e["decode"][1]) for e in ev) / len(ev)
+    achieved = plan.decode_bytes / (dec_ms / 1e3) / 1e9
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 K/V/q; shuffled block placement)",
-        "config": {"workload": WORKLOAD, "B": B, "Hq": Hq, "Hkv": Hkv, "head_dim": d,
-                   "block_size": bs, "context_len": "U[128,4096] seed %d" % args.seed,
-                   "total_context_tokens": int(w.lens.sum()), "pool_blocks": w.num_blocks,
-                   "partition_tokens": PT, "parallelism": f"replicas{world}",
-                   "l2": f"inputs larger than L2 ({decode_bytes(w) / 1e6:.0f} MB per step) "
-                         f"and {len(pools)} pools rotated"},
+        "config": dict({"workload": WORKLOADS[args.workload]}, **plan.config,
+                       parallelism=f"replicas{world}",
+                       l2="inputs larger than L2 and %d pools rotated" % len(plan.pools)),
         "tokens_per_s": round(tok_s, 1),
-        "pct_of_hbm_peak": round(100 * value / peak, 2),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+        "pct_of_hbm_peak": round(100 * value / hbm, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": kernel_traffic(f"decode_traffic_{args.workload}.json",
+                                               "pa_decode.cu", "pa_device.cuh"),
                      "kernel": "pa_decode (decode_persistent_kernel, split-KV merge inside)",
                      "peak_source": f"{peak_kind} hbm_gbs",
-                     "avg_launch_us": round(dec_avg_ms * 1e3, 2),
-                     "algorithmic_bytes": decode_bytes(w)},
+                     "avg_launch_us": round(dec_ms * 1e3, 2),
+                     "algorithmic_bytes": plan.decode_bytes},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 5)},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": plan.launches * args.steps,
         "clocks": clk,
     }
+    if plan.prefill_flops:
+        pre_ms = sum(e["prefill"][0].elapsed_time(e["prefill"][1]) for e in ev) / len(ev)
+        tf = plan.prefill_flops / (pre_ms / 1e3) / 1e12
+        result["roofline_prefill"] = {
+            "bound": "tensor", "achieved": round(tf, 2), "peak": bf16_sus, "unit": "TFLOP/s",
+            "frac": round(tf / bf16_sus, 4), "traffic": None, "kernel": "pa_prefill_chunk",
+            "peak_source": f"{peak_kind} bf16_tflops_sustained",
+            "avg_launch_us": round(pre_ms * 1e3, 2), "algorithmic_flops": plan.prefill_flops}
+    if plan.extra:
+        result["workload_detail"] = plan.extra
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, args)
+        result["cpu_baseline"] = cpu_baseline(plan, args)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -367,42 +642,36 @@ def run_gpu(args, world, rank, local):
 # CPU oracle (baseline leg and reference arm)
 # ----------------------------------------------------------------------------
 
-def oracle_sample(w, n_seq, seed):
+def time_oracle_decode(w, n_seq, seed, threads=None):
+    """Time the fp64 oracle's decode of n_seq seeded sequences of workload w."""
+    import oracle
     seqs = synth.sample_indices(w.B, n_seq, seed=seed)
     offs = w.kv_offsets
-    k = torch.cat([w.k[offs[s]:offs[s] + w.lens[s]] for s in seqs]).double().numpy()
-    v = torch.cat([w.v[offs[s]:offs[s] + w.lens[s]] for s in seqs]).double().numpy()
-    q = w.q[torch.from_numpy(seqs)].double().numpy()
+    k = torch.cat([w.k[offs[s]:offs[s] + w.lens[s]] for s in seqs]).double().cpu().numpy()
+    v = torch.cat([w.v[offs[s]:offs[s] + w.lens[s]] for s in seqs]).double().cpu().numpy()
+    q = w.q[torch.from_numpy(seqs).to(w.q.device)].double().cpu().numpy()
     lens = w.lens[seqs]
-    es = 2 if w.dtype == torch.bfloat16 else 4
+    es = _es(w.dtype)
     nbytes = int(lens.sum()) * 2 * w.Hkv * w.d * es + 2 * len(seqs) * w.Hq * w.d * es
-    return q, k, v, lens, nbytes, seqs
-
-
-def time_oracle(w, n_seq, seed, threads):
-    import oracle
-    q, k, v, lens, nbytes, seqs = oracle_sample(w, n_seq, seed)
     t0 = time.perf_counter()
-    oracle.decode(q, k, v, lens, 1.0 / math.sqrt(w.d), nthreads=threads)
-    dt = time.perf_counter() - t0
-    return dt, nbytes, len(seqs)
+    oracle.decode(q, k, v, lens, 1.0 / math.sqrt(w.d), nthreads=threads or os.cpu_count() or 1)
+    return time.perf_counter() - t0, nbytes, len(seqs)
 
 
-def cpu_baseline(w, args, budget_s=10.0):
-    """The oracle as it stands on the host cores: the whole batch's decode,
-    repeated until about budget_s seconds of CPU time have passed."""
-    import oracle
+def cpu_baseline(plan, args, budget_s=10.0):
+    """The oracle as it stands on the host cores, on a bounded seeded sample of
+    the workload's decode, repeated until about budget_s seconds have passed."""
     threads = os.cpu_count() or 1
-    q, k, v, lens, nbytes, seqs = oracle_sample(w, w.B, args.seed)
-    reps, total = 0, 0.0
+    n = args.cpu_sample_seqs
+    reps, total, nb, k = 0, 0.0, 0, 0
     while reps == 0 or total < budget_s:
-        t0 = time.perf_counter()
-        oracle.decode(q, k, v, lens, 1.0 / math.sqrt(w.d), nthreads=threads)
-        total += time.perf_counter() - t0
+        dt, nbytes, k = plan.oracle_sample(n, args.seed + reps)
+        total += dt
+        nb += nbytes
         reps += 1
-    return {"value": round(reps * nbytes / total / 1e9, 4), "unit": "GB/s", "cores": threads,
+    return {"value": round(nb / total / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
-            "sample": f"whole batch ({w.B} sequences) decoded {reps}x by the fp64 C oracle on "
+            "sample": f"{reps} x {k} seeded sequences of the workload's decode, fp64 C oracle on "
                       f"{threads} threads, {total:.1f} s"}
 
 
@@ -413,10 +682,10 @@ def run_reference(args, world, rank):
     threads = os.cpu_count() or 1
     n_seq = args.cpu_sample_seqs
     for _ in range(args.warmup):
-        time_oracle(w, max(1, n_seq // 8), args.seed, threads)
+        time_oracle_decode(w, max(1, n_seq // 8), args.seed, threads)
     total_t, total_b = 0.0, 0
     for i in range(args.steps):
-        dt, nbytes, n = time_oracle(w, n_seq, args.seed + i, threads)
+        dt, nbytes, n = time_oracle_decode(w, n_seq, args.seed + i, threads)
         total_t += dt
         total_b += nbytes
     value = total_b / total_t / 1e9
@@ -425,9 +694,9 @@ def run_reference(args, world, rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * total_t / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d,
-                   "block_size": w.bs, "context_len": "U[128,4096] seed %d" % args.seed,
-                   "parallelism": "host cores"},
+        "config": {"workload": WORKLOADS["8b"], "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "head_dim": w.d, "block_size": w.bs,
+                   "context_len": "U[128,4096] seed %d" % args.seed, "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
                          "sample": f"{n_seq} of {w.B} sequences per step (seeded), fp64 C "
@@ -444,6 +713,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="8b")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--partition", type=int, default=512)
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)

@@ -8,8 +8,10 @@ layout): both the CUDA path and the fp64 oracle receive what it draws.
 Recipe (every config; seed defaults to 0):
 * lengths: numpy PCG64(seed), uniform integers in the config's range
   (inclusive), or the fixed list of the tiny config;
-* values: torch CPU generator seeded with seed+1, i.i.d. N(0,1), rounded to
-  the config's dtype once (bf16 round-to-nearest-even, or fp32);
+* values: torch generator seeded with seed+1, i.i.d. N(0,1), rounded to the
+  config's dtype once (bf16 round-to-nearest-even, or fp32); the CPU
+  generator by default (tests), the CUDA one where a benchmark only needs a
+  multi-GB batch quickly (it then draws a different, equally seeded stream);
 * placement: numpy PCG64(seed+2) permutation of the pool's block ids, handed
   out to sequences in order; the pool is 1.2x the blocks needed unless the
   config fixes it (tiny: 32 blocks).  Blocks no sequence owns stay unused.
@@ -78,8 +80,14 @@ class Workload:
 
 
 def _values(shape, dtype, gen, device="cpu"):
-    x = torch.randn(*shape, generator=gen, dtype=torch.float32, device="cpu")
+    """N(0,1) values drawn by `gen` on the generator's own device, rounded to
+    dtype once, then moved to `device`."""
+    x = torch.randn(*shape, generator=gen, dtype=torch.float32, device=gen.device)
     return x.to(dtype).to(device)
+
+
+def _generator(seed, gen_device):
+    return torch.Generator(device=gen_device).manual_seed(seed)
 
 
 def _blocks_of(lens, bs):
@@ -105,8 +113,11 @@ def pool_size(blocks_per_seq, factor=1.2):
 
 
 def decode_workload(name="8b", seed=0, B=None, lens=None, Hq=None, Hkv=None, d=None, bs=None,
-                    dtype=None, num_blocks=None, max_blocks=None, device="cpu"):
-    """Decode batch of config ``name`` (one query per sequence), with overrides."""
+                    dtype=None, num_blocks=None, max_blocks=None, device="cpu", gen_device="cpu"):
+    """Decode batch of config ``name`` (one query per sequence), with overrides.
+
+    gen_device="cuda" draws the values with the CUDA generator (same recipe,
+    different stream of numbers) -- used to set up multi-GB batches quickly."""
     cfg = dict(CONFIGS[name])
     Hq = Hq or cfg["Hq"]
     Hkv = Hkv or cfg["Hkv"]
@@ -129,7 +140,7 @@ def decode_workload(name="8b", seed=0, B=None, lens=None, Hq=None, Hkv=None, d=N
         max_blocks = max(nblk) if "len_range" not in cfg else (cfg["len_range"][1] + bs - 1) // bs
         max_blocks = max(max_blocks, max(nblk))
     table = place(nblk, num_blocks, np.random.Generator(np.random.PCG64(seed + 2)), max_blocks)
-    gen = torch.Generator().manual_seed(seed + 1)
+    gen = _generator(seed + 1, gen_device)
     n_kv = int(lens.sum())
     q = _values((len(lens), Hq, d), dtype, gen, device)
     k = _values((n_kv, Hkv, d), dtype, gen, device)

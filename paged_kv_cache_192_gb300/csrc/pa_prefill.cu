@@ -19,6 +19,7 @@
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_tcgen05.cuh"
 
 namespace {
 
@@ -298,14 +299,310 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
     }
 }
 
+// ---------------------------------------------------------------------------
+// tcgen05 prefill kernel (default).
+//
+// One CTA of 128 threads per (request, KV head, tile of 128/GQ query tokens);
+// thread r owns query row r = (token r / GQ, head r % GQ), which is also TMEM
+// lane r, so every row's softmax is thread-local.  Per 64-token K/V tile:
+//   S = Q K^T   tcgen05.mma, Q and K from 128-byte-swizzled shared memory,
+//               S (fp32) in TMEM
+//   softmax     tcgen05.ld of the row, scale, causal mask, running max with a
+//               lazy rescale of O, p = exp2(s - m), row sum in fp32;
+//               P = hi + lo (both bf16) written back to TMEM
+//   O += P V    tcgen05.mma with A = P from TMEM and B = V (MN-major) from
+//               shared memory, twice (hi, lo), O (fp32) stays in TMEM
+// K/V tiles are gathered block by block through the block table with cp.async
+// into two buffers (tile j+1 loads while tile j computes).  TMEM columns:
+// O [0, D), S [128, 192), P hi [192, 224), P lo [224, 256).
+// ---------------------------------------------------------------------------
+constexpr int kTcKT = 64;        // KV tokens per tile
+constexpr int kTcCols = 256;     // TMEM columns per CTA
+constexpr int kTcS = 128, kTcPH = 192, kTcPL = 224;
+constexpr float kTcTau = 8.0f;   // lazy-rescale headroom (log2 units)
+
+template <int D>
+struct TcLayout {
+    static constexpr int Q_BYTES = 128 * D * 2;
+    static constexpr int T_BYTES = kTcKT * D * 2;  // one K or V tile
+    static constexpr int OFF_K = Q_BYTES;
+    static constexpr int OFF_V = OFF_K + 2 * T_BYTES;
+    static constexpr int OFF_BAR = OFF_V + 2 * T_BYTES;
+    static constexpr int OFF_BT = OFF_BAR + 64;        // block-table slice
+    static constexpr int BT_MAX = 1024;                // entries kept in smem
+    static constexpr int SMEM = OFF_BT + 4 * BT_MAX + 1024;  // + alignment slack
+};
+
+__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity) {
+    return pa::mbar_wait(bar, parity);
+}
+
+template <int D, int GQ>
+__global__ void __launch_bounds__(128, 2) prefill_tc_kernel(const PrefillParams p) {
+    using Lay = TcLayout<D>;
+    constexpr int CH = D * 2 / 16;  // 16-byte chunks per row
+    constexpr int QTOK = 128 / GQ;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sq = pa::smem_u32(smem);
+    const uint32_t sk = sq + Lay::OFF_K, sv = sq + Lay::OFF_V;
+    uint64_t *bar_s = reinterpret_cast<uint64_t *>(smem + Lay::OFF_BAR);
+    uint64_t *bar_o = bar_s + 1;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_s + 2);
+
+    // later query tiles see more context: start them first
+    const int qt = gridDim.x - 1 - blockIdx.x, hk = blockIdx.y, r = blockIdx.z;
+    const int qs = p.query_start[r];
+    const int n = p.query_start[r + 1] - qs;
+    const int t0 = qt * QTOK;
+    if (t0 >= n) return;
+    const int cap = p.MB << p.bs_log2;
+    const int L = p.context_lens[r];
+    if (L > cap || L < n) {
+        if (threadIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+        return;
+    }
+    const int P = L - n;
+    const int kv_end = min(L, P + t0 + QTOK);
+    const int ntiles = (kv_end + kTcKT - 1) / kTcKT;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int32_t *bt_g = p.block_table + static_cast<size_t>(r) * p.MB;
+    // this CTA's block-table entries, checked, in shared memory when they fit
+    int32_t *bt_s = reinterpret_cast<int32_t *>(smem + Lay::OFF_BT);
+    const int nblk = (kv_end + p.bs - 1) >> p.bs_log2;
+    const bool bt_in_smem = nblk <= Lay::BT_MAX;
+    auto checked = [&](int blk) {
+        if (blk < 0 || blk >= p.num_blocks) {
+            pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+            blk = 0;
+        }
+        return blk;
+    };
+    if (bt_in_smem) {
+        for (int i = tid; i < nblk; i += 128) bt_s[i] = checked(bt_g[i]);
+        __syncthreads();
+    }
+
+    // ---- loads (cp.async, swizzled) ----------------------------------------------
+    for (int idx = tid; idx < 128 * CH; idx += 128) {
+        const int m = idx / CH, c = idx % CH;
+        const int t = t0 + m / GQ;
+        const bool valid = t < n;
+        const __nv_bfloat16 *src =
+            p.q + (static_cast<size_t>(qs + (valid ? t : 0)) * p.Hq + hk * GQ + m % GQ) * D + c * 8;
+        cp_async16(sq + pa::tc::sw128(m, c * 8, 128), src, valid);
+    }
+    auto load_tile = [&](int it, int buf) {
+        const int j0 = it * kTcKT;
+        const uint32_t dk = sk + buf * Lay::T_BYTES, dv = sv + buf * Lay::T_BYTES;
+        for (int idx = tid; idx < kTcKT * CH; idx += 128) {
+            const int row = idx / CH, c = idx % CH;
+            const int j = j0 + row;
+            const bool valid = j < kv_end;
+            size_t off = 0;
+            if (valid) {
+                const int blk =
+                    bt_in_smem ? bt_s[j >> p.bs_log2] : checked(bt_g[j >> p.bs_log2]);
+                off = ((static_cast<size_t>(blk) * p.Hkv + hk) * p.bs + (j & (p.bs - 1))) * D * 2 +
+                      c * 16;
+            }
+            const uint32_t o = pa::tc::sw128(row, c * 8, kTcKT);
+            cp_async16(dk + o, p.k_cache + off, valid);
+            cp_async16(dv + o, p.v_cache + off, valid);
+        }
+    };
+    load_tile(0, 0);
+    cp_async_commit();
+    if (ntiles > 1) {
+        load_tile(1, 1);
+        cp_async_commit();
+    }
+
+    if (tid == 0) {
+        pa::mbar_init(bar_s, 1);
+        pa::mbar_init(bar_o, 1);
+        pa::fence_barrier_init();
+    }
+    if (warp == 0) pa::tc::alloc(tslot, kTcCols);
+    pa::tc::fence_before();
+    __syncthreads();
+    pa::tc::fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+
+    const int g = tid / GQ;
+    const int pos = P + min(t0 + g, n - 1);  // rows past the chunk reuse the last row
+    float m_used = -INFINITY, lsum = 0.f;
+    bool failed = false;
+    constexpr uint32_t kIdS = pa::tc::idesc_bf16(128, kTcKT, 0, 0);
+    constexpr uint32_t kIdO = pa::tc::idesc_bf16(128, D, 0, 1);
+
+    for (int it = 0; it < ntiles; ++it) {
+        const int buf = it & 1;
+        if (it == 0 && ntiles > 1) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        pa::tc::fence_before();
+        __syncthreads();
+        pa::tc::fence_after();
+        // ---- S = Q K^T -------------------------------------------------------------
+        if (tid == 0) {
+            const uint32_t kb = sk + buf * Lay::T_BYTES;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint64_t a = pa::tc::sdesc(sq + (ks >> 2) * 128 * 128 + (ks & 3) * 32, 16, 1024);
+                const uint64_t b =
+                    pa::tc::sdesc(kb + (ks >> 2) * kTcKT * 128 + (ks & 3) * 32, 16, 1024);
+                pa::tc::mma_ss(tmem + kTcS, a, b, kIdS, ks > 0);
+            }
+            pa::tc::commit(bar_s);
+        }
+        // PV of the previous tile done: its buffers take tile it+1 now, while
+        // this tile's S and softmax run
+        if (it > 0) {
+            failed = __syncthreads_or(!tc_wait(bar_o, (it - 1) & 1));
+            if (failed) break;
+            if (it + 1 < ntiles) {
+                load_tile(it + 1, (it + 1) & 1);
+                cp_async_commit();
+            }
+        }
+        failed = __syncthreads_or(!tc_wait(bar_s, it & 1));
+        if (failed) break;
+        pa::tc::fence_after();
+        // ---- softmax of this row --------------------------------------------------------
+        uint32_t sr[2][32];
+        pa::tc::ld32(lane_base + kTcS, sr[0]);
+        pa::tc::ld32(lane_base + kTcS + 32, sr[1]);
+        pa::tc::wait_ld();
+        const int j0 = it * kTcKT;
+        float s[64];
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+            const float v = __uint_as_float(sr[c >> 5][c & 31]) * p.qscale;
+            s[c] = (j0 + c <= pos) ? v : -INFINITY;
+            tmax = fmaxf(tmax, s[c]);
+        }
+        float alpha = 1.f;
+        if (tmax > m_used + kTcTau) {  // also true on the first tile (m_used = -inf)
+            alpha = (m_used == -INFINITY) ? 0.f : exp2f(m_used - tmax);
+            m_used = tmax;
+        }
+        uint32_t ph[32], pl[32];
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const float p0 = fast_exp2(s[2 * c] - m_used);
+            const float p1 = fast_exp2(s[2 * c + 1] - m_used);
+            rs += p0 + p1;
+            ph[c] = pack_bf16(p0, p1);
+            const float2 hv = pa::bf16x2_to_float2(ph[c]);
+            pl[c] = pack_bf16(p0 - hv.x, p1 - hv.y);
+        }
+        lsum = lsum * alpha + rs;
+        // ---- rescale O (the previous PV is complete) ---------------------------------
+        if (it > 0) {
+            if (__any_sync(pa::kFull, alpha != 1.f)) {
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    pa::tc::ld32(lane_base + c0, o);
+                    pa::tc::wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                    pa::tc::st32(lane_base + c0, o);
+                }
+            }
+        }
+        pa::tc::st32(lane_base + kTcPH, ph);
+        pa::tc::st32(lane_base + kTcPL, pl);
+        pa::tc::wait_st();
+        pa::tc::fence_before();
+        __syncthreads();
+        pa::tc::fence_after();
+        // ---- O += P V (hi, then lo) ---------------------------------------------------
+        if (tid == 0) {
+            const uint32_t vb = sv + buf * Lay::T_BYTES;
+#pragma unroll
+            for (int ks = 0; ks < kTcKT / 16; ++ks) {
+                const uint64_t b = pa::tc::sdesc(vb + ks * 16 * 128, kTcKT * 128, 1024);
+                pa::tc::mma_ts(tmem, tmem + kTcPH + ks * 8, b, kIdO, (it > 0 || ks > 0) ? 1 : 0);
+                pa::tc::mma_ts(tmem, tmem + kTcPL + ks * 8, b, kIdO, 1);
+            }
+            pa::tc::commit(bar_o);
+        }
+    }
+    // ---- normalise and store ----------------------------------------------------------
+    if (!failed) failed = __syncthreads_or(!tc_wait(bar_o, (ntiles - 1) & 1));
+    if (!failed) {
+        pa::tc::fence_after();
+        const int t = t0 + g;
+        const float inv = 1.f / lsum;
+        __nv_bfloat16 *dst =
+            p.out + (static_cast<size_t>(qs + min(t, n - 1)) * p.Hq + hk * GQ + tid % GQ) * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            pa::tc::ld32(lane_base + c0, o);
+            pa::tc::wait_ld();
+            if (t < n) {
+#pragma unroll
+                for (int c = 0; c < 32; c += 8) {
+                    uint4 w;
+                    w.x = pack_bf16(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv);
+                    w.y = pack_bf16(__uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+                    w.z = pack_bf16(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv);
+                    w.w = pack_bf16(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv);
+                    *reinterpret_cast<uint4 *>(dst + c0 + c) = w;
+                }
+            }
+        }
+    } else {
+        // a wait ran out: record it, wait (bounded) for this CTA's MMAs and
+        // copies, free TMEM, write nothing
+        if (tid == 0) {
+            pa::record_error(p.err, PA_DEVERR_TIMEOUT);
+            // give MMAs still in flight one more bounded chance to finish
+            // before their TMEM is released
+            (void)pa::mbar_wait(bar_s, 0);
+            (void)pa::mbar_wait(bar_o, 0);
+        }
+        cp_async_wait<0>();
+    }
+    pa::tc::fence_before();
+    __syncthreads();
+    if (warp == 0) pa::tc::dealloc(tmem, kTcCols);
+}
+
 int log2_int(int x) {
     int l = 0;
     while ((1 << l) < x) ++l;
     return l;
 }
 
+#ifndef PA_PREFILL_TCGEN05
+#define PA_PREFILL_TCGEN05 1  // 1: tcgen05 kernel; 0: warp-level mma.sync kernel
+#endif
+
+template <int D, int GQ>
+int launch_tc(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
+    const size_t smem = TcLayout<D>::SMEM;
+    auto kern = prefill_tc_kernel<D, GQ>;
+    (void)cudaGetLastError();
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return pa::cuda_fail(e, "prefill: shared memory attribute");
+    constexpr int qtok = 128 / GQ;
+    dim3 grid((max_query_len + qtok - 1) / qtok, p.Hkv, p.R);
+    kern<<<grid, 128, smem, stream>>>(p);
+    return pa::check_launch("prefill launch");
+}
+
 template <int D, int GQ>
 int launch(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
+    if (PA_PREFILL_TCGEN05) return launch_tc<D, GQ>(p, max_query_len, stream);
     const size_t smem = kRows * D * 2 + 4 * kKT * D * 2;
     auto kern = prefill_kernel<D, GQ>;
     (void)cudaGetLastError();

@@ -238,7 +238,17 @@ class DecodePlan(Plan):
         super().__init__(name)
         from paged_kv_cache_192_gb300 import layout, ops
         gen_dev = "cuda" if name == "70b" else "cpu"
-        w = synth.decode_workload(name, seed=args.seed, gen_device=gen_dev)
+        w = synth.decode_workload(name, seed=args.seed, gen_device=gen_dev,
+                                  bs=args.block_size or None)
+        if args.placement == "identity":
+            # paging-overhead control: every sequence's blocks consecutive
+            table = np.zeros_like(w.table)
+            pos = 0
+            for s_, L_ in enumerate(w.lens):
+                nb_ = -(-int(L_) // w.bs)
+                table[s_, :nb_] = np.arange(pos, pos + nb_)
+                pos += nb_
+            w.table = table
         self.w = w
         for _ in range(args.pools):
             kc, vc = layout.alloc_pools(w.num_blocks, w.Hkv, w.bs, w.d, w.dtype, dev, poison=False)
@@ -265,7 +275,11 @@ class DecodePlan(Plan):
         self.config = {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d, "block_size": w.bs,
                        "context_len": f"U[{lo},{hi}] seed {args.seed}",
                        "total_context_tokens": int(w.lens.sum()), "pool_blocks": w.num_blocks,
-                       "partition_tokens": self.PT}
+                       "partition_tokens": self.PT, "placement": args.placement}
+        paged, contig = layout.kv_utilization(w.lens, w.bs, hi)
+        self.extra = {"kv_utilization_paged": round(paged, 4),
+                      f"kv_utilization_contiguous_reserve_{hi}": round(contig, 4),
+                      "block_table_bytes": int(sum(-(-int(L) // w.bs) for L in w.lens)) * 4}
         self.oracle_sample = lambda n, seed: time_oracle_decode(w, n, seed)
 
     def run(self, i, L, sp, ev=None, src=None):
@@ -716,6 +730,10 @@ def main(argv=None):
     ap.add_argument("--workload", choices=list(WORKLOADS), default="8b")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--partition", type=int, default=512)
+    ap.add_argument("--block-size", type=int, default=0,
+                    help="override the decode workload's block size (block-size sweep)")
+    ap.add_argument("--placement", choices=["shuffled", "identity"], default="shuffled",
+                    help="physical placement of each sequence's blocks (decode workloads)")
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pools", type=int, default=N_POOLS, help="pools rotated between steps")

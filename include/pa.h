@@ -114,6 +114,25 @@ int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int64_t n
                    pa_stream_t stream);
 
 /*
+ * pa_swap_blocks -- move whole blocks between two pools of the same shape,
+ * e.g. swap a sequence's blocks out to pinned host memory and back: when the
+ * device pool is full, small pages go to the CPU instead of whole sequences
+ * ("KV Cache and PagedAttention: Why Your LLM Server Slows Down", section
+ * "How PagedAttention fixes this", fine-grained eviction).
+ * For each pair (src, dst): block dst of the destination pools becomes a byte
+ * copy of block src of the source pools, K and V.  Each pool (and the pairs
+ * array) may be device memory or pinned host memory (reached through its
+ * mapped device alias); pageable host memory is rejected.
+ *   pairs  int64 [n][2] (src block in the source pool, dst block in the
+ *          destination pool); destinations must be distinct (validate mode).
+ * Bit exact; asynchronous on the stream like every op.
+ */
+int pa_swap_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_v,
+                   const int64_t *pairs, int64_t n, int64_t src_num_blocks,
+                   int64_t dst_num_blocks, int Hkv, int block_size, int head_dim, int dtype,
+                   pa_stream_t stream);
+
+/*
  * pa_decode_workspace_size -- bytes of fp32 workspace pa_decode needs for
  * split-KV partials (0 when no sequence can span more than one partition).
  * partition_tokens as for pa_decode (0 = library default).

@@ -29,6 +29,8 @@ SIGNATURES = {
                                       _c_int, _c_int, _c_int, _c_vp]),
     "pa_copy_blocks": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_int, _c_int, _c_int,
                                 _c_int, _c_vp]),
+    "pa_swap_blocks": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
+                                _c_int, _c_int, _c_int, _c_int, _c_vp]),
     "pa_decode_workspace_size": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                           ctypes.POINTER(_c_sz)]),
     "pa_decode": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_int,

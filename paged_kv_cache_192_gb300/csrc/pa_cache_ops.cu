@@ -56,6 +56,49 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ k_
     for (int64_t i = threadIdx.x; i < chunks_per_block; i += blockDim.x) d[i] = s[i];
 }
 
+// blockIdx.x = pair, blockIdx.y = cache (0: K, 1: V): block dst of the
+// destination pool becomes a copy of block src of the source pool (either
+// pool may be pinned host memory reached through its device alias).
+__global__ void __launch_bounds__(256) swap_blocks_kernel(uint4 *__restrict__ dst_k,
+                                                          uint4 *__restrict__ dst_v,
+                                                          const uint4 *__restrict__ src_k,
+                                                          const uint4 *__restrict__ src_v,
+                                                          const int64_t *__restrict__ pairs,
+                                                          int64_t chunks_per_block,
+                                                          int64_t src_blocks, int64_t dst_blocks,
+                                                          int *err) {
+    const int64_t p = blockIdx.x;
+    const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+    if (src < 0 || dst < 0 || src >= src_blocks || dst >= dst_blocks) {
+        if (threadIdx.x == 0) pa::record_error(err, PA_DEVERR_BAD_BLOCK);
+        return;
+    }
+    const uint4 *s = (blockIdx.y ? src_v : src_k) + src * chunks_per_block;
+    uint4 *d = (blockIdx.y ? dst_v : dst_k) + dst * chunks_per_block;
+    for (int64_t i = threadIdx.x; i < chunks_per_block; i += blockDim.x) d[i] = s[i];
+}
+
+// Device address of a pool: device memory as is, pinned host memory through
+// its mapped device alias; anything else is rejected.
+int device_view(const void *ptr, void **dev, const char *what) {
+    cudaPointerAttributes a{};
+    cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+    if (e != cudaSuccess) return pa::cuda_fail(e, what);
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+        *dev = const_cast<void *>(ptr);
+        return PA_OK;
+    }
+    if (a.type == cudaMemoryTypeHost) {
+        if (a.devicePointer) {
+            *dev = a.devicePointer;
+            return PA_OK;
+        }
+        e = cudaHostGetDevicePointer(dev, const_cast<void *>(ptr), 0);
+        return e == cudaSuccess ? PA_OK : pa::cuda_fail(e, what);
+    }
+    return pa::fail(PA_ERR_INVALID, "%s: pool must be device or pinned host memory", what);
+}
+
 int log2_int(int x) {
     int l = 0;
     while ((1 << l) < x) ++l;
@@ -152,6 +195,54 @@ int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int64_t n
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), pairs,
         static_cast<int64_t>(block_bytes / 16), num_blocks, pa::device_error_word());
     return pa::check_launch("copy_blocks launch");
+}
+
+int pa_swap_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_v,
+                   const int64_t *pairs, int64_t n, int64_t src_num_blocks,
+                   int64_t dst_num_blocks, int Hkv, int block_size, int head_dim, int dtype,
+                   pa_stream_t stream) {
+    pa::clear_error();
+    const size_t es = pa::dtype_size(dtype);
+    if (!es) return pa::fail(PA_ERR_INVALID, "swap_blocks: bad dtype %d", dtype);
+    if (n < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0 || Hkv <= 0 || block_size <= 0 ||
+        head_dim <= 0)
+        return pa::fail(PA_ERR_INVALID, "swap_blocks: bad sizes");
+    const size_t block_bytes = size_t(Hkv) * block_size * head_dim * es;
+    if (block_bytes % 16) return pa::fail(PA_ERR_INVALID, "swap_blocks: block bytes % 16 != 0");
+    if (n == 0) return PA_OK;
+    if (!dst_k || !dst_v || !src_k || !src_v || !pairs)
+        return pa::fail(PA_ERR_INVALID, "swap_blocks: NULL pointer");
+    if (!pa::aligned16(dst_k) || !pa::aligned16(dst_v) || !pa::aligned16(src_k) ||
+        !pa::aligned16(src_v))
+        return pa::fail(PA_ERR_INVALID, "swap_blocks: pools must be 16-byte aligned");
+    if (n > 0x7fffffff) return pa::fail(PA_ERR_INVALID, "swap_blocks: too many pairs");
+    void *dk, *dv, *sk2, *sv2, *pp;
+    if (int rc = device_view(dst_k, &dk, "swap_blocks dst_k")) return rc;
+    if (int rc = device_view(dst_v, &dv, "swap_blocks dst_v")) return rc;
+    if (int rc = device_view(src_k, &sk2, "swap_blocks src_k")) return rc;
+    if (int rc = device_view(src_v, &sv2, "swap_blocks src_v")) return rc;
+    if (int rc = device_view(pairs, &pp, "swap_blocks pairs")) return rc;
+    if (pa::validate_on()) {
+        std::vector<int64_t> p(2 * n);
+        if (int rc = pa::fetch(p.data(), pairs, 2 * n * sizeof(int64_t), stream)) return rc;
+        std::unordered_set<int64_t> dsts;
+        for (int64_t i = 0; i < n; ++i) {
+            if (p[2 * i] < 0 || p[2 * i] >= src_num_blocks || p[2 * i + 1] < 0 ||
+                p[2 * i + 1] >= dst_num_blocks)
+                return pa::fail(PA_ERR_INVALID, "validate: swap pair %lld outside its pool",
+                                (long long)i);
+            if (!dsts.insert(p[2 * i + 1]).second)
+                return pa::fail(PA_ERR_INVALID, "validate: duplicate destination block");
+        }
+    }
+    dim3 grid(static_cast<unsigned>(n), 2);
+    (void)cudaGetLastError();
+    swap_blocks_kernel<<<grid, 256, 0, stream>>>(
+        static_cast<uint4 *>(dk), static_cast<uint4 *>(dv), static_cast<const uint4 *>(sk2),
+        static_cast<const uint4 *>(sv2), static_cast<const int64_t *>(pp),
+        static_cast<int64_t>(block_bytes / 16), src_num_blocks, dst_num_blocks,
+        pa::device_error_word());
+    return pa::check_launch("swap_blocks launch");
 }
 
 }  // extern "C"

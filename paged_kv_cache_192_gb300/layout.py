@@ -55,3 +55,23 @@ def fill_pools(k_cache, v_cache, k_logical, v_logical, table, lens, block_size, 
         ops.reshape_and_cache(k_logical[sl].to(k_cache.device).contiguous(),
                               v_logical[sl].to(k_cache.device).contiguous(), k_cache, v_cache,
                               slots[sl].contiguous())
+
+
+def kv_utilization(lens, block_size, reserve_len=None):
+    """Fraction of allocated KV slots that hold tokens.
+
+    Paged: every sequence holds ceil(L/bs) blocks, so the unfilled slots are
+    less than one block per sequence ("PagedAttention: memetakan blok KV
+    logis ke memori fisik tidak kontigu", section "Sisa alokasi dibatasi oleh
+    granularitas blok").  Contiguous: every sequence reserves reserve_len
+    slots up front, the max-length reservation the pages contrast with paging
+    ("Apa itu PagedAttention?", section "Masalah fragmentasi memori KV Cache
+    konvensional").  Returns (paged, contiguous or None).
+    """
+    lens = np.asarray(lens, dtype=np.int64)
+    used = int(lens.sum())
+    paged = used / float(int(sum(-(-int(L) // block_size) for L in lens)) * block_size)
+    contiguous = None
+    if reserve_len is not None:
+        contiguous = used / float(len(lens) * int(reserve_len))
+    return paged, contiguous

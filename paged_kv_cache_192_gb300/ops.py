@@ -76,6 +76,27 @@ def copy_blocks(k_cache, v_cache, pairs, stream=None):
         _stream(stream)))
 
 
+def swap_blocks(dst_k, dst_v, src_k, src_v, pairs, stream=None):
+    """Copy blocks pairs[i][0] of the source pools into blocks pairs[i][1] of
+    the destination pools; either side may be pinned host memory."""
+    NBs, Hkv, bs, d = src_k.shape
+    NBd = dst_k.shape[0]
+    assert dst_k.shape[1:] == src_k.shape[1:] and dst_v.shape == dst_k.shape
+    assert src_v.shape == src_k.shape and src_k.dtype == dst_k.dtype
+    n = pairs.shape[0] if pairs.numel() else 0
+    for name, t in (("dst_k", dst_k), ("dst_v", dst_v), ("src_k", src_k), ("src_v", src_v),
+                    ("pairs", pairs)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if pairs.dtype != torch.int64:
+        raise TypeError("pairs must be int64")
+    check(lib().pa_swap_blocks(dst_k.data_ptr(), dst_v.data_ptr(), src_k.data_ptr(),
+                               src_v.data_ptr(), pairs.data_ptr() if n else None, n, NBs, NBd,
+                               Hkv, bs, d, _dt(src_k), _stream(stream)))
+
+
 def decode_workspace_size(B, Hq, head_dim, max_blocks_per_seq, block_size, partition_tokens=0):
     out = ctypes.c_size_t(0)
     check(lib().pa_decode_workspace_size(B, Hq, head_dim, max_blocks_per_seq, block_size,

@@ -29,3 +29,26 @@ def test_300_of_4096_reservation_waste():
     assert round(100 * (reserved - used) / reserved) == 93
     paged = -(-used // bs) * bs
     assert 0 <= paged - used < bs
+
+
+def test_kv_utilization_closed_forms():
+    from paged_kv_cache_192_gb300.layout import kv_utilization
+    # one 300-token sequence, 16-token blocks, 4096 reserved (the pages' example)
+    paged, contig = kv_utilization([300], 16, 4096)
+    assert paged == pytest.approx(300 / 304) and contig == pytest.approx(300 / 4096)
+    # full blocks waste nothing; the waste is always < one block per sequence
+    assert kv_utilization([32, 64], 16)[0] == 1.0
+    lens = [1, 17, 31, 100]
+    paged, _ = kv_utilization(lens, 16)
+    assert sum(lens) / paged - sum(lens) < 16 * len(lens)
+
+
+def test_kv_utilization_8b_config():
+    """8B-shaped batch (L ~ U[128,4096]): paged keeps ~99.6% of the slots
+    busy, a 4096-token reservation ~52%."""
+    from paged_kv_cache_192_gb300 import synth
+    from paged_kv_cache_192_gb300.layout import kv_utilization
+    w = synth.decode_workload("8b", seed=0)
+    paged, contig = kv_utilization(w.lens, 16, 4096)
+    assert 0.99 < paged < 1.0
+    assert 0.45 < contig < 0.6

@@ -14,7 +14,11 @@
 // share a KV head share every K/V tile (GQA packed into M).  K/V tiles of 64
 // tokens are gathered block by block into swizzled shared memory with
 // cp.async (double-buffered); online softmax in the log2 domain.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cmath>
+#include <mutex>
 #include <vector>
 
 #include "pa_device.cuh"
@@ -38,7 +42,7 @@ struct PrefillParams {
     const int32_t *context_lens;
     int *err;
     int64_t num_blocks;
-    int R, Hq, Hkv, bs, bs_log2, MB;
+    int R, Hq, Hkv, bs, bs_log2, MB, max_query_len;
     float qscale;
 };
 
@@ -576,6 +580,375 @@ __global__ void __launch_bounds__(128, 2) prefill_tc_kernel(const PrefillParams 
     if (warp == 0) pa::tc::dealloc(tmem, kTcCols);
 }
 
+// ---------------------------------------------------------------------------
+// tcgen05 prefill kernel, warp-specialised (default).
+//
+// One CTA of 320 threads per (request, KV head, 2 x 128 query rows):
+//   warps 0-3  softmax of query tile A (rows 0..127, TMEM lanes 0..127)
+//   warps 4-7  softmax of query tile B (rows 128..255, same lanes)
+//   warp 8     issues every tcgen05.mma (one lane)
+//   warp 9     loads K/V tiles with TMA (2D tensor copies, 128-byte swizzle)
+// The tensor core alternates between the tiles: while one tile's softmax
+// runs, it computes the other tile's QK^T or PV.  64-token K/V tiles go
+// through a 3-stage ring; a (block, 64 columns) box per copy, gathered
+// through the block table; boxes for blocks past the context are read out of
+// bounds and arrive zero-filled.  TMEM (512 columns): O_A [0,128),
+// O_B [128,256), S_A [256,320), S_B [320,384), P_A hi/lo [384,448),
+// P_B hi/lo [448,512).  All hand-offs are mbarriers; every wait is bounded.
+// ---------------------------------------------------------------------------
+constexpr int kT2KT = 64;      // KV tokens per tile
+constexpr int kT2NST = 3;      // K/V ring stages
+constexpr int kT2Threads = 320;
+constexpr int kT2RankMax = 256;  // (request, query tile) pairs ranked in-kernel
+
+template <int D>
+struct Tc2Layout {
+    static constexpr int Q_BYTES = 2 * 128 * D * 2;  // two query tiles
+    static constexpr int T_BYTES = kT2KT * D * 2;    // one K or V tile
+    static constexpr int OFF_KV = Q_BYTES;           // [stage][K|V]
+    static constexpr int OFF_BAR = OFF_KV + kT2NST * 2 * T_BYTES;
+    static constexpr int N_BAR = 3 * kT2NST + 6;     // kv_full, kv_empty, (s, p, o) x 2
+    static constexpr int OFF_SLOT = OFF_BAR + 8 * N_BAR;
+    static constexpr int OFF_BT = OFF_SLOT + 16;
+    static constexpr int BT_MAX = 1024;
+    static constexpr int SMEM = OFF_BT + 4 * BT_MAX + 1024;
+};
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(pa::smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(pa::smem_u32(bar)) : "memory");
+}
+
+template <int D, int GQ>
+__global__ void __launch_bounds__(kT2Threads, 1)
+    prefill_tc2_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap) {
+    using Lay = Tc2Layout<D>;
+    constexpr int CH = D * 2 / 16;
+    constexpr int QTOK = 256 / GQ;  // query tokens per CTA
+    constexpr int TILE_TX = 2 * kT2KT * D * 2;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sq = pa::smem_u32(smem);
+    const uint32_t skv = sq + Lay::OFF_KV;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::OFF_BAR);
+    uint64_t *kv_full = bars, *kv_empty = bars + kT2NST;
+    uint64_t *s_full = bars + 2 * kT2NST, *p_full = s_full + 2, *o_done = s_full + 4;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + Lay::OFF_SLOT);
+    volatile int *fail = reinterpret_cast<volatile int *>(smem + Lay::OFF_SLOT + 4);
+    int32_t *bt_s = reinterpret_cast<int32_t *>(smem + Lay::OFF_BT);
+
+    // Work item: the (request, query tile) pair of rank blockIdx.x / Hkv when
+    // all pairs are ordered by decreasing number of K/V tiles (longest
+    // first, so the biggest items do not form the tail), KV head
+    // blockIdx.x % Hkv.  Pairs that do not exist (t0 >= n) cost -1.
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nqt = (p.max_query_len + QTOK - 1) / QTOK;
+    const int npairs = p.R * nqt;
+    int *pick = reinterpret_cast<int *>(smem + Lay::OFF_SLOT + 8);
+    auto cost = [&](int pair) {
+        const int rr = pair / nqt, tq = (pair % nqt) * QTOK;
+        const int nr = p.query_start[rr + 1] - p.query_start[rr];
+        if (tq >= nr) return -1;
+        const int Pr = p.context_lens[rr] - nr;
+        return (Pr + tq + QTOK + kT2KT - 1) / kT2KT;
+    };
+    const int want = blockIdx.x / p.Hkv, hk = blockIdx.x % p.Hkv;
+    int pair = want;  // natural order when there are too many pairs to rank
+    if (npairs <= kT2RankMax) {
+        int *costs = reinterpret_cast<int *>(smem + Lay::OFF_BT);  // reused below
+        for (int i = tid; i < npairs; i += kT2Threads) costs[i] = cost(i);
+        if (tid == 0) *pick = -1;
+        __syncthreads();
+        for (int i = tid; i < npairs; i += kT2Threads) {
+            const int ci = costs[i];
+            int rank = 0;
+            for (int j = 0; j < npairs; ++j) {
+                const int cj = costs[j];
+                rank += (cj > ci || (cj == ci && j < i)) ? 1 : 0;
+            }
+            if (rank == want) *pick = i;
+        }
+        __syncthreads();
+        pair = *pick;
+    }
+    if (pair < 0) return;
+    const int r = pair / nqt, qt = pair % nqt;
+    const int qs = p.query_start[r];
+    const int n = p.query_start[r + 1] - qs;
+    const int t0 = qt * QTOK;
+    if (t0 >= n) return;
+    const int cap = p.MB << p.bs_log2;
+    const int L = p.context_lens[r];
+    if (L > cap || L < n) {
+        if (threadIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+        return;
+    }
+    const int P = L - n;
+    const int kv_end = min(L, P + t0 + QTOK);
+    const int ntiles = (kv_end + kT2KT - 1) / kT2KT;
+    const int nblk = (kv_end + p.bs - 1) >> p.bs_log2;
+    if (nblk > Lay::BT_MAX) {  // the host routes such requests elsewhere
+        if (tid == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+        return;
+    }
+
+    // ---- set-up: block-table slice, Q tiles (cp.async), barriers, TMEM -----------
+    const int32_t *bt_g = p.block_table + static_cast<size_t>(r) * p.MB;
+    for (int i = tid; i < nblk; i += kT2Threads) {
+        int b = bt_g[i];
+        if (b < 0 || b >= p.num_blocks) {
+            pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+            b = 0;
+        }
+        bt_s[i] = b;
+    }
+    for (int idx = tid; idx < 256 * CH; idx += kT2Threads) {
+        const int m = idx / CH, c = idx % CH;  // row m of the CTA's 256
+        const int t = t0 + m / GQ;
+        const bool valid = t < n;
+        const __nv_bfloat16 *src =
+            p.q + (static_cast<size_t>(qs + (valid ? t : 0)) * p.Hq + hk * GQ + m % GQ) * D + c * 8;
+        const uint32_t tile = sq + (m >> 7) * (128 * D * 2);
+        cp_async16(tile + pa::tc::sw128(m & 127, c * 8, 128), src, valid);
+    }
+    cp_async_commit();
+    if (tid == 0) {
+        for (int i = 0; i < kT2NST; ++i) {
+            pa::mbar_init(&kv_full[i], 1);
+            pa::mbar_init(&kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            pa::mbar_init(&s_full[i], 1);
+            pa::mbar_init(&p_full[i], 128);
+            pa::mbar_init(&o_done[i], 1);
+        }
+        *fail = 0;
+        pa::fence_barrier_init();
+    }
+    if (warp == 8) pa::tc::alloc(tslot, 512);
+    cp_async_wait<0>();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    pa::tc::fence_before();
+    __syncthreads();
+    pa::tc::fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 9) {
+        // ---------------- loader ----------------
+        if (lane == 0) {
+            const int rows_total = static_cast<int>(p.num_blocks * p.Hkv) << p.bs_log2;
+            for (int j = 0; j < ntiles && !*fail; ++j) {
+                const int st = j % kT2NST;
+                if (j >= kT2NST && !pa::mbar_wait(&kv_empty[st], ((j / kT2NST) - 1) & 1)) {
+                    *fail = 1;
+                    break;
+                }
+                pa::mbar_arrive_expect_tx(&kv_full[st], TILE_TX);
+                const uint32_t kst = skv + st * 2 * Lay::T_BYTES, vst = kst + Lay::T_BYTES;
+                for (int b = 0; b < kT2KT; b += p.bs) {  // bs >= 8: boxes land 1024-aligned
+                    const int tok = j * kT2KT + b;
+                    const int y = tok < kv_end
+                                      ? ((bt_s[tok >> p.bs_log2] * p.Hkv + hk) << p.bs_log2)
+                                      : rows_total;  // out of bounds: zero-filled
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h) {
+                        const uint32_t off = h * kT2KT * 128 + b * 128;
+                        tma_load_2d(kst + off, &kmap, h * 64, y, &kv_full[st]);
+                        tma_load_2d(vst + off, &vmap, h * 64, y, &kv_full[st]);
+                    }
+                }
+            }
+        }
+    } else if (warp == 8) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t kIdS = pa::tc::idesc_bf16(128, kT2KT, 0, 0);
+            constexpr uint32_t kIdO = pa::tc::idesc_bf16(128, D, 0, 1);
+            auto issue_s = [&](int wg, int st) {
+                const uint32_t qb = sq + wg * (128 * D * 2);
+                const uint32_t kb = skv + st * 2 * Lay::T_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint64_t a =
+                        pa::tc::sdesc(qb + (ks >> 2) * 128 * 128 + (ks & 3) * 32, 16, 1024);
+                    const uint64_t b =
+                        pa::tc::sdesc(kb + (ks >> 2) * kT2KT * 128 + (ks & 3) * 32, 16, 1024);
+                    pa::tc::mma_ss(tmem + 256 + wg * 64, a, b, kIdS, ks > 0);
+                }
+                pa::tc::commit(&s_full[wg]);
+            };
+            auto issue_pv = [&](int wg, int st, int first) {
+                const uint32_t vb = skv + st * 2 * Lay::T_BYTES + Lay::T_BYTES;
+                const uint32_t ph = tmem + 384 + wg * 64, pl = ph + 32;
+#pragma unroll
+                for (int ks = 0; ks < kT2KT / 16; ++ks) {
+                    const uint64_t b = pa::tc::sdesc(vb + ks * 16 * 128, kT2KT * 128, 1024);
+                    pa::tc::mma_ts(tmem + wg * 128, ph + ks * 8, b, kIdO,
+                                   (first && ks == 0) ? 0 : 1);
+                    pa::tc::mma_ts(tmem + wg * 128, pl + ks * 8, b, kIdO, 1);
+                }
+                pa::tc::commit(&o_done[wg]);
+            };
+            bool ok = true;
+            for (int j = 0; j < ntiles && ok; ++j) {
+                const int st = j % kT2NST;
+                ok = pa::mbar_wait(&kv_full[st], (j / kT2NST) & 1);
+                if (!ok) break;
+                pa::tc::fence_after();
+                for (int wg = 0; wg < 2 && ok; ++wg) {
+                    if (j > 0) {
+                        ok = pa::mbar_wait(&p_full[wg], (j - 1) & 1);
+                        if (!ok) break;
+                        pa::tc::fence_after();
+                        issue_pv(wg, (j - 1) % kT2NST, j == 1);
+                        if (wg == 1) pa::tc::commit(&kv_empty[(j - 1) % kT2NST]);
+                    }
+                    issue_s(wg, st);
+                }
+            }
+            for (int wg = 0; wg < 2 && ok; ++wg) {
+                ok = pa::mbar_wait(&p_full[wg], (ntiles - 1) & 1);
+                if (!ok) break;
+                pa::tc::fence_after();
+                issue_pv(wg, (ntiles - 1) % kT2NST, ntiles == 1);
+            }
+            if (!ok) *fail = 1;
+        }
+    } else {
+        // ---------------- softmax warp groups ----------------
+        const int wg = warp >> 2;                 // query tile A or B
+        const int row = tid & 127;                // TMEM lane
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t o_col = wg * 128, s_col = 256 + wg * 64, ph_col = 384 + wg * 64;
+        const int m = wg * 128 + row;
+        const int pos = P + min(t0 + m / GQ, n - 1);
+        float m_used = -INFINITY, lsum = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            ok = pa::mbar_wait(&s_full[wg], j & 1);
+            if (!ok) break;
+            pa::tc::fence_after();
+            uint32_t sr[2][32];
+            pa::tc::ld32(lane_base + s_col, sr[0]);
+            pa::tc::ld32(lane_base + s_col + 32, sr[1]);
+            pa::tc::wait_ld();
+            const int j0 = j * kT2KT;
+            float s[64];
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float v = __uint_as_float(sr[c >> 5][c & 31]) * p.qscale;
+                s[c] = (j0 + c <= pos) ? v : -INFINITY;
+                tmax = fmaxf(tmax, s[c]);
+            }
+            float alpha = 1.f;
+            if (tmax > m_used + kTcTau) {
+                alpha = (m_used == -INFINITY) ? 0.f : exp2f(m_used - tmax);
+                m_used = tmax;
+            }
+            uint32_t ph[32], pl[32];
+            float rs = 0.f;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float p0 = fast_exp2(s[2 * c] - m_used);
+                const float p1 = fast_exp2(s[2 * c + 1] - m_used);
+                rs += p0 + p1;
+                ph[c] = pack_bf16(p0, p1);
+                const float2 hv = pa::bf16x2_to_float2(ph[c]);
+                pl[c] = pack_bf16(p0 - hv.x, p1 - hv.y);
+            }
+            lsum = lsum * alpha + rs;
+            if (j > 0) {  // the previous PV must be done: O stable, P free
+                ok = pa::mbar_wait(&o_done[wg], (j - 1) & 1);
+                if (!ok) break;
+                pa::tc::fence_after();
+                if (__any_sync(pa::kFull, alpha != 1.f)) {
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        pa::tc::ld32(lane_base + o_col + c0, o);
+                        pa::tc::wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        pa::tc::st32(lane_base + o_col + c0, o);
+                    }
+                }
+            }
+            if (j == ntiles - 1 && wg == 0) {
+                // rows past the context in the last tile may hold anything
+                // (unwritten slots); P is 0 there but 0 * NaN is NaN: zero them
+                const int first = kv_end - j0;
+                const uint32_t vst = skv + (j % kT2NST) * 2 * Lay::T_BYTES + Lay::T_BYTES;
+                for (int idx = row; idx < (kT2KT - first) * CH; idx += 128) {
+                    const int rr = first + idx / CH, c = idx % CH;
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(
+                                     vst + pa::tc::sw128(rr, c * 8, kT2KT)),
+                                 "r"(0u)
+                                 : "memory");
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            pa::tc::st32(lane_base + ph_col, ph);
+            pa::tc::st32(lane_base + ph_col + 32, pl);
+            pa::tc::wait_st();
+            pa::tc::fence_before();
+            mbar_arrive(&p_full[wg]);
+        }
+        if (ok) ok = pa::mbar_wait(&o_done[wg], (ntiles - 1) & 1);
+        if (ok) {
+            pa::tc::fence_after();
+            const int t = t0 + m / GQ;
+            const float inv = 1.f / lsum;
+            __nv_bfloat16 *dst =
+                p.out + (static_cast<size_t>(qs + min(t, n - 1)) * p.Hq + hk * GQ + m % GQ) * D;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o[32];
+                pa::tc::ld32(lane_base + o_col + c0, o);
+                pa::tc::wait_ld();
+                if (t < n) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 8) {
+                        uint4 w4;
+                        w4.x = pack_bf16(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv);
+                        w4.y = pack_bf16(__uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+                        w4.z = pack_bf16(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv);
+                        w4.w = pack_bf16(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(dst + c0 + c) = w4;
+                    }
+                }
+            }
+        } else {
+            *fail = 1;
+        }
+    }
+    // ---- tear-down ----------------------------------------------------------------
+    pa::tc::fence_before();
+    __syncthreads();
+    if (*fail) {
+        // a wait ran out: record it and give the MMAs and copies in flight a
+        // bounded chance to land before the TMEM and shared memory go away
+        if (tid == 0) {
+            pa::record_error(p.err, PA_DEVERR_TIMEOUT);
+            for (int i = 0; i < 2; ++i) (void)pa::mbar_wait(&o_done[i], 0);
+            for (int i = 0; i < kT2NST; ++i) (void)pa::mbar_wait(&kv_full[i], 0);
+        }
+        __syncthreads();
+    }
+    if (warp == 8) pa::tc::dealloc(tmem, 512);
+}
+
 int log2_int(int x) {
     int l = 0;
     while ((1 << l) < x) ++l;
@@ -600,8 +973,75 @@ int launch_tc(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
     return pa::check_launch("prefill launch");
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no
+// libcuda link dependency), looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// A pool viewed as a 2D tensor of rows (block, KV head, slot) x head_dim,
+// read in boxes of 64 columns x block_size rows with the 128-byte swizzle.
+int pool_tensor_map(CUtensorMap *map, const void *pool, int64_t rows, int D, int bs) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return pa::fail(PA_ERR_UNSUPPORTED, "prefill: no cuTensorMapEncodeTiled");
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bs)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK
+                             : pa::fail(PA_ERR_CUDA, "prefill: tensor map encode failed (%d)", (int)r);
+}
+
+// The warp-specialised kernel needs blocks of 8..64 tokens, a block-table
+// slice of at most BT_MAX entries and 32-bit pool row coordinates.
+template <int D>
+bool tc2_ok(const PrefillParams &p) {
+    const int64_t rows = (p.num_blocks * p.Hkv) << p.bs_log2;
+    return p.bs >= 8 && p.bs <= 64 && p.MB <= Tc2Layout<D>::BT_MAX && rows < (int64_t(1) << 31);
+}
+
+template <int D, int GQ>
+int launch_tc2(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
+    const int64_t rows = (p.num_blocks * p.Hkv) << p.bs_log2;
+    CUtensorMap kmap, vmap;
+    if (int rc = pool_tensor_map(&kmap, p.k_cache, rows, D, p.bs)) return rc;
+    if (int rc = pool_tensor_map(&vmap, p.v_cache, rows, D, p.bs)) return rc;
+    const size_t smem = Tc2Layout<D>::SMEM;
+    auto kern = prefill_tc2_kernel<D, GQ>;
+    (void)cudaGetLastError();
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return pa::cuda_fail(e, "prefill: shared memory attribute");
+    constexpr int qtok = 256 / GQ;
+    const int64_t ctas = int64_t((max_query_len + qtok - 1) / qtok) * p.R * p.Hkv;
+    if (ctas > 0x7fffffff) return pa::fail(PA_ERR_INVALID, "prefill: grid too large");
+    kern<<<static_cast<unsigned>(ctas), kT2Threads, smem, stream>>>(p, kmap, vmap);
+    return pa::check_launch("prefill launch");
+}
+
+#ifndef PA_PREFILL_WARP_SPECIALIZED
+#define PA_PREFILL_WARP_SPECIALIZED 1
+#endif
+
 template <int D, int GQ>
 int launch(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
+    if (PA_PREFILL_TCGEN05 && PA_PREFILL_WARP_SPECIALIZED && tc2_ok<D>(p))
+        return launch_tc2<D, GQ>(p, max_query_len, stream);
     if (PA_PREFILL_TCGEN05) return launch_tc<D, GQ>(p, max_query_len, stream);
     const size_t smem = kRows * D * 2 + 4 * kKT * D * 2;
     auto kern = prefill_kernel<D, GQ>;
@@ -693,6 +1133,7 @@ extern "C" int pa_prefill_chunk(void *out, const void *q, const void *k_cache, c
     p.bs = block_size;
     p.bs_log2 = log2_int(block_size);
     p.MB = max_blocks_per_seq;
+    p.max_query_len = max_query_len;
     p.qscale = scale * kLog2e;
     const int gq = Hq / Hkv;
     return head_dim == 128 ? dispatch_gq<128>(gq, p, max_query_len, stream)

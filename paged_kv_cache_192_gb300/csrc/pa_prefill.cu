@@ -18,6 +18,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -588,13 +589,16 @@ __global__ void __launch_bounds__(128, 2) prefill_tc_kernel(const PrefillParams 
 //   warps 4-7  softmax of query tile B (rows 128..255, same lanes)
 //   warp 8     issues every tcgen05.mma (one lane)
 //   warp 9     loads K/V tiles with TMA (2D tensor copies, 128-byte swizzle)
-// The tensor core alternates between the tiles: while one tile's softmax
-// runs, it computes the other tile's QK^T or PV.  64-token K/V tiles go
-// through a 3-stage ring; a (block, 64 columns) box per copy, gathered
-// through the block table; boxes for blocks past the context are read out of
-// bounds and arrive zero-filled.  TMEM (512 columns): O_A [0,128),
-// O_B [128,256), S_A [256,320), S_B [320,384), P_A hi/lo [384,448),
-// P_B hi/lo [448,512).  All hand-offs are mbarriers; every wait is bounded.
+// S is double-buffered per query tile and computed one K/V tile ahead: the
+// MMA warp issues QK^T of tile j+1 before PV of tile j, so a softmax warp
+// group finds its next S ready when it finishes the current one, and the
+// tensor core works on the other group's products meanwhile.  P (bf16 hi and
+// lo halves) overwrites the S buffer it was computed from.  64-token K/V
+// tiles go through a 3-stage ring; a (block, 64 columns) box per copy,
+// gathered through the block table; boxes for blocks past the context are
+// read out of bounds and arrive zero-filled.  TMEM (512 columns):
+// O_A [0,128), O_B [128,256), S_A[0..1] [256,384), S_B[0..1] [384,512).
+// All hand-offs are mbarriers; every wait is bounded.
 // ---------------------------------------------------------------------------
 constexpr int kT2KT = 64;      // KV tokens per tile
 constexpr int kT2NST = 3;      // K/V ring stages
@@ -607,7 +611,7 @@ struct Tc2Layout {
     static constexpr int T_BYTES = kT2KT * D * 2;    // one K or V tile
     static constexpr int OFF_KV = Q_BYTES;           // [stage][K|V]
     static constexpr int OFF_BAR = OFF_KV + kT2NST * 2 * T_BYTES;
-    static constexpr int N_BAR = 3 * kT2NST + 6;     // kv_full, kv_empty, (s, p, o) x 2
+    static constexpr int N_BAR = 2 * kT2NST + 8;     // kv_full, kv_empty, s x 4, (p, o) x 2
     static constexpr int OFF_SLOT = OFF_BAR + 8 * N_BAR;
     static constexpr int OFF_BT = OFF_SLOT + 16;
     static constexpr int BT_MAX = 1024;
@@ -642,7 +646,8 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     const uint32_t skv = sq + Lay::OFF_KV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::OFF_BAR);
     uint64_t *kv_full = bars, *kv_empty = bars + kT2NST;
-    uint64_t *s_full = bars + 2 * kT2NST, *p_full = s_full + 2, *o_done = s_full + 4;
+    // s_full[2 * group + buffer]; p_full / o_done per query-tile group
+    uint64_t *s_full = bars + 2 * kT2NST, *p_full = s_full + 4, *o_done = p_full + 2;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + Lay::OFF_SLOT);
     volatile int *fail = reinterpret_cast<volatile int *>(smem + Lay::OFF_SLOT + 4);
     int32_t *bt_s = reinterpret_cast<int32_t *>(smem + Lay::OFF_BT);
@@ -727,9 +732,9 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             pa::mbar_init(&kv_full[i], 1);
             pa::mbar_init(&kv_empty[i], 1);
         }
+        for (int i = 0; i < 4; ++i) pa::mbar_init(&s_full[i], 1);
         for (int i = 0; i < 2; ++i) {
-            pa::mbar_init(&s_full[i], 1);
-            pa::mbar_init(&p_full[i], 128);
+            pa::mbar_init(&p_full[i], 4);  // one arrival per softmax warp
             pa::mbar_init(&o_done[i], 1);
         }
         *fail = 0;
@@ -771,71 +776,95 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         }
     } else if (warp == 8) {
         // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            constexpr uint32_t kIdS = pa::tc::idesc_bf16(128, kT2KT, 0, 0);
-            constexpr uint32_t kIdO = pa::tc::idesc_bf16(128, D, 0, 1);
-            auto issue_s = [&](int wg, int st) {
-                const uint32_t qb = sq + wg * (128 * D * 2);
-                const uint32_t kb = skv + st * 2 * Lay::T_BYTES;
+        // The whole warp follows the schedule (barrier waits, descriptor
+        // arithmetic on warp-uniform values); one elected lane issues each
+        // tcgen05 operation.  Shared-memory descriptors are built once and
+        // advanced by constant offsets (16-byte units in the start-address
+        // field; every operand lies below 227 KB, so the field cannot carry).
+        constexpr uint32_t kIdS = pa::tc::idesc_bf16(128, kT2KT, 0, 0);
+        constexpr uint32_t kIdO = pa::tc::idesc_bf16(128, D, 0, 1);
+        constexpr uint32_t kStage = (2 * Lay::T_BYTES) >> 4;
+        const uint64_t dq = pa::tc::sdesc(sq, 16, 1024);
+        const uint64_t dk = pa::tc::sdesc(skv, 16, 1024);
+        const uint64_t dv = pa::tc::sdesc(skv + Lay::T_BYTES, kT2KT * 128, 1024);
+        // S of tile j for group wg goes to TMEM columns 256 + 128 wg + 64 (j % 2)
+        auto issue_s = [&](int wg, int j) {
+            const uint64_t a0 = dq + static_cast<uint32_t>(wg * ((128 * D * 2) >> 4));
+            const uint64_t b0 = dk + static_cast<uint32_t>((j % kT2NST) * kStage);
+            const uint32_t sc = tmem + 256 + wg * 128 + (j & 1) * 64;
+            if (pa::tc::elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t a =
-                        pa::tc::sdesc(qb + (ks >> 2) * 128 * 128 + (ks & 3) * 32, 16, 1024);
-                    const uint64_t b =
-                        pa::tc::sdesc(kb + (ks >> 2) * kT2KT * 128 + (ks & 3) * 32, 16, 1024);
-                    pa::tc::mma_ss(tmem + 256 + wg * 64, a, b, kIdS, ks > 0);
-                }
-                pa::tc::commit(&s_full[wg]);
-            };
-            auto issue_pv = [&](int wg, int st, int first) {
-                const uint32_t vb = skv + st * 2 * Lay::T_BYTES + Lay::T_BYTES;
-                const uint32_t ph = tmem + 384 + wg * 64, pl = ph + 32;
+                for (int ks = 0; ks < D / 16; ++ks)
+                    pa::tc::mma_ss(sc, a0 + (((ks >> 2) * 128 * 128 + (ks & 3) * 32) >> 4),
+                                   b0 + (((ks >> 2) * kT2KT * 128 + (ks & 3) * 32) >> 4), kIdS,
+                                   ks > 0);
+                pa::tc::commit(&s_full[2 * wg + (j & 1)]);
+            }
+            __syncwarp();
+        };
+        // O_wg += P_hi V + P_lo V; P of tile j sits in the S buffer it came from
+        auto issue_pv = [&](int wg, int j) {
+            const uint64_t b0 = dv + static_cast<uint32_t>((j % kT2NST) * kStage);
+            const uint32_t ph = tmem + 256 + wg * 128 + (j & 1) * 64, pl = ph + 32;
+            const uint32_t od = tmem + wg * 128;
+            const int acc0 = j > 0;
+            if (pa::tc::elect_one()) {
 #pragma unroll
                 for (int ks = 0; ks < kT2KT / 16; ++ks) {
-                    const uint64_t b = pa::tc::sdesc(vb + ks * 16 * 128, kT2KT * 128, 1024);
-                    pa::tc::mma_ts(tmem + wg * 128, ph + ks * 8, b, kIdO,
-                                   (first && ks == 0) ? 0 : 1);
-                    pa::tc::mma_ts(tmem + wg * 128, pl + ks * 8, b, kIdO, 1);
+                    const uint64_t b = b0 + ((ks * 16 * 128) >> 4);
+                    pa::tc::mma_ts(od, ph + ks * 8, b, kIdO, ks == 0 ? acc0 : 1);
+                    pa::tc::mma_ts(od, pl + ks * 8, b, kIdO, 1);
                 }
                 pa::tc::commit(&o_done[wg]);
-            };
-            bool ok = true;
-            for (int j = 0; j < ntiles && ok; ++j) {
-                const int st = j % kT2NST;
-                ok = pa::mbar_wait(&kv_full[st], (j / kT2NST) & 1);
+            }
+            __syncwarp();
+        };
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+            return __all_sync(pa::kFull, pa::mbar_wait(bar, parity));
+        };
+        // Issue order: S(0) of both groups; then per tile j: S(j+1) of both
+        // groups (its buffer last held P(j-1), whose PV was issued before),
+        // PV(j) of group 0, PV(j) of group 1, release of the K/V stage.
+        // Group 1's PV of the last tile thus follows group 0's arrival, which
+        // comes after group 0 cleared the stale V rows of that tile.
+        bool ok = wait_all(&kv_full[0], 0);
+        if (ok) {
+            pa::tc::fence_after();
+            issue_s(0, 0);
+            issue_s(1, 0);
+        }
+        for (int j = 0; j < ntiles && ok; ++j) {
+            if (j + 1 < ntiles) {
+                ok = wait_all(&kv_full[(j + 1) % kT2NST], ((j + 1) / kT2NST) & 1);
                 if (!ok) break;
                 pa::tc::fence_after();
-                for (int wg = 0; wg < 2 && ok; ++wg) {
-                    if (j > 0) {
-                        ok = pa::mbar_wait(&p_full[wg], (j - 1) & 1);
-                        if (!ok) break;
-                        pa::tc::fence_after();
-                        issue_pv(wg, (j - 1) % kT2NST, j == 1);
-                        if (wg == 1) pa::tc::commit(&kv_empty[(j - 1) % kT2NST]);
-                    }
-                    issue_s(wg, st);
-                }
+                issue_s(0, j + 1);
+                issue_s(1, j + 1);
             }
             for (int wg = 0; wg < 2 && ok; ++wg) {
-                ok = pa::mbar_wait(&p_full[wg], (ntiles - 1) & 1);
+                ok = wait_all(&p_full[wg], j & 1);
                 if (!ok) break;
                 pa::tc::fence_after();
-                issue_pv(wg, (ntiles - 1) % kT2NST, ntiles == 1);
+                issue_pv(wg, j);
             }
-            if (!ok) *fail = 1;
+            if (ok && pa::tc::elect_one()) pa::tc::commit(&kv_empty[j % kT2NST]);
+            __syncwarp();
         }
+        if (!ok) *fail = 1;
     } else {
         // ---------------- softmax warp groups ----------------
         const int wg = warp >> 2;                 // query tile A or B
         const int row = tid & 127;                // TMEM lane
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        const uint32_t o_col = wg * 128, s_col = 256 + wg * 64, ph_col = 384 + wg * 64;
+        const uint32_t o_col = wg * 128;
         const int m = wg * 128 + row;
         const int pos = P + min(t0 + m / GQ, n - 1);
+        const float qs2 = p.qscale;  // softmax scale in log2 units
         float m_used = -INFINITY, lsum = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            ok = pa::mbar_wait(&s_full[wg], j & 1);
+            const uint32_t s_col = 256 + wg * 128 + (j & 1) * 64;
+            ok = pa::mbar_wait(&s_full[2 * wg + (j & 1)], (j >> 1) & 1);
             if (!ok) break;
             pa::tc::fence_after();
             uint32_t sr[2][32];
@@ -844,31 +873,48 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             pa::tc::wait_ld();
             const int j0 = j * kT2KT;
             float s[64];
-            float tmax = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float v = __uint_as_float(sr[c >> 5][c & 31]) * p.qscale;
-                s[c] = (j0 + c <= pos) ? v : -INFINITY;
-                tmax = fmaxf(tmax, s[c]);
+            for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+            if (j0 + kT2KT - 1 > pos) {  // tile on or past the diagonal: mask
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (j0 + c > pos) s[c] = -INFINITY;
             }
+            // row maximum as a tree (independent chains)
+            float mx[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) mx[c] = fmaxf(s[c], s[c + 8]);
+#pragma unroll
+            for (int c = 16; c < 64; c += 8) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], s[c + e]);
+            }
+            const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                               qs2;
             float alpha = 1.f;
             if (tmax > m_used + kTcTau) {
                 alpha = (m_used == -INFINITY) ? 0.f : exp2f(m_used - tmax);
                 m_used = tmax;
             }
             uint32_t ph[32], pl[32];
-            float rs = 0.f;
+            float2 rs2[4] = {};
+            const float nm = -m_used;
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                const float p0 = fast_exp2(s[2 * c] - m_used);
-                const float p1 = fast_exp2(s[2 * c + 1] - m_used);
-                rs += p0 + p1;
+                const float p0 = fast_exp2(fmaf(s[2 * c], qs2, nm));
+                const float p1 = fast_exp2(fmaf(s[2 * c + 1], qs2, nm));
+                rs2[c & 3].x += p0;
+                rs2[c & 3].y += p1;
                 ph[c] = pack_bf16(p0, p1);
-                const float2 hv = pa::bf16x2_to_float2(ph[c]);
-                pl[c] = pack_bf16(p0 - hv.x, p1 - hv.y);
+                const float2 lo = pa::ffma2(pa::bf16x2_to_float2(ph[c]), make_float2(-1.f, -1.f),
+                                            make_float2(p0, p1));
+                pl[c] = pack_bf16(lo.x, lo.y);
             }
+            const float rs = ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y)) +
+                             ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
             lsum = lsum * alpha + rs;
-            if (j > 0) {  // the previous PV must be done: O stable, P free
+            if (j > 0) {  // PV(j-1) must be done before O is rescaled
                 ok = pa::mbar_wait(&o_done[wg], (j - 1) & 1);
                 if (!ok) break;
                 pa::tc::fence_after();
@@ -887,7 +933,8 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             }
             if (j == ntiles - 1 && wg == 0) {
                 // rows past the context in the last tile may hold anything
-                // (unwritten slots); P is 0 there but 0 * NaN is NaN: zero them
+                // (unwritten slots); P is 0 there but 0 * NaN is NaN: zero them.
+                // Group 1's PV of this tile is issued after group 0's arrival.
                 const int first = kv_end - j0;
                 const uint32_t vst = skv + (j % kT2NST) * 2 * Lay::T_BYTES + Lay::T_BYTES;
                 for (int idx = row; idx < (kT2KT - first) * CH; idx += 128) {
@@ -899,11 +946,12 @@ __global__ void __launch_bounds__(kT2Threads, 1)
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
-            pa::tc::st32(lane_base + ph_col, ph);
-            pa::tc::st32(lane_base + ph_col + 32, pl);
+            pa::tc::st32(lane_base + s_col, ph);
+            pa::tc::st32(lane_base + s_col + 32, pl);
             pa::tc::wait_st();
             pa::tc::fence_before();
-            mbar_arrive(&p_full[wg]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[wg]);
         }
         if (ok) ok = pa::mbar_wait(&o_done[wg], (ntiles - 1) & 1);
         if (ok) {
@@ -992,7 +1040,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // A pool viewed as a 2D tensor of rows (block, KV head, slot) x head_dim,
 // read in boxes of 64 columns x block_size rows with the 128-byte swizzle.
-int pool_tensor_map(CUtensorMap *map, const void *pool, int64_t rows, int D, int bs) {
+int encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int D, int bs) {
     auto enc = tensor_map_encoder();
     if (!enc) return pa::fail(PA_ERR_UNSUPPORTED, "prefill: no cuTensorMapEncodeTiled");
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
@@ -1005,6 +1053,54 @@ int pool_tensor_map(CUtensorMap *map, const void *pool, int64_t rows, int D, int
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK
                              : pa::fail(PA_ERR_CUDA, "prefill: tensor map encode failed (%d)", (int)r);
+}
+
+// A tensor map is a pure function of (address, rows, D, bs), so the last few
+// encoded maps are kept and reused by value: a serving loop calls with the
+// same two pools every step and the encode (host work of a few microseconds
+// per map) is then paid once.
+int pool_tensor_map(CUtensorMap *map, const void *pool, int64_t rows, int D, int bs) {
+    struct Entry {
+        const void *pool;
+        int64_t rows;
+        int D, bs;
+        CUtensorMap map;
+    };
+    constexpr int kSlots = 8;
+    static std::mutex mu;
+    static Entry cache[kSlots];
+    static int used = 0, next = 0;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < used; ++i)
+            if (cache[i].pool == pool && cache[i].rows == rows && cache[i].D == D &&
+                cache[i].bs == bs) {
+                *map = cache[i].map;
+                return PA_OK;
+            }
+    }
+    if (int rc = encode_pool_map(map, pool, rows, D, bs)) return rc;
+    std::lock_guard<std::mutex> lk(mu);
+    cache[next] = Entry{pool, rows, D, bs, *map};
+    next = (next + 1) % kSlots;
+    if (used < kSlots) ++used;
+    return PA_OK;
+}
+
+// cudaFuncSetAttribute for the dynamic shared memory of `kern`, once per
+// device (bit d of *done).
+template <typename K>
+int set_smem_once(K kern, size_t smem, std::atomic<uint64_t> *done) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return pa::cuda_fail(cudaGetLastError(), "prefill: device");
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (bit && (done->load(std::memory_order_acquire) & bit)) return PA_OK;
+    (void)cudaGetLastError();
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return pa::cuda_fail(e, "prefill: shared memory attribute");
+    if (bit) done->fetch_or(bit, std::memory_order_acq_rel);
+    return PA_OK;
 }
 
 // The warp-specialised kernel needs blocks of 8..64 tokens, a block-table
@@ -1023,10 +1119,9 @@ int launch_tc2(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
     if (int rc = pool_tensor_map(&vmap, p.v_cache, rows, D, p.bs)) return rc;
     const size_t smem = Tc2Layout<D>::SMEM;
     auto kern = prefill_tc2_kernel<D, GQ>;
+    static std::atomic<uint64_t> attr_done{0};
+    if (int rc = set_smem_once(kern, smem, &attr_done)) return rc;
     (void)cudaGetLastError();
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return pa::cuda_fail(e, "prefill: shared memory attribute");
     constexpr int qtok = 256 / GQ;
     const int64_t ctas = int64_t((max_query_len + qtok - 1) / qtok) * p.R * p.Hkv;
     if (ctas > 0x7fffffff) return pa::fail(PA_ERR_INVALID, "prefill: grid too large");

@@ -64,6 +64,15 @@ __device__ __forceinline__ void commit(uint64_t *bar) {
         : "memory");
 }
 
+// True in exactly one active lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 __device__ __forceinline__ void fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }

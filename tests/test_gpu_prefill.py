@@ -52,6 +52,39 @@ def test_prefill_shapes(Hq, Hkv, d, bs):
     compare(got, ref, torch.bfloat16, f"prefill {Hq}/{Hkv} d{d} bs{bs}")
 
 
+def test_prefill_many_requests_natural_order():
+    """70 requests x up to 4 query tiles = 280 (request, query tile) pairs:
+    past the in-kernel longest-first ranking, the pairs run in request order."""
+    rng = np.random.default_rng(5)
+    n_new = [int(x) for x in rng.integers(1, 201, size=70)]
+    n_new[3] = 200
+    priors = [int(x) for x in rng.integers(0, 300, size=70)]
+    w, q = _prefill_workload(priors, n_new, Hq=8, Hkv=2, seed=5)
+    got, ref = _run(w, q, priors, n_new)
+    compare(got, ref, torch.bfloat16, "prefill 70 requests")
+
+
+@pytest.mark.parametrize("bs", [128])
+def test_prefill_large_block_fallback_kernel(bs):
+    """Block size 128 is served by the 128-thread tcgen05 kernel."""
+    priors = [0, 200, 77, 1000]
+    n_new = [100, 129, 3, 64]
+    w, q = _prefill_workload(priors, n_new, Hq=8, Hkv=2, bs=bs, seed=6)
+    got, ref = _run(w, q, priors, n_new)
+    compare(got, ref, torch.bfloat16, f"prefill bs{bs}")
+
+
+def test_prefill_long_block_table_fallback_kernel():
+    """8-token blocks over 8,300 tokens: a block table of 1,038 entries, past
+    the warp-specialised kernel's staged slice."""
+    priors = [8236, 5]
+    n_new = [64, 40]
+    w, q = _prefill_workload(priors, n_new, Hq=8, Hkv=2, bs=8, seed=7)
+    assert w.table.shape[1] > 1024
+    got, ref = _run(w, q, priors, n_new)
+    compare(got, ref, torch.bfloat16, "prefill long table")
+
+
 def test_prefill_first_query_sees_only_itself():
     w, q = _prefill_workload([0], [48], seed=2)
     got, _ = _run(w, q, [0], [48])

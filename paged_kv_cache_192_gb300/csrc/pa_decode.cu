@@ -519,6 +519,44 @@ __device__ __forceinline__ void prefetch_q(const DecodeParams &p, const Cursor &
 // End of this warp's segment of item c: write the output (the whole item is
 // in this warp's range) or a partial, and merge the item's partials if this
 // segment is the last of them to finish.
+// Merge of an item spread over more than 32 warps (a few very long
+// sequences): the weights are recomputed from loads instead of travelling
+// by shuffle.  Kept out of line so the common path's code is unaffected.
+template <typename T, int D, int GQ>
+__device__ __noinline__ void merge_many(const DecodeParams &p, size_t hq0, int nseg, int lane) {
+    constexpr int EL = D / 32;
+    T *out = static_cast<T *>(p.out);
+    for (int h = 0; h < GQ; ++h) {
+        const size_t sb = (hq0 + h) * p.maxseg;
+        const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + sb;
+        float M = -INFINITY;
+        for (int sg = lane; sg < nseg; sg += 32) M = fmaxf(M, __ldcg(&ml[sg]).x);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(pa::kFull, M, o));
+        float den = 0.f;
+        for (int sg = lane; sg < nseg; sg += 32) {
+            const float2 v = __ldcg(&ml[sg]);
+            den += exp2f(v.x - M) * v.y;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(pa::kFull, den, o);
+        float acc[EL];
+#pragma unroll
+        for (int e = 0; e < EL; ++e) acc[e] = 0.f;
+        const float *src = p.ws_acc + sb * D + EL * lane;
+#pragma unroll 4
+        for (int sg = 0; sg < nseg; ++sg) {
+            const float f = exp2f(__ldcg(&ml[sg]).x - M);
+#pragma unroll
+            for (int e = 0; e < EL; ++e) acc[e] += f * __ldcg(src + sg * D + e);
+        }
+        const float inv = 1.f / den;
+#pragma unroll
+        for (int e = 0; e < EL; e += 2)
+            store_pair<T>(out + (hq0 + h) * D + EL * lane + e, acc[e] * inv, acc[e + 1] * inv);
+    }
+}
+
 template <typename T, int D, int GQ>
 __device__ __forceinline__ void finish_segment(WarpAttn<T, D, GQ> &st, const DecodeParams &p,
                                                const BatchTables &bt, const Cursor &c,
@@ -599,7 +637,12 @@ __device__ __forceinline__ void finish_segment(WarpAttn<T, D, GQ> &st, const Dec
     last = __shfl_sync(pa::kFull, last, 0);
     if (!last) return;
     __syncwarp();
-    // Merge: lane s < nseg holds segment s's (max, sum) per head; every lane
+    if (nseg > 32) {
+        merge_many<T, D, GQ>(p, hq0, nseg, lane);
+        if (lane == 0) atomicExch(ctr, 0ull);
+        return;
+    }
+    // Merge (up to 32 segments): lane s < nseg holds segment s's (max, sum) per head; every lane
     // owns D/32 output elements; all loads are independent (issued ahead).
     // Heads go in groups of up to 4 so the accumulators stay in registers.
     constexpr int EL = D / 32;
@@ -1033,6 +1076,9 @@ int launch_persistent(const DecodeParams &p, cudaStream_t stream) {
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, smem);
     if (e != cudaSuccess) return pa::cuda_fail(e, "decode: occupancy");
+    // the split of the work (and the register budget) is designed for MINB
+    // CTAs per SM; more would only add split items (measured slower)
+    per_sm = std::min(per_sm, C::MINB);
 #ifdef PA_DECODE_FORCE_PER_SM
     per_sm = PA_DECODE_FORCE_PER_SM;
 #endif

@@ -96,6 +96,16 @@ def test_split_matches_unsplit():
     compare(o_whole.double().cpu().numpy(), ref, torch.bfloat16, "whole")
 
 
+@pytest.mark.parametrize("lens,Hq,Hkv", [([32768], 32, 8), ([20000, 3], 8, 1)])
+def test_long_sequence_many_segments(lens, Hq, Hkv):
+    """Few long sequences: each (sequence, KV head) item is spread over more
+    than 32 warps of the persistent grid (one 32k-token sequence: 64
+    segments per item), all merged by log-sum-exp."""
+    w = synth.decode_workload("8b", seed=11, lens=lens, Hq=Hq, Hkv=Hkv)
+    got, ref, _ = run(w, partition_tokens=512)
+    compare(got, ref, torch.bfloat16, f"long {lens}")
+
+
 def test_single_token_returns_v0_exactly():
     w = synth.decode_workload("8b", seed=7, lens=[1, 1, 1])
     _, _, out = run(w)

@@ -239,7 +239,7 @@ class DecodePlan(Plan):
         from paged_kv_cache_192_gb300 import layout, ops
         gen_dev = "cuda" if name == "70b" else "cpu"
         w = synth.decode_workload(name, seed=args.seed, gen_device=gen_dev,
-                                  bs=args.block_size or None)
+                                  bs=args.block_size or None, B=args.batch or None)
         if args.placement == "identity":
             # paging-overhead control: every sequence's blocks consecutive
             table = np.zeros_like(w.table)
@@ -734,6 +734,9 @@ def main(argv=None):
                     help="override the decode workload's block size (block-size sweep)")
     ap.add_argument("--placement", choices=["shuffled", "identity"], default="shuffled",
                     help="physical placement of each sequence's blocks (decode workloads)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the decode workload's batch size (small profiling cases "
+                         "of the same shape)")
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pools", type=int, default=N_POOLS, help="pools rotated between steps")

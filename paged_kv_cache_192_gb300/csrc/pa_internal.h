@@ -1,6 +1,7 @@
 // Host-side helpers shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -29,6 +30,10 @@ inline int check_launch(const char *what) {
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? PA_OK : cuda_fail(e, what);
 }
+
+// 2D tensor map (128-byte swizzle, boxes of 64 columns x box_rows rows) over
+// a bf16 pool of `rows` rows of D elements; cached by value (pa_tma.cpp).
+int pool_tensor_map(CUtensorMap *map, const void *pool, int64_t rows, int D, int box_rows);
 
 inline size_t dtype_size(int dtype) { return dtype == PA_BF16 ? 2 : (dtype == PA_F32 ? 4 : 0); }
 

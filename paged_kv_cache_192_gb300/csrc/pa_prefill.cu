@@ -1021,72 +1021,6 @@ int launch_tc(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
     return pa::check_launch("prefill launch");
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no
-// libcuda link dependency), looked up once.
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-        (void)cudaGetLastError();
-    });
-    return fn;
-}
-
-// A pool viewed as a 2D tensor of rows (block, KV head, slot) x head_dim,
-// read in boxes of 64 columns x block_size rows with the 128-byte swizzle.
-int encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int D, int bs) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return pa::fail(PA_ERR_UNSUPPORTED, "prefill: no cuTensorMapEncodeTiled");
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bs)};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims,
-                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? PA_OK
-                             : pa::fail(PA_ERR_CUDA, "prefill: tensor map encode failed (%d)", (int)r);
-}
-
-// A tensor map is a pure function of (address, rows, D, bs), so the last few
-// encoded maps are kept and reused by value: a serving loop calls with the
-// same two pools every step and the encode (host work of a few microseconds
-// per map) is then paid once.
-int pool_tensor_map(CUtensorMap *map, const void *pool, int64_t rows, int D, int bs) {
-    struct Entry {
-        const void *pool;
-        int64_t rows;
-        int D, bs;
-        CUtensorMap map;
-    };
-    constexpr int kSlots = 8;
-    static std::mutex mu;
-    static Entry cache[kSlots];
-    static int used = 0, next = 0;
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        for (int i = 0; i < used; ++i)
-            if (cache[i].pool == pool && cache[i].rows == rows && cache[i].D == D &&
-                cache[i].bs == bs) {
-                *map = cache[i].map;
-                return PA_OK;
-            }
-    }
-    if (int rc = encode_pool_map(map, pool, rows, D, bs)) return rc;
-    std::lock_guard<std::mutex> lk(mu);
-    cache[next] = Entry{pool, rows, D, bs, *map};
-    next = (next + 1) % kSlots;
-    if (used < kSlots) ++used;
-    return PA_OK;
-}
-
 // cudaFuncSetAttribute for the dynamic shared memory of `kern`, once per
 // device (bit d of *done).
 template <typename K>
@@ -1115,8 +1049,8 @@ template <int D, int GQ>
 int launch_tc2(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
     const int64_t rows = (p.num_blocks * p.Hkv) << p.bs_log2;
     CUtensorMap kmap, vmap;
-    if (int rc = pool_tensor_map(&kmap, p.k_cache, rows, D, p.bs)) return rc;
-    if (int rc = pool_tensor_map(&vmap, p.v_cache, rows, D, p.bs)) return rc;
+    if (int rc = pa::pool_tensor_map(&kmap, p.k_cache, rows, D, p.bs)) return rc;
+    if (int rc = pa::pool_tensor_map(&vmap, p.v_cache, rows, D, p.bs)) return rc;
     const size_t smem = Tc2Layout<D>::SMEM;
     auto kern = prefill_tc2_kernel<D, GQ>;
     static std::atomic<uint64_t> attr_done{0};

@@ -96,6 +96,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -880,18 +887,18 @@ __global__ void __launch_bounds__(kT2Threads, 1)
                 for (int c = 0; c < 64; ++c)
                     if (j0 + c > pos) s[c] = -INFINITY;
             }
-            // row maximum as a tree (independent chains)
+            // row maximum: 8 independent chains of three-input maxima
             float mx[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) mx[c] = fmaxf(s[c], s[c + 8]);
-#pragma unroll
-            for (int c = 16; c < 64; c += 8) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], s[c + e]);
+            for (int e = 0; e < 8; ++e) {
+                float m3 = max3f(s[e], s[8 + e], s[16 + e]);
+                m3 = max3f(m3, s[24 + e], s[32 + e]);
+                m3 = max3f(m3, s[40 + e], s[48 + e]);
+                mx[e] = fmaxf(m3, s[56 + e]);
             }
-            const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
-                               qs2;
+            const float tmax =
+                max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+                qs2;
             float alpha = 1.f;
             if (tmax > m_used + kTcTau) {
                 alpha = (m_used == -INFINITY) ? 0.f : exp2f(m_used - tmax);
@@ -899,13 +906,13 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             }
             uint32_t ph[32], pl[32];
             float2 rs2[4] = {};
-            const float nm = -m_used;
+            const float2 q2 = make_float2(qs2, qs2), nm2 = make_float2(-m_used, -m_used);
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                const float p0 = fast_exp2(fmaf(s[2 * c], qs2, nm));
-                const float p1 = fast_exp2(fmaf(s[2 * c + 1], qs2, nm));
-                rs2[c & 3].x += p0;
-                rs2[c & 3].y += p1;
+                const float2 x = pa::ffma2(make_float2(s[2 * c], s[2 * c + 1]), q2, nm2);
+                const float p0 = fast_exp2(x.x);
+                const float p1 = fast_exp2(x.y);
+                rs2[c & 3] = __fadd2_rn(rs2[c & 3], make_float2(p0, p1));
                 ph[c] = pack_bf16(p0, p1);
                 const float2 lo = pa::ffma2(pa::bf16x2_to_float2(ph[c]), make_float2(-1.f, -1.f),
                                             make_float2(p0, p1));

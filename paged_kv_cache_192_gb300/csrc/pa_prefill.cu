@@ -714,7 +714,8 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         return;
     }
 
-    // ---- set-up: block-table slice, Q tiles (cp.async), barriers, TMEM -----------
+    // ---- set-up: block-table slice, barriers, TMEM; then the loader starts
+    // while warps 0-8 bring in the Q tiles (cp.async) ------------------------------
     const int32_t *bt_g = p.block_table + static_cast<size_t>(r) * p.MB;
     for (int i = tid; i < nblk; i += kT2Threads) {
         int b = bt_g[i];
@@ -724,16 +725,6 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         }
         bt_s[i] = b;
     }
-    for (int idx = tid; idx < 256 * CH; idx += kT2Threads) {
-        const int m = idx / CH, c = idx % CH;  // row m of the CTA's 256
-        const int t = t0 + m / GQ;
-        const bool valid = t < n;
-        const __nv_bfloat16 *src =
-            p.q + (static_cast<size_t>(qs + (valid ? t : 0)) * p.Hq + hk * GQ + m % GQ) * D + c * 8;
-        const uint32_t tile = sq + (m >> 7) * (128 * D * 2);
-        cp_async16(tile + pa::tc::sw128(m & 127, c * 8, 128), src, valid);
-    }
-    cp_async_commit();
     if (tid == 0) {
         for (int i = 0; i < kT2NST; ++i) {
             pa::mbar_init(&kv_full[i], 1);
@@ -748,12 +739,29 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         pa::fence_barrier_init();
     }
     if (warp == 8) pa::tc::alloc(tslot, 512);
-    cp_async_wait<0>();
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     pa::tc::fence_before();
     __syncthreads();
     pa::tc::fence_after();
     const uint32_t tmem = *tslot;
+    if (warp != 9) {
+        // Q tiles: only the MMA warp's QK^T reads them; warps 0-8 load them
+        // and meet on named barrier 1 before it
+        constexpr int kQThreads = kT2Threads - 32;
+        for (int idx = tid; idx < 256 * CH; idx += kQThreads) {
+            const int m = idx / CH, c = idx % CH;  // row m of the CTA's 256
+            const int t = t0 + m / GQ;
+            const bool valid = t < n;
+            const __nv_bfloat16 *src =
+                p.q + (static_cast<size_t>(qs + (valid ? t : 0)) * p.Hq + hk * GQ + m % GQ) * D +
+                c * 8;
+            const uint32_t tile = sq + (m >> 7) * (128 * D * 2);
+            cp_async16(tile + pa::tc::sw128(m & 127, c * 8, 128), src, valid);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(kQThreads) : "memory");
+    }
 
     if (warp == 9) {
         // ---------------- loader ----------------

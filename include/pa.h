@@ -191,6 +191,16 @@ int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void 
                       int dtype, pa_stream_t stream);
 
 /*
+ * pa_check_wait_timeout -- diagnostic of the device-side failure path: one
+ * warp waits, with the same bounded wait (about 2 s) the pipelined kernels
+ * use on their copies and hand-offs, on an mbarrier that nothing completes.
+ * The wait runs out, PA_DEVERR_TIMEOUT is recorded in the device error word
+ * and the kernel returns: nothing faults and the context stays usable.
+ * Asynchronous on `stream`; read the outcome with pa_device_error().
+ */
+int pa_check_wait_timeout(pa_stream_t stream);
+
+/*
  * pa_prefill_chunk -- chunked prefill over paged context ("Melihat Lebih
  * Dalam vLLM v0.7", section "Blueprint Arsitektur 3: Chunked Prefill": a long
  * prompt is cut into chunks of e.g. 512 tokens and run next to decode).

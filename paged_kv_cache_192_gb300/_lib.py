@@ -25,6 +25,7 @@ SIGNATURES = {
     "pa_version": (_c_int, []),
     "pa_set_validate": (_c_int, [_c_int]),
     "pa_device_error": (_c_int, [ctypes.POINTER(_c_int), _c_int, _c_vp]),
+    "pa_check_wait_timeout": (_c_int, [_c_vp]),
     "pa_reshape_and_cache": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_int,
                                       _c_int, _c_int, _c_int, _c_vp]),
     "pa_copy_blocks": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_int, _c_int, _c_int,

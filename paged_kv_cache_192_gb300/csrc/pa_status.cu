@@ -2,6 +2,7 @@
 #include <cstdio>
 #include <mutex>
 
+#include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace {
@@ -14,6 +15,25 @@ std::mutex g_word_mu;
 
 // One error word per device; kernels OR PA_DEVERR_* bits into it.
 __device__ int g_pa_device_error = 0;
+
+namespace {
+
+// One warp waits, with the library's bounded pipeline wait, on an mbarrier
+// that nothing arrives on.  When the wait runs out it records
+// PA_DEVERR_TIMEOUT and returns, as a decode or prefill kernel does when a
+// copy never lands.
+__global__ void wait_timeout_kernel(int *err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        pa::mbar_init(&bar, 1);
+        pa::fence_barrier_init();
+    }
+    __syncwarp();
+    const bool ok = __all_sync(pa::kFull, pa::mbar_wait(&bar, 0));
+    if (!ok && threadIdx.x == 0) pa::record_error(err, PA_DEVERR_TIMEOUT);
+}
+
+}  // namespace
 
 namespace pa {
 
@@ -75,6 +95,15 @@ int pa_device_error(int *bits, int clear, pa_stream_t stream) {
     if (e != cudaSuccess) return pa::cuda_fail(e, "pa_device_error");
     *bits = v;
     return v ? pa::fail(PA_ERR_DEVICE, "device error bits 0x%x", v) : PA_OK;
+}
+
+int pa_check_wait_timeout(pa_stream_t stream) {
+    pa::clear_error();
+    int *word = pa::device_error_word();
+    if (!word) return pa::fail(PA_ERR_CUDA, "pa_check_wait_timeout: no device error word");
+    (void)cudaGetLastError();
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(word);
+    return pa::check_launch("wait-timeout check launch");
 }
 
 }  // extern "C"

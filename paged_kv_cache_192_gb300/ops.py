@@ -53,6 +53,12 @@ def device_error(clear: bool = True, stream=None) -> int:
     return bits.value
 
 
+def check_wait_timeout(stream=None):
+    """Launch the bounded-wait diagnostic (about 2 s on the GPU); its
+    outcome is read with device_error()."""
+    check(lib().pa_check_wait_timeout(_stream(stream)))
+
+
 def reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None):
     """Store new K/V rows [T][Hkv][d] into their slots of the [NB][Hkv][bs][d] pools."""
     NB, Hkv, bs, d = k_cache.shape

@@ -219,7 +219,7 @@ class Plan:
         self.decode_bytes = 0
         self.prefill_flops = 0
         self.launches = 0
-        self.oracle_sample = None  # callable(n_seq, seed) -> (seconds, bytes, n) on the host
+        self.oracle_sample = None  # callable(n_seq, seed, threads) -> (seconds, bytes, n)
 
     def run(self, i, L, sp, ev=None, src=None):
         raise NotImplementedError
@@ -280,7 +280,7 @@ class DecodePlan(Plan):
         self.extra = {"kv_utilization_paged": round(paged, 4),
                       f"kv_utilization_contiguous_reserve_{hi}": round(contig, 4),
                       "block_table_bytes": int(sum(-(-int(L) // w.bs) for L in w.lens)) * 4}
-        self.oracle_sample = lambda n, seed: time_oracle_decode(w, n, seed)
+        self.oracle_sample = lambda n, seed, threads=None: time_oracle_decode(w, n, seed, threads)
 
     def run(self, i, L, sp, ev=None, src=None):
         from paged_kv_cache_192_gb300._lib import PA_BF16, check
@@ -388,7 +388,7 @@ class PrefixPlan(Plan):
                        "suffix_len": "U[1,512]", "Hq": Hq, "Hkv": Hkv, "head_dim": d,
                        "block_size": bs, "pool_blocks": NB, "partition_tokens": self.PT,
                        "cow_pairs": self.npairs}
-        self.oracle_sample = lambda n, seed: time_oracle_decode(w, n, seed)
+        self.oracle_sample = lambda n, seed, threads=None: time_oracle_decode(w, n, seed, threads)
 
     def run(self, i, L, sp, ev=None, src=None):
         from paged_kv_cache_192_gb300._lib import PA_BF16, check
@@ -479,7 +479,7 @@ class MixedPlan(Plan):
                        "chunk": n, "priors": [int(x) for x in priors], "Hq": dec.Hq,
                        "Hkv": dec.Hkv, "head_dim": dec.d, "block_size": dec.bs,
                        "pool_blocks": dec.num_blocks, "partition_tokens": self.PT}
-        self.oracle_sample = lambda k, seed: time_oracle_decode(dec, k, seed)
+        self.oracle_sample = lambda k, seed, threads=None: time_oracle_decode(dec, k, seed, threads)
 
     def run(self, i, L, sp, ev=None, src=None):
         from paged_kv_cache_192_gb300._lib import PA_BF16, check
@@ -683,10 +683,19 @@ def cpu_baseline(plan, args, budget_s=10.0):
         total += dt
         nb += nbytes
         reps += 1
+    # the same oracle on one thread, on a smaller sample (about 1 s)
+    dt1, nb1, k1, r1 = 0.0, 0, 0, 0
+    while r1 == 0 or dt1 < 1.0:
+        dt, nbytes, k1 = plan.oracle_sample(2, args.seed + r1, 1)
+        dt1 += dt
+        nb1 += nbytes
+        r1 += 1
     return {"value": round(nb / total / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
             "sample": f"{reps} x {k} seeded sequences of the workload's decode, fp64 C oracle on "
-                      f"{threads} threads, {total:.1f} s"}
+                      f"{threads} threads, {total:.1f} s",
+            "one_thread": {"value": round(nb1 / dt1 / 1e9, 4), "unit": "GB/s",
+                           "sample": f"{r1} x {k1} seeded sequences, 1 thread, {dt1:.1f} s"}}
 
 
 def run_reference(args, world, rank):

@@ -81,3 +81,53 @@ def test_sequence_swap_roundtrip_decodes_identically():
     torch.cuda.synchronize()
     assert ops().device_error() == 0
     assert torch.equal(before, after)
+
+
+def test_swap_states_through_block_managers():
+    """Swap-out / swap-in bookkeeping on both sides: while a sequence is out,
+    the host manager holds its blocks and the device manager has released
+    them (here another sequence takes and overwrites them); on swap-in the
+    device manager hands out blocks again and the sequence decodes to the
+    same bits, through the block table the manager builds."""
+    from paged_kv_cache_192_gb300.block_manager import BlockManager
+    lens = [300, 77, 1024]
+    NB, MB = 200, 64
+    w = synth.decode_workload("8b", seed=41, lens=lens, num_blocks=NB, max_blocks=MB)
+    dev_bm = BlockManager(NB, w.bs, seed=5)
+    for i, L in enumerate(lens):
+        dev_bm.add_seq(i, L)
+    w.table = dev_bm.block_table(np.arange(3), MB)
+    k_cache, v_cache, table, lens_d = device_inputs(w, DEV)
+    before = ops().decode(w.q.to(DEV), k_cache, v_cache, table, lens_d)
+    torch.cuda.synchronize()
+
+    host_bm = BlockManager(80, w.bs, seed=0)
+    kh = torch.zeros(80, w.Hkv, w.bs, w.d, dtype=w.dtype).pin_memory()
+    vh = torch.zeros_like(kh).pin_memory()
+    free0 = dev_bm.num_free()
+    # swap out sequence 2 (1024 tokens = 64 blocks)
+    dev_blocks = dev_bm.seq_blocks(2)
+    host_bm.add_seq(2, lens[2])
+    host_blocks = host_bm.seq_blocks(2)
+    ops().swap_blocks(kh, vh, k_cache, v_cache,
+                      torch.tensor(np.stack([dev_blocks, host_blocks], 1), device=DEV))
+    dev_bm.free_seq(2)
+    assert dev_bm.num_free() == free0 + len(dev_blocks)
+    # meanwhile another sequence takes device blocks and overwrites them
+    dev_bm.add_seq(9, 700)
+    taken = torch.tensor(dev_bm.seq_blocks(9), device=DEV)
+    k_cache[taken] = float("nan")
+    v_cache[taken] = float("nan")
+    dev_bm.free_seq(9)
+    # swap in: fresh device blocks from the manager, host blocks released
+    dev_bm.add_seq(2, lens[2])
+    new_blocks = dev_bm.seq_blocks(2)
+    ops().swap_blocks(k_cache, v_cache, kh, vh,
+                      torch.tensor(np.stack([host_blocks, new_blocks], 1), device=DEV))
+    host_bm.free_seq(2)
+    assert host_bm.num_free() == 80 and dev_bm.num_free() == free0
+    table2 = torch.from_numpy(dev_bm.block_table(np.arange(3), MB)).to(DEV)
+    after = ops().decode(w.q.to(DEV), k_cache, v_cache, table2, lens_d)
+    torch.cuda.synchronize()
+    assert ops().device_error() == 0
+    assert torch.equal(before, after)

@@ -106,6 +106,17 @@ def test_long_sequence_many_segments(lens, Hq, Hkv):
     compare(got, ref, torch.bfloat16, f"long {lens}")
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (16, 2)])
+def test_large_batch_grid_kernel(Hq, Hkv):
+    """More than 1024 sequences: the grid kernel (one CTA per sequence, KV
+    head and 64-token partition) and its separate log-sum-exp merge kernel."""
+    rng = np.random.default_rng(13)
+    lens = [int(x) for x in rng.integers(1, 301, size=1100)]
+    w = synth.decode_workload("8b", seed=13, lens=lens, Hq=Hq, Hkv=Hkv)
+    got, ref, _ = run(w, partition_tokens=64)
+    compare(got, ref, torch.bfloat16, f"B=1100 {Hq}/{Hkv}")
+
+
 def test_single_token_returns_v0_exactly():
     w = synth.decode_workload("8b", seed=7, lens=[1, 1, 1])
     _, _, out = run(w)

@@ -9,17 +9,21 @@
 // table").  Prefill is the compute-bound phase (same page), so QK^T and PV run
 // as dense bf16 tiles on the tensor cores with fp32 accumulation.
 //
-// Layout of the work: one CTA of 4 warps per (request, KV head, 64-row query
-// tile); a row is one (query token, query head) pair, so the GQ heads that
-// share a KV head share every K/V tile (GQA packed into M).  K/V tiles of 64
-// tokens are gathered block by block into swizzled shared memory with
-// cp.async (double-buffered); online softmax in the log2 domain.
+// A row is one (query token, query head) pair, so the GQ heads that share a
+// KV head share every K/V tile (GQA packed into the M dimension); K/V tiles
+// of 64 tokens; online softmax in the log2 domain with a lazy rescale.
+// Three kernels:
+//   prefill_tc2_kernel  (default) warp-specialised tcgen05: TMA loader warp,
+//                       MMA warp, two softmax warp groups over 2 x 128 rows;
+//   prefill_tc_kernel   (block sizes outside 8..64, block tables longer than
+//                       1024 entries) 128 threads per 128 rows, tcgen05,
+//                       cp.async K/V;
+//   prefill_kernel      (compile-time alternative, PA_PREFILL_TCGEN05=0)
+//                       warp-level mma.sync, kept for comparison.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
-#include <cmath>
 #include <atomic>
-#include <mutex>
+#include <cmath>
 #include <vector>
 
 #include "pa_device.cuh"

@@ -11,8 +11,8 @@
 // "Blueprint Arsitektur 3", the decode phase is memory-bandwidth intensive):
 //  * Work unit: one tile of TT tokens of one (sequence, KV head) item.  All
 //    GQ query heads of a KV head share one K/V load.
-//  * Default kernel (decode_persistent_kernel): a persistent grid of ~3 CTAs
-//    per SM; every warp owns an equal, contiguous range of units across all
+//  * Default kernel (decode_persistent_kernel): a persistent grid of 2 CTAs
+//    of 4 warps per SM; every warp owns an equal, contiguous range of units across all
 //    items (perfect balance) and streams its tiles through its own ring of NST
 //    shared-memory stages.  One lane issues a bulk copy (cp.async.bulk,
 //    non-tensor TMA) per contiguous (block, KV head) piece of K and of V,

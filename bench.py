@@ -227,7 +227,7 @@ class Plan:
         self.launches = 0
         self.oracle_sample = None  # callable(n_seq, seed, threads) -> (seconds, bytes, n)
 
-    def run(self, i, L, sp, ev=None, src=None):
+    def run(self, i, L, sp, ev=None, src=None, dst=None):
         raise NotImplementedError
 
 
@@ -288,7 +288,7 @@ class DecodePlan(Plan):
                       "block_table_bytes": int(sum(-(-int(L) // w.bs) for L in w.lens)) * 4}
         self.oracle_sample = lambda n, seed, threads=None: time_oracle_decode(w, n, seed, threads)
 
-    def run(self, i, L, sp, ev=None, src=None):
+    def run(self, i, L, sp, ev=None, src=None, dst=None):
         from paged_kv_cache_192_gb300._lib import PA_BF16, check
         w, x = self.w, (src or self.inputs)
         kc, vc = self.pools[i % len(self.pools)]
@@ -297,7 +297,7 @@ class DecodePlan(Plan):
                                      w.Hkv, w.bs, w.d, PA_BF16, sp))
         if ev:
             ev["decode"][0].record()
-        check(L.pa_decode(self.outputs["out"].data_ptr(), x["q"].data_ptr(), kc.data_ptr(),
+        check(L.pa_decode((dst or self.outputs)["out"].data_ptr(), x["q"].data_ptr(), kc.data_ptr(),
                           vc.data_ptr(), x["table"].data_ptr(), w.max_blocks,
                           x["lens"].data_ptr(), w.B, w.Hq, w.Hkv, w.d, w.bs, w.num_blocks,
                           1.0 / math.sqrt(w.d), self.PT, self.ws.data_ptr(), self.ws_bytes,
@@ -396,7 +396,7 @@ class PrefixPlan(Plan):
                        "cow_pairs": self.npairs}
         self.oracle_sample = lambda n, seed, threads=None: time_oracle_decode(w, n, seed, threads)
 
-    def run(self, i, L, sp, ev=None, src=None):
+    def run(self, i, L, sp, ev=None, src=None, dst=None):
         from paged_kv_cache_192_gb300._lib import PA_BF16, check
         x = src or self.inputs
         kc, vc = self.pools[i % len(self.pools)]
@@ -408,7 +408,7 @@ class PrefixPlan(Plan):
                                      self.Hkv, self.bs, self.d, PA_BF16, sp))
         if ev:
             ev["decode"][0].record()
-        check(L.pa_decode(self.outputs["out"].data_ptr(), x["q"].data_ptr(), kc.data_ptr(),
+        check(L.pa_decode((dst or self.outputs)["out"].data_ptr(), x["q"].data_ptr(), kc.data_ptr(),
                           vc.data_ptr(), x["table"].data_ptr(), self.MB, x["lens"].data_ptr(),
                           self.Bd, self.Hq, self.Hkv, self.d, self.bs, self.NB,
                           1.0 / math.sqrt(self.d), self.PT, self.ws.data_ptr(), self.ws_bytes,
@@ -487,7 +487,7 @@ class MixedPlan(Plan):
                        "pool_blocks": dec.num_blocks, "partition_tokens": self.PT}
         self.oracle_sample = lambda k, seed, threads=None: time_oracle_decode(dec, k, seed, threads)
 
-    def run(self, i, L, sp, ev=None, src=None):
+    def run(self, i, L, sp, ev=None, src=None, dst=None):
         from paged_kv_cache_192_gb300._lib import PA_BF16, check
         dec, pre, x = self.dec, self.pre, (src or self.inputs)
         kc, vc = self.pools[i % len(self.pools)]
@@ -496,7 +496,7 @@ class MixedPlan(Plan):
                                      dec.Hkv, dec.bs, dec.d, PA_BF16, sp))
         if ev:
             ev["decode"][0].record()
-        check(L.pa_decode(self.outputs["out"].data_ptr(), x["q"].data_ptr(), kc.data_ptr(),
+        check(L.pa_decode((dst or self.outputs)["out"].data_ptr(), x["q"].data_ptr(), kc.data_ptr(),
                           vc.data_ptr(), x["table"].data_ptr(), dec.max_blocks,
                           x["lens"].data_ptr(), dec.B, dec.Hq, dec.Hkv, dec.d, dec.bs,
                           dec.num_blocks, 1.0 / math.sqrt(dec.d), self.PT, self.ws.data_ptr(),
@@ -504,7 +504,7 @@ class MixedPlan(Plan):
         if ev:
             ev["decode"][1].record()
             ev["prefill"][0].record()
-        check(L.pa_prefill_chunk(self.outputs["outp"].data_ptr(), x["qp"].data_ptr(),
+        check(L.pa_prefill_chunk((dst or self.outputs)["outp"].data_ptr(), x["qp"].data_ptr(),
                                  kc.data_ptr(), vc.data_ptr(), x["ptable"].data_ptr(),
                                  pre.max_blocks, x["qstart"].data_ptr(), x["plens"].data_ptr(),
                                  self.R, self.n, pre.Hq, pre.Hkv, pre.d, pre.bs, dec.num_blocks,
@@ -585,28 +585,56 @@ def run_gpu(args, world, rank, local):
                           "value": value}))
         return
 
-    # end to end: host buffers through the C ABI, copies inside the timed region
+    # end to end: host buffers through the C ABI, every step's copies inside the
+    # timed region.  Three streams pipeline the steps: the inputs of step i+1
+    # go up (h2d stream) while step i computes, and step i's result comes back
+    # (d2h stream) while step i+1 computes; device buffers alternate between
+    # two sets, ordered by events.
     h_in = {k: t.cpu().pin_memory() for k, t in plan.inputs.items()}
-    d_in = {k: torch.empty_like(t) for k, t in plan.inputs.items()}
+    d_in = [{k: torch.empty_like(t) for k, t in plan.inputs.items()} for _ in range(2)]
+    d_out = [{k: torch.empty_like(t) for k, t in plan.outputs.items()} for _ in range(2)]
     h_out = {k: torch.empty_like(t, device="cpu").pin_memory() for k, t in plan.outputs.items()}
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of a buffer set landed
+    ev_run = [torch.cuda.Event() for _ in range(2)]   # a set's step computed
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # a set's result read back
 
-    def e2e_step(i):
-        for k in d_in:
-            d_in[k].copy_(h_in[k], non_blocking=True)
-        plan.run(i, L, sp, src=d_in)
-        for k in h_out:
-            h_out[k].copy_(plan.outputs[k], non_blocking=True)
+    def upload(i):
+        b = i % 2
+        with torch.cuda.stream(up):
+            up.wait_event(ev_run[b])          # step i-2 is done with these inputs
+            for k in h_in:
+                d_in[b][k].copy_(h_in[k], non_blocking=True)
+            ev_in[b].record(up)
 
-    for i in range(args.warmup):
-        e2e_step(i)
+    def e2e_steps(n, first):
+        upload(first)
+        for i in range(first, first + n):
+            b = i % 2
+            if i + 1 < first + n:
+                upload(i + 1)
+            stream.wait_event(ev_in[b])
+            stream.wait_event(ev_out[b])      # step i-2's result has been read back
+            plan.run(i, L, sp, src=d_in[b], dst=d_out[b])
+            ev_run[b].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_run[b])
+                for k in h_out:
+                    h_out[k].copy_(d_out[b][k], non_blocking=True)
+                ev_out[b].record(down)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
+
+    e2e_steps(args.warmup, 0)
     torch.cuda.synchronize()
     barrier(world)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    for i in range(args.steps):
-        e2e_step(i)
+    up.wait_event(f0)
+    down.wait_event(f0)
+    e2e_steps(args.steps, args.warmup)
     f1.record(stream)
     torch.cuda.synchronize()
     barrier(world)

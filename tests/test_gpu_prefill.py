@@ -85,6 +85,17 @@ def test_prefill_long_block_table_fallback_kernel():
     compare(got, ref, torch.bfloat16, "prefill long table")
 
 
+@pytest.mark.parametrize("bs", [16, 128])
+def test_prefill_requests_without_new_tokens(bs):
+    """Requests with no new tokens in the batch (n_r = 0) produce no rows and
+    disturb nothing; the others match the oracle (both prefill kernels)."""
+    priors = [10, 0, 3, 200, 0]
+    n_new = [0, 5, 0, 70, 1]
+    w, q = _prefill_workload(priors, n_new, Hq=8, Hkv=2, bs=bs, seed=9)
+    got, ref = _run(w, q, priors, n_new)
+    compare(got, ref, torch.bfloat16, f"prefill zero-token requests bs{bs}")
+
+
 def test_prefill_first_query_sees_only_itself():
     w, q = _prefill_workload([0], [48], seed=2)
     got, _ = _run(w, q, [0], [48])

@@ -72,6 +72,11 @@ def build(verbose: bool = False) -> str:
             futs.append(ex.submit(_compile, src, obj, headers))
         for f in futs:
             f.result()
+    # objects of earlier sources or flags are not reused: drop them
+    keep = {os.path.basename(o) for o in objs}
+    for old in glob.glob(os.path.join(BUILD, "*.o")):
+        if os.path.basename(old) not in keep:
+            os.remove(old)
     link_key = _digest(objs, ["link"])
     stamp = os.path.join(BUILD, "lib.stamp")
     if os.path.exists(LIB) and os.path.exists(stamp) and open(stamp).read() == link_key:

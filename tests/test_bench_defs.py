@@ -1,0 +1,64 @@
+"""The measurement definitions bench.py reports against: algorithmic decode
+bytes, causal prefill flops, and the comment-insensitive source key of the
+counter records (CPU only)."""
+import importlib.util
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_decode_bytes_by_hand(bench):
+    # 2 sequences of 5 and 17 tokens, 4 query / 2 KV heads, d 64, bf16, 16-token blocks
+    kv = (5 + 17) * 2 * 2 * 64 * 2          # K and V rows, once per KV head
+    q_out = 2 * 2 * 4 * 64 * 2              # q and out of 2 sequences
+    tables = (1 + 2) * 4                    # block-table entries read
+    lens = 2 * 4                            # context lengths
+    assert bench.decode_bytes([5, 17], 2, 4, 2, 64, 16, torch.bfloat16) == kv + q_out + tables + lens
+
+
+def test_decode_bytes_of_the_8b_batch(bench):
+    from paged_kv_cache_192_gb300 import synth
+    w = synth.decode_workload("8b", seed=0)
+    assert bench.decode_bytes(w.lens, w.B, w.Hq, w.Hkv, w.d, w.bs, w.dtype) == 564_951_004
+
+
+def test_prefill_flops_brute_force(bench):
+    rng = np.random.default_rng(3)
+    Hq, d = 4, 16
+    for _ in range(5):
+        priors = [int(x) for x in rng.integers(0, 40, size=3)]
+        n_new = [int(x) for x in rng.integers(1, 20, size=3)]
+        pairs = sum(1 for P, n in zip(priors, n_new) for i in range(n) for j in range(P + i + 1))
+        # per (query, key, head): 2 d flops for q.k and 2 d for p*v
+        assert bench.prefill_flops(priors, n_new, Hq, d) == pairs * Hq * 4 * d
+
+
+def test_prefill_flops_of_the_mixed_batch(bench):
+    from paged_kv_cache_192_gb300 import synth
+    _, pre = synth.mixed_workload(seed=0)
+    flops = bench.prefill_flops(pre.extra["prior"], [pre.extra["chunk"]] * len(pre.lens), pre.Hq, pre.d)
+    assert flops == 74_675_388_416
+
+
+def test_source_key_ignores_comments_only(bench, tmp_path, monkeypatch):
+    csrc = tmp_path / "paged_kv_cache_192_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (csrc / "a.cu").write_text("int f() { return 1; }  // one\n/* block\n comment */\n")
+    k1 = bench.source_sha1("a.cu")
+    (csrc / "a.cu").write_text("int f() { return 1; }  // changed\n/* other */\n")
+    assert bench.source_sha1("a.cu") == k1
+    (csrc / "a.cu").write_text("int f() { return 2; }\n")
+    assert bench.source_sha1("a.cu") != k1

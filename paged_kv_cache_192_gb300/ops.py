@@ -133,6 +133,30 @@ def decode(q, k_cache, v_cache, block_table, context_lens, scale=None, partition
     return out
 
 
+def decode_noalloc_capacity() -> int:
+    """Bytes of the library's fixed decode scratch (pa_decode_noalloc)."""
+    return int(lib().pa_decode_noalloc_capacity())
+
+
+def decode_noalloc(q, k_cache, v_cache, block_table, context_lens, scale=None,
+                   partition_tokens=0, out=None, stream=None):
+    """pa_decode_noalloc: as decode, with the split-KV workspace taken from the
+    library's fixed device array (nothing is allocated when `out` is given);
+    calls that overlap on the GPU race on that array."""
+    B, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    assert d2 == d and block_table.shape[0] == B and context_lens.shape == (B,)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    check(lib().pa_decode_noalloc(
+        _cuda(out, "out", q.dtype), _cuda(q, "q", k_cache.dtype), _cuda(k_cache, "k_cache"),
+        _cuda(v_cache, "v_cache", k_cache.dtype), _cuda(block_table, "block_table", torch.int32),
+        block_table.shape[1], _cuda(context_lens, "context_lens", torch.int32), B, Hq, Hkv, d,
+        bs, NB, scale, partition_tokens, _dt(q), _stream(stream)))
+    return out
+
+
 def prefill_chunk(q, k_cache, v_cache, block_table, query_start, context_lens, max_query_len,
                   scale=None, out=None, stream=None):
     """Causal chunked prefill; q [sum n][Hq][d] -> out [sum n][Hq][d] (bf16)."""

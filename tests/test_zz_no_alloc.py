@@ -71,3 +71,19 @@ def test_noalloc_rejects_batches_beyond_its_scratch(lib):
                                x.data_ptr(), 1024, x.data_ptr(), 32, 64, 8, 128, 32, 1000, 0.08,
                                512, 0, None)
     assert rc == 1 and b"scratch" in lib.pa_last_error_string()
+
+
+def test_noalloc_through_the_python_binding(lib):
+    """ops.decode_noalloc (same call through the binding) matches ops.decode
+    bit for bit: both run the same kernel on the same inputs, only the
+    workspace differs."""
+    from paged_kv_cache_192_gb300 import ops
+    assert ops.decode_noalloc_capacity() == 16 << 20
+    w = synth.decode_workload("8b", seed=23, B=16)
+    k_cache, v_cache, table, lens = device_inputs(w, DEV)
+    q = w.q.to(DEV)
+    ref = ops.decode(q, k_cache, v_cache, table, lens, partition_tokens=256)
+    out = ops.decode_noalloc(q, k_cache, v_cache, table, lens, partition_tokens=256)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    assert torch.equal(out, ref)

@@ -62,3 +62,22 @@ def test_source_key_ignores_comments_only(bench, tmp_path, monkeypatch):
     assert bench.source_sha1("a.cu") == k1
     (csrc / "a.cu").write_text("int f() { return 2; }\n")
     assert bench.source_sha1("a.cu") != k1
+
+
+def test_reference_arm_prints_the_contract_line(bench, capsys):
+    """bench.py --impl reference: the fp64 oracle on the host cores, one JSON
+    line with the same metric and the keys the contract names."""
+    import json
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3", "--cpu-sample-seqs", "2"])
+    line = capsys.readouterr().out.strip().splitlines()[-1]
+    j = json.loads(line)
+    assert j["impl"] == "reference" and j["metric"] == bench.METRIC and j["unit"] == "GB/s"
+    assert j["value"] > 0 and j["higher_is_better"] is True and j["vs_baseline"] is None
+    for k in ("n_gpus", "steps", "warmup", "ms_per_step", "scaling", "dtype", "data", "config"):
+        assert k in j
+    assert j["config"]["workload"] == bench.WORKLOADS["8b"]
+    cb = j["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == j["value"] and cb["sample"]
+    e2e = j["e2e"]
+    assert e2e["value"] == j["value"] and e2e["h2d_bytes_per_step"] == 0
+    assert e2e["d2h_bytes_per_step"] == 0

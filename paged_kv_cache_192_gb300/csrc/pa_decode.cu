@@ -516,9 +516,6 @@ __device__ __forceinline__ void prefetch_q(const DecodeParams &p, const Cursor &
     if (lane < kLines) asm volatile("prefetch.global.L1 [%0];" ::"l"(qa + lane * 128));
 }
 
-// End of this warp's segment of item c: write the output (the whole item is
-// in this warp's range) or a partial, and merge the item's partials if this
-// segment is the last of them to finish.
 // Merge of an item spread over more than 32 warps (a few very long
 // sequences): the weights are recomputed from loads instead of travelling
 // by shuffle.  Kept out of line so the common path's code is unaffected.
@@ -557,6 +554,9 @@ __device__ __noinline__ void merge_many(const DecodeParams &p, size_t hq0, int n
     }
 }
 
+// End of this warp's segment of item c: write the output (the whole item is
+// in this warp's range) or a partial, and merge the item's partials if this
+// segment is the last of them to finish.
 template <typename T, int D, int GQ>
 __device__ __forceinline__ void finish_segment(WarpAttn<T, D, GQ> &st, const DecodeParams &p,
                                                const BatchTables &bt, const Cursor &c,

@@ -132,15 +132,16 @@ def peaks():
 
 
 def source_sha1(*names):
-    """sha1 of the kernel sources with comments removed: a counter record
-    stays valid across comment edits and no longer across code edits."""
+    """sha1 of the kernel sources with comments removed and whitespace
+    collapsed: a counter record stays valid across comment and layout edits
+    and no longer across code edits."""
     h = hashlib.sha1()
     for name in names:
         with open(os.path.join(ROOT, "paged_kv_cache_192_gb300", "csrc", name)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
-        h.update(text.encode())
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 

@@ -75,11 +75,27 @@ def test_shapes_ragged(dtype, d, Hq, Hkv, bs):
     compare(got, ref, dtype, f"ragged d{d} {Hq}/{Hkv} bs{bs}")
 
 
-def test_placement_invariance_bit_identical():
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4), (8, 2), (16, 2)])
+@pytest.mark.parametrize("bs", [8, 16, 32, 64])
+def test_shapes_ragged_persistent(dtype, d, Hq, Hkv, bs):
+    """The ragged lengths of test_shapes_ragged in a batch of 45 sequences,
+    enough (sequence, KV head) items for the persistent kernel (the 15-sequence
+    batch above runs on the grid kernel)."""
+    lens = [1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 300] * 3
+    w = synth.decode_workload("8b", seed=4, lens=lens, Hq=Hq, Hkv=Hkv, d=d, bs=bs, dtype=dtype)
+    got, ref, _ = run(w, partition_tokens=max(64, bs))
+    compare(got, ref, dtype, f"ragged x3 d{d} {Hq}/{Hkv} bs{bs}")
+
+
+@pytest.mark.parametrize("B", [4, 16])
+def test_placement_invariance_bit_identical(B):
     """Two different physical placements of the same logical K/V give
-    bit-identical outputs (the reduction order follows logical positions)."""
-    w1 = synth.decode_workload("8b", seed=5, B=16)
-    w2 = synth.decode_workload("8b", seed=5, B=16)
+    bit-identical outputs (the reduction order follows logical positions);
+    4 sequences run on the grid kernel, 16 on the persistent one."""
+    w1 = synth.decode_workload("8b", seed=5, B=B)
+    w2 = synth.decode_workload("8b", seed=5, B=B)
     rng = np.random.default_rng(99)
     perm = rng.permutation(w2.num_blocks).astype(np.int32)
     w2.table = perm[w1.table]
@@ -96,11 +112,14 @@ def test_split_matches_unsplit():
     compare(o_whole.double().cpu().numpy(), ref, torch.bfloat16, "whole")
 
 
-@pytest.mark.parametrize("lens,Hq,Hkv", [([32768], 32, 8), ([20000, 3], 8, 1)])
+@pytest.mark.parametrize("lens,Hq,Hkv", [([32768], 32, 8), ([20000, 3], 8, 1),
+                                          ([32768] * 9, 32, 8), ([20000] + [3] * 64, 8, 1)])
 def test_long_sequence_many_segments(lens, Hq, Hkv):
-    """Few long sequences: each (sequence, KV head) item is spread over more
-    than 32 warps of the persistent grid (one 32k-token sequence: 64
-    segments per item), all merged by log-sum-exp."""
+    """Long sequences split into 40-64 partitions of 512 tokens, merged by
+    log-sum-exp: one or two sequences on the grid kernel (merge kernel over
+    the partitions), and batches of more than 64 (sequence, KV head) items on
+    the persistent kernel, where a long item spreads over more than 32
+    segments (the out-of-line merge)."""
     w = synth.decode_workload("8b", seed=11, lens=lens, Hq=Hq, Hkv=Hkv)
     got, ref, _ = run(w, partition_tokens=512)
     compare(got, ref, torch.bfloat16, f"long {lens}")
@@ -146,11 +165,13 @@ def test_dominant_key_selects_its_value():
     compare(got, ref, torch.bfloat16, "dominant")
 
 
-def test_bad_block_id_is_recorded_not_faulted():
+@pytest.mark.parametrize("nseq", [1, 9])
+def test_bad_block_id_is_recorded_not_faulted(nseq):
     """An out-of-pool table entry is replaced by block 0 in the kernel and
-    reported in the device error word (no out-of-bounds access)."""
+    reported in the device error word (no out-of-bounds access); one sequence
+    runs on the grid kernel, nine (72 items) on the persistent one."""
     from paged_kv_cache_192_gb300._lib import PA_DEVERR_BAD_BLOCK
-    w = synth.decode_workload("8b", seed=10, lens=[40])
+    w = synth.decode_workload("8b", seed=10, lens=[40] * nseq)
     k_cache, v_cache, table, lens = device_inputs(w, DEV)
     table[0, 1] = w.num_blocks + 5
     ops().device_error(clear=True)

@@ -228,10 +228,20 @@ class Plan:
         self.roofline_basis = "algorithmic bytes"
         self.prefill_flops = 0
         self.launches = 0
+        self.decode_kernel = None
         self.oracle_sample = None  # callable(n_seq, seed, threads) -> (seconds, bytes, n)
 
     def run(self, i, L, sp, ev=None, src=None, dst=None):
         raise NotImplementedError
+
+
+def decode_kernel_info(B, Hkv, MB, bs, PT):
+    """(name of the decode kernel for the roofline line, launches of one
+    pa_decode) for a batch of these sizes."""
+    from paged_kv_cache_192_gb300 import ops
+    if ops.decode_kernel_for(B, Hkv, MB, bs, PT) == "persistent":
+        return "pa_decode (decode_persistent_kernel, split-KV merge inside)", 1
+    return "pa_decode (decode_kernel, then merge_kernel)", 2
 
 
 def _slots_last(table, lens, bs):
@@ -275,11 +285,12 @@ class DecodePlan(Plan):
         self.outputs = {"out": torch.empty_like(self.inputs["q"])}
         self.PT = args.partition
         self.ws_bytes = ops.decode_workspace_size(w.B, w.Hq, w.d, w.max_blocks, w.bs, self.PT)
+        self.decode_kernel, n_dec = decode_kernel_info(w.B, w.Hkv, w.max_blocks, w.bs, self.PT)
         self.ws = torch.zeros(max(self.ws_bytes // 4, 1), dtype=torch.float32, device=dev)
         self.decode_bytes = decode_bytes(w.lens, w.B, w.Hq, w.Hkv, w.d, w.bs, w.dtype)
         self.step_bytes = self.decode_bytes + store_bytes(w.B, w.Hkv, w.d, w.dtype)
         self.tokens = w.B
-        self.launches = 2
+        self.launches = 1 + n_dec
         lo, hi = synth.CONFIGS[name]["len_range"]
         self.config = {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d, "block_size": w.bs,
                        "context_len": f"U[{lo},{hi}] seed {args.seed}",
@@ -380,6 +391,7 @@ class PrefixPlan(Plan):
         self.outputs = {"out": torch.empty_like(self.inputs["q"])}
         self.PT = args.partition
         self.ws_bytes = ops.decode_workspace_size(self.Bd, Hq, d, MB, bs, self.PT)
+        self.decode_kernel, n_dec = decode_kernel_info(self.Bd, Hkv, MB, bs, self.PT)
         self.ws = torch.zeros(max(self.ws_bytes // 4, 1), dtype=torch.float32, device=dev)
         es = _es(w.dtype)
         self.decode_bytes = decode_bytes(lens, self.Bd, Hq, Hkv, d, bs, w.dtype)
@@ -395,7 +407,7 @@ class PrefixPlan(Plan):
         self.step_bytes = (self.decode_bytes + store_bytes(self.Bd, Hkv, d, w.dtype) +
                            self.npairs * 2 * 2 * Hkv * bs * d * es)
         self.tokens = self.Bd
-        self.launches = 3 if self.npairs else 2
+        self.launches = (2 if self.npairs else 1) + n_dec
         self.extra = {"unique_kv_bytes": unique, "logical_kv_bytes": self.decode_bytes,
                       "cow_pairs": self.npairs}
         self.config = {"B": self.Bd, "sequences": f"{B} sharing a {P}-token prompt + {nf} forks",
@@ -477,6 +489,8 @@ class MixedPlan(Plan):
         self.PT = args.partition
         self.ws_bytes = ops.decode_workspace_size(dec.B, dec.Hq, dec.d, dec.max_blocks, dec.bs,
                                                   self.PT)
+        self.decode_kernel, n_dec = decode_kernel_info(dec.B, dec.Hkv, dec.max_blocks, dec.bs,
+                                                       self.PT)
         self.ws = torch.zeros(max(self.ws_bytes // 4, 1), dtype=torch.float32, device=dev)
         self.decode_bytes = decode_bytes(dec.lens, dec.B, dec.Hq, dec.Hkv, dec.d, dec.bs,
                                          dec.dtype)
@@ -487,7 +501,7 @@ class MixedPlan(Plan):
                            store_bytes(self.T, dec.Hkv, dec.d, dec.dtype))
         self.prefill_flops = prefill_flops(priors, [n] * R, pre.Hq, pre.d)
         self.tokens = dec.B + R * n
-        self.launches = 3
+        self.launches = 2 + n_dec
         self.extra = {"prefill_flops": self.prefill_flops, "priors": [int(x) for x in priors]}
         self.config = {"B_decode": dec.B, "decode_len": "U[256,8192]", "prefill_requests": R,
                        "chunk": n, "priors": [int(x) for x in priors], "Hq": dec.Hq,
@@ -668,7 +682,7 @@ def run_gpu(args, world, rank, local):
                      "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "traffic": kernel_traffic(f"decode_traffic_{args.workload}.json",
                                                "pa_decode.cu", "pa_device.cuh"),
-                     "kernel": "pa_decode (decode_persistent_kernel, split-KV merge inside)",
+                     "kernel": plan.decode_kernel,
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "avg_launch_us": round(dec_ms * 1e3, 2),
                      "algorithmic_bytes": rbytes, "bytes_basis": plan.roofline_basis},

@@ -140,6 +140,29 @@ int pa_swap_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_
 int pa_decode_workspace_size(int B, int Hq, int head_dim, int max_blocks_per_seq,
                              int block_size, int partition_tokens, size_t *bytes);
 
+/* kernels pa_decode can launch (pa_decode_kernel_for) */
+enum { PA_DECODE_PERSISTENT = 1, PA_DECODE_GRID = 2 };
+
+/*
+ * pa_decode_kernel_for -- which kernel pa_decode launches for a batch of these
+ * sizes on the current device.  The choice depends on the sizes only (never
+ * on context lengths or device data), so one batch shape always runs the
+ * same kernel:
+ *   PA_DECODE_PERSISTENT  one persistent grid (2 CTAs of 4 warps per SM) that
+ *                         splits the batch's (sequence, KV head, 16-token
+ *                         tile) units evenly over its warps;
+ *   PA_DECODE_GRID        one CTA per (sequence, KV head, partition), then a
+ *                         merge kernel; chosen when B * Hkv * (partitions of
+ *                         the table capacity) is at most twice the persistent
+ *                         grid's warp count (little work), and for B > 1024.
+ * Both meet the same error bound; their results may differ in the last bits
+ * (another order of the partial sums).  Arguments as for pa_decode;
+ * *kernel receives PA_DECODE_PERSISTENT or PA_DECODE_GRID.  PA_ERR_INVALID
+ * on bad sizes, PA_ERR_CUDA without a current device.
+ */
+int pa_decode_kernel_for(int B, int Hkv, int max_blocks_per_seq, int block_size,
+                         int partition_tokens, int *kernel);
+
 /*
  * pa_decode -- paged decode attention: one query token per sequence.
  * For sequence b with context length L = context_lens[b] (the newest token,

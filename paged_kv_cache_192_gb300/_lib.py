@@ -13,6 +13,7 @@ LIB_PATH = os.path.join(_HERE, "libpa_gb300.so")
 PA_OK, PA_ERR_INVALID, PA_ERR_OOM, PA_ERR_CUDA, PA_ERR_UNSUPPORTED, PA_ERR_DEVICE = range(6)
 PA_BF16, PA_F32 = 0, 1
 PA_DEVERR_BAD_BLOCK, PA_DEVERR_TIMEOUT = 1, 2
+PA_DECODE_PERSISTENT, PA_DECODE_GRID = 1, 2
 
 _c_int, _c_i64, _c_sz, _c_vp, _c_f = (ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
                                       ctypes.c_void_p, ctypes.c_float)
@@ -34,6 +35,8 @@ SIGNATURES = {
                                 _c_int, _c_int, _c_int, _c_int, _c_vp]),
     "pa_decode_workspace_size": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                           ctypes.POINTER(_c_sz)]),
+    "pa_decode_kernel_for": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int,
+                                      ctypes.POINTER(_c_int)]),
     "pa_decode": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_int,
                            _c_int, _c_int, _c_int, _c_i64, _c_f, _c_int, _c_vp, _c_sz, _c_int,
                            _c_vp]),

@@ -1109,22 +1109,33 @@ int launch_grid(const DecodeParams &p, cudaStream_t stream) {
     return PA_OK;
 }
 
-// The persistent kernel needs the batch's tile counts in shared memory and
-// 32-bit tile prefix sums.  Batches of few (sequence, KV head) items go to
-// the grid kernel instead: there every partition gets its own CTA, while the
-// persistent split would keep most warps idle and leave each item's many
-// segments to one merging warp (one 3.5k-token sequence, 8 KV heads:
-// 21-23 us against 53 us; from 16 sequences the persistent kernel is ahead).
-constexpr int kGridMaxItems = 64;
-bool use_persistent(const DecodeParams &p) {
-    return p.B <= kPersistentMaxB && p.B * p.Hkv > kGridMaxItems &&
-           int64_t(p.B) * (int64_t(p.MB) << p.bs_log2) / 8 < (1ll << 31);
+// Which kernel a batch runs on; sizes only, so the host decides without
+// reading device data.  The persistent kernel needs the batch's tile counts in
+// shared memory and 32-bit tile prefix sums.  A batch with little work runs on
+// the grid kernel: there every (sequence, KV head, partition) gets a CTA of
+// four warps, while the persistent split leaves a partition to one warp (its
+// tiles streamed one after another) and an item's segments to one merging
+// warp.  Measured with 512-token partitions, 32 query / 8 KV heads, d 128:
+// 16-token blocks and 4096-token tables, the grid kernel is ahead up to 32
+// sequences (26.6 against 53.2 us at 8, 67.7 against 69.6 at 32) and behind
+// from 48 (88.1 against 77.8); 64 query heads, 32k-token tables, up to 4
+// sequences (63.5 against 155.7 us at 1) and even at 8 (233 against 231).
+// Rule: the grid kernel while its CTA count, bounded by the table capacity,
+// is at most twice the persistent grid's warps.
+int kernel_for(int B, int Hkv, int MB, int bs_log2, int partitions, int sms) {
+    if (B > kPersistentMaxB || int64_t(B) * (int64_t(MB) << bs_log2) / 8 >= (1ll << 31))
+        return PA_DECODE_GRID;
+    const int64_t grid_ctas = int64_t(B) * Hkv * partitions;
+    return grid_ctas <= 2ll * sms * kMinCtas * kWarps ? PA_DECODE_GRID : PA_DECODE_PERSISTENT;
 }
 
 template <typename T, int D, int GQ>
 int launch(const DecodeParams &p, cudaStream_t stream) {
-    return use_persistent(p) ? launch_persistent<T, D, GQ>(p, stream)
-                             : launch_grid<T, D, GQ>(p, stream);
+    const int sms = sm_count();
+    if (sms <= 0) return pa::fail(PA_ERR_CUDA, "decode: no SM count");
+    return kernel_for(p.B, p.Hkv, p.MB, p.bs_log2, p.max_parts - 1, sms) == PA_DECODE_PERSISTENT
+               ? launch_persistent<T, D, GQ>(p, stream)
+               : launch_grid<T, D, GQ>(p, stream);
 }
 
 template <typename T, int D>
@@ -1165,6 +1176,23 @@ int pa_decode_workspace_size(int B, int Hq, int head_dim, int max_blocks_per_seq
     const int64_t cap = int64_t(max_blocks_per_seq) * block_size;
     const int maxseg = static_cast<int>((cap + pt - 1) / pt) + 1;
     *bytes = workspace_bytes_for(B, Hq, head_dim, maxseg);
+    return PA_OK;
+}
+
+int pa_decode_kernel_for(int B, int Hkv, int max_blocks_per_seq, int block_size,
+                         int partition_tokens, int *kernel) {
+    pa::clear_error();
+    if (!kernel) return pa::fail(PA_ERR_INVALID, "decode_kernel_for: kernel is NULL");
+    if (B < 0 || Hkv <= 0 || max_blocks_per_seq <= 0 || !pa::pow2_in(block_size, 8, 128))
+        return pa::fail(PA_ERR_INVALID, "decode_kernel_for: bad sizes");
+    const int pt = resolve_partition(partition_tokens);
+    if (!partition_ok(pt, block_size))
+        return pa::fail(PA_ERR_INVALID, "decode_kernel_for: bad partition_tokens %d", pt);
+    const int sms = sm_count();
+    if (sms <= 0) return pa::fail(PA_ERR_CUDA, "decode_kernel_for: no SM count");
+    const int64_t cap = int64_t(max_blocks_per_seq) * block_size;
+    *kernel = kernel_for(B, Hkv, max_blocks_per_seq, log2_int(block_size),
+                         static_cast<int>((cap + pt - 1) / pt), sms);
     return PA_OK;
 }
 

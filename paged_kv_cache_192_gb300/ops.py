@@ -110,6 +110,15 @@ def decode_workspace_size(B, Hq, head_dim, max_blocks_per_seq, block_size, parti
     return out.value
 
 
+def decode_kernel_for(B, Hkv, max_blocks_per_seq, block_size, partition_tokens=0) -> str:
+    """Kernel pa_decode runs for these sizes on the current device:
+    "persistent" or "grid"."""
+    out = ctypes.c_int(0)
+    check(lib().pa_decode_kernel_for(B, Hkv, max_blocks_per_seq, block_size, partition_tokens,
+                                     ctypes.byref(out)))
+    return {_lib.PA_DECODE_PERSISTENT: "persistent", _lib.PA_DECODE_GRID: "grid"}[out.value]
+
+
 def decode(q, k_cache, v_cache, block_table, context_lens, scale=None, partition_tokens=0,
            workspace=None, out=None, stream=None):
     """Paged decode attention; q [B][Hq][d] -> out [B][Hq][d]."""

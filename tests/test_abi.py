@@ -73,6 +73,20 @@ def test_decode_rejects_bad_arguments(lib, kw, code):
     assert lib.pa_last_error_string()
 
 
+@pytest.mark.parametrize("args", [
+    (-1, 8, 256, 16, 0),    # negative batch
+    (4, 0, 256, 16, 0),     # no KV heads
+    (4, 8, 0, 16, 0),       # empty table
+    (4, 8, 256, 24, 0),     # block size not a power of two
+    (4, 8, 256, 16, 48),    # partition not a multiple of 32
+])
+def test_decode_kernel_for_rejects_bad_sizes(lib, args):
+    k = ctypes.c_int(0)
+    assert lib.pa_decode_kernel_for(*args, ctypes.byref(k)) == 1
+    assert lib.pa_last_error_string()
+    assert lib.pa_decode_kernel_for(4, 8, 256, 16, 0, None) == 1
+
+
 def test_null_pointers_rejected(lib):
     rc = lib.pa_decode(None, None, None, None, None, 4, None, 2, 4, 4, 64, 16, 8, 0.125, 0, None,
                        0, 1, None)

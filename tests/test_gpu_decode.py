@@ -23,7 +23,15 @@ def ops():
     return o
 
 
-def run(w, partition_tokens=0, seqs=None, poison=True):
+def kernel_of(w, partition_tokens=0):
+    return ops().decode_kernel_for(len(w.lens), w.Hkv, w.table.shape[1], w.bs, partition_tokens)
+
+
+def run(w, partition_tokens=0, seqs=None, poison=True, kernel=None):
+    """Decode the batch on the GPU and the oracle; `kernel` ("persistent" or
+    "grid") asserts which decode kernel the batch runs on."""
+    if kernel is not None:
+        assert kernel_of(w, partition_tokens) == kernel
     k_cache, v_cache, table, lens = device_inputs(w, DEV, poison)
     out = ops().decode(w.q.to(DEV), k_cache, v_cache, table, lens,
                        partition_tokens=partition_tokens)
@@ -40,7 +48,7 @@ def test_tiny_fp32_config():
     """4 sequences {5,17,33,64}, MHA 4 heads, d 64, 16-token blocks, 32-block pool, fp32."""
     w = synth.decode_workload("tiny", seed=0)
     assert w.num_blocks == 32 and list(w.lens) == [5, 17, 33, 64]
-    got, ref, _ = run(w)
+    got, ref, _ = run(w, kernel="grid")
     compare(got, ref, torch.float32, "tiny")
 
 
@@ -48,7 +56,7 @@ def test_8b_config_full_size():
     """Llama-3-8B-shaped: 64 sequences, L ~ U[128,4096], 32/8 heads, d 128, bf16,
     shuffled 1.2x pool; every output element against the oracle."""
     w = synth.decode_workload("8b", seed=0)
-    got, ref, _ = run(w)
+    got, ref, _ = run(w, kernel="persistent")
     compare(got, ref, torch.bfloat16, "8b")
 
 
@@ -58,7 +66,7 @@ def test_70b_config_full_size_sampled():
     checks 3 seeded sequences element by element."""
     w = synth.decode_workload("70b", seed=0)
     seqs = synth.sample_indices(w.B, 3, seed=0)
-    got, ref, _ = run(w, partition_tokens=512, seqs=seqs)
+    got, ref, _ = run(w, partition_tokens=512, seqs=seqs, kernel="persistent")
     compare(got, ref, torch.bfloat16, "70b")
 
 
@@ -70,8 +78,9 @@ def test_shapes_ragged(dtype, d, Hq, Hkv, bs):
     """Ragged lengths around tile, block and partition edges; 64-token
     partitions so that long sequences split and merge."""
     lens = [1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 300]
-    w = synth.decode_workload("8b", seed=3, lens=lens, Hq=Hq, Hkv=Hkv, d=d, bs=bs, dtype=dtype)
-    got, ref, _ = run(w, partition_tokens=max(64, bs))
+    w = synth.decode_workload("8b", seed=3, lens=lens, Hq=Hq, Hkv=Hkv, d=d, bs=bs, dtype=dtype,
+                              max_blocks=-(-300 // bs) + 1)
+    got, ref, _ = run(w, partition_tokens=max(64, bs), kernel="grid")
     compare(got, ref, dtype, f"ragged d{d} {Hq}/{Hkv} bs{bs}")
 
 
@@ -80,48 +89,51 @@ def test_shapes_ragged(dtype, d, Hq, Hkv, bs):
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4), (8, 2), (16, 2)])
 @pytest.mark.parametrize("bs", [8, 16, 32, 64])
 def test_shapes_ragged_persistent(dtype, d, Hq, Hkv, bs):
-    """The ragged lengths of test_shapes_ragged in a batch of 45 sequences,
-    enough (sequence, KV head) items for the persistent kernel (the 15-sequence
-    batch above runs on the grid kernel)."""
+    """The ragged lengths of test_shapes_ragged, 45 sequences with 4096-token
+    tables: enough work for the persistent kernel (the 15 sequences with short
+    tables above run on the grid kernel)."""
     lens = [1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 300] * 3
     w = synth.decode_workload("8b", seed=4, lens=lens, Hq=Hq, Hkv=Hkv, d=d, bs=bs, dtype=dtype)
-    got, ref, _ = run(w, partition_tokens=max(64, bs))
+    got, ref, _ = run(w, partition_tokens=max(64, bs), kernel="persistent")
     compare(got, ref, dtype, f"ragged x3 d{d} {Hq}/{Hkv} bs{bs}")
 
 
-@pytest.mark.parametrize("B", [4, 16])
-def test_placement_invariance_bit_identical(B):
+@pytest.mark.parametrize("B,kernel", [(4, "grid"), (64, "persistent")])
+def test_placement_invariance_bit_identical(B, kernel):
     """Two different physical placements of the same logical K/V give
-    bit-identical outputs (the reduction order follows logical positions);
-    4 sequences run on the grid kernel, 16 on the persistent one."""
+    bit-identical outputs (the reduction order follows logical positions)
+    on both decode kernels."""
     w1 = synth.decode_workload("8b", seed=5, B=B)
     w2 = synth.decode_workload("8b", seed=5, B=B)
     rng = np.random.default_rng(99)
     perm = rng.permutation(w2.num_blocks).astype(np.int32)
     w2.table = perm[w1.table]
-    _, _, o1 = run(w1, seqs=[0])
+    _, _, o1 = run(w1, seqs=[0], kernel=kernel)
     _, _, o2 = run(w2, seqs=[0])
     assert torch.equal(o1, o2)
 
 
-def test_split_matches_unsplit():
-    w = synth.decode_workload("8b", seed=6, B=8)
+@pytest.mark.parametrize("B", [8, 64])
+def test_split_matches_unsplit(B):
+    """128- and 4096-token partitions both match the oracle (at 64 sequences
+    the first runs on the persistent kernel, the second on the grid one)."""
+    w = synth.decode_workload("8b", seed=6, B=B)
     _, ref, o_split = run(w, partition_tokens=128)
     _, _, o_whole = run(w, partition_tokens=4096)
     compare(o_split.double().cpu().numpy(), ref, torch.bfloat16, "split")
     compare(o_whole.double().cpu().numpy(), ref, torch.bfloat16, "whole")
 
 
-@pytest.mark.parametrize("lens,Hq,Hkv", [([32768], 32, 8), ([20000, 3], 8, 1),
-                                          ([32768] * 9, 32, 8), ([20000] + [3] * 64, 8, 1)])
-def test_long_sequence_many_segments(lens, Hq, Hkv):
+@pytest.mark.parametrize("lens,Hq,Hkv,kernel", [
+    ([32768], 32, 8, "grid"), ([20000, 3], 8, 1, "grid"),
+    ([32768] * 9, 32, 8, "persistent"), ([20000] + [3] * 80, 8, 1, "persistent")])
+def test_long_sequence_many_segments(lens, Hq, Hkv, kernel):
     """Long sequences split into 40-64 partitions of 512 tokens, merged by
     log-sum-exp: one or two sequences on the grid kernel (merge kernel over
-    the partitions), and batches of more than 64 (sequence, KV head) items on
-    the persistent kernel, where a long item spreads over more than 32
-    segments (the out-of-line merge)."""
+    the partitions), and larger batches on the persistent kernel, where a
+    long item spreads over more than 32 segments (the out-of-line merge)."""
     w = synth.decode_workload("8b", seed=11, lens=lens, Hq=Hq, Hkv=Hkv)
-    got, ref, _ = run(w, partition_tokens=512)
+    got, ref, _ = run(w, partition_tokens=512, kernel=kernel)
     compare(got, ref, torch.bfloat16, f"long {lens}")
 
 
@@ -132,8 +144,29 @@ def test_large_batch_grid_kernel(Hq, Hkv):
     rng = np.random.default_rng(13)
     lens = [int(x) for x in rng.integers(1, 301, size=1100)]
     w = synth.decode_workload("8b", seed=13, lens=lens, Hq=Hq, Hkv=Hkv)
-    got, ref, _ = run(w, partition_tokens=64)
+    got, ref, _ = run(w, partition_tokens=64, kernel="grid")
     compare(got, ref, torch.bfloat16, f"B=1100 {Hq}/{Hkv}")
+
+
+def test_kernel_choice_follows_the_work_bound():
+    """The grid kernel runs a batch while B * Hkv * partitions of the table
+    capacity is at most 2 x the persistent grid's warps (8 per SM), and for
+    B > 1024; the persistent kernel otherwise.  On a 152-SM GB300, 8B-shaped
+    batches (4096-token tables, 512-token partitions) switch after 38
+    sequences and 32k-token tables after 4."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for B in range(1, 200):
+        for Hkv, MB, bs in ((8, 256, 16), (8, 1024, 32), (2, 64, 64)):
+            parts = -(-MB * bs // 512)
+            want = "grid" if B * Hkv * parts <= 16 * sms else "persistent"
+            assert ops().decode_kernel_for(B, Hkv, MB, bs, 512) == want, (B, Hkv, MB, bs)
+    assert ops().decode_kernel_for(1025, 8, 256, 16, 512) == "grid"
+    assert ops().decode_kernel_for(1024, 8, 256, 16, 512) == "persistent"
+    if sms == 152:
+        assert ops().decode_kernel_for(38, 8, 256, 16, 512) == "grid"
+        assert ops().decode_kernel_for(39, 8, 256, 16, 512) == "persistent"
+        assert ops().decode_kernel_for(4, 8, 1024, 32, 512) == "grid"
+        assert ops().decode_kernel_for(5, 8, 1024, 32, 512) == "persistent"
 
 
 def test_single_token_returns_v0_exactly():
@@ -165,13 +198,14 @@ def test_dominant_key_selects_its_value():
     compare(got, ref, torch.bfloat16, "dominant")
 
 
-@pytest.mark.parametrize("nseq", [1, 9])
-def test_bad_block_id_is_recorded_not_faulted(nseq):
+@pytest.mark.parametrize("nseq,kernel", [(1, "grid"), (64, "persistent")])
+def test_bad_block_id_is_recorded_not_faulted(nseq, kernel):
     """An out-of-pool table entry is replaced by block 0 in the kernel and
-    reported in the device error word (no out-of-bounds access); one sequence
-    runs on the grid kernel, nine (72 items) on the persistent one."""
+    reported in the device error word (no out-of-bounds access), on both
+    decode kernels."""
     from paged_kv_cache_192_gb300._lib import PA_DEVERR_BAD_BLOCK
     w = synth.decode_workload("8b", seed=10, lens=[40] * nseq)
+    assert kernel_of(w) == kernel
     k_cache, v_cache, table, lens = device_inputs(w, DEV)
     table[0, 1] = w.num_blocks + 5
     ops().device_error(clear=True)

@@ -153,8 +153,9 @@ enum { PA_DECODE_PERSISTENT = 1, PA_DECODE_GRID = 2 };
  *                         tile) units evenly over its warps;
  *   PA_DECODE_GRID        one CTA per (sequence, KV head, partition), then a
  *                         merge kernel; chosen when B * Hkv * (partitions of
- *                         the table capacity) is at most twice the persistent
- *                         grid's warp count (little work), and for B > 1024.
+ *                         the table capacity) is at most 1.75 times the
+ *                         persistent grid's warp count (little work), and for
+ *                         B > 1024.
  * Both meet the same error bound; their results may differ in the last bits
  * (another order of the partial sums).  Arguments as for pa_decode;
  * *kernel receives PA_DECODE_PERSISTENT or PA_DECODE_GRID.  PA_ERR_INVALID

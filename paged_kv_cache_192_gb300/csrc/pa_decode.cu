@@ -1115,18 +1115,18 @@ int launch_grid(const DecodeParams &p, cudaStream_t stream) {
 // the grid kernel: there every (sequence, KV head, partition) gets a CTA of
 // four warps, while the persistent split leaves a partition to one warp (its
 // tiles streamed one after another) and an item's segments to one merging
-// warp.  Measured with 512-token partitions, 32 query / 8 KV heads, d 128:
-// 16-token blocks and 4096-token tables, the grid kernel is ahead up to 32
-// sequences (26.6 against 53.2 us at 8, 67.7 against 69.6 at 32) and behind
-// from 48 (88.1 against 77.8); 64 query heads, 32k-token tables, up to 4
-// sequences (63.5 against 155.7 us at 1) and even at 8 (233 against 231).
-// Rule: the grid kernel while its CTA count, bounded by the table capacity,
-// is at most twice the persistent grid's warps.
+// warp.  Measured with 512-token partitions, 32 query / 8 KV heads, d 128,
+// 16-token blocks and 4096-token tables: grid against persistent kernel 20.3
+// against 53.2 us at 1 sequence, 25.6 against 53.2 at 8, 69.3 against 69.6 at
+// 32, 76.6 at 38 against 71.1 at 39; 64 query heads, 32-token blocks and
+// 32k-token tables: 63.6 against 155.7 us at 1, 151.1 against 190.5 at 4,
+// 233 against 231 at 8.  Rule: the grid kernel while its CTA count, bounded
+// by the table capacity, is at most 1.75 times the persistent grid's warps.
 int kernel_for(int B, int Hkv, int MB, int bs_log2, int partitions, int sms) {
     if (B > kPersistentMaxB || int64_t(B) * (int64_t(MB) << bs_log2) / 8 >= (1ll << 31))
         return PA_DECODE_GRID;
     const int64_t grid_ctas = int64_t(B) * Hkv * partitions;
-    return grid_ctas <= 2ll * sms * kMinCtas * kWarps ? PA_DECODE_GRID : PA_DECODE_PERSISTENT;
+    return 4 * grid_ctas <= 7ll * sms * kMinCtas * kWarps ? PA_DECODE_GRID : PA_DECODE_PERSISTENT;
 }
 
 template <typename T, int D, int GQ>

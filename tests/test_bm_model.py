@@ -95,3 +95,31 @@ def test_freed_blocks_are_reused_first():
     bm.free_seq(0)
     bm.add_seq(1, 4)
     assert bm.blocks[1] == [blocks[-1]]
+
+
+def test_copy_on_write_counts_against_the_pool():
+    """The copy a diverging branch needs is a new block like any other: with
+    the pool exhausted the append is refused and nothing changes."""
+    bm = BlockManagerModel(1, 16)
+    bm.add_seq(0, 4)   # the only block, partly filled
+    bm.fork(0, 1)
+    before = (list(bm.free), list(bm.ref), {k: list(v) for k, v in bm.blocks.items()},
+              dict(bm.length))
+    with pytest.raises(OutOfBlocks):
+        bm.append(0)
+    with pytest.raises(OutOfBlocks):
+        bm.append_n(1, 1)
+    assert (bm.free, bm.ref, bm.blocks, bm.length) == before
+
+
+def test_shuffled_order_reaches_every_permutation():
+    """Fisher-Yates (swap with j uniform in [0, i]) can produce every
+    permutation: over many seeds all 3! orders of three blocks appear, each
+    about equally often.  (Drawing j from [0, i) instead, Sattolo's variant,
+    gives only the two cyclic orders.)"""
+    counts = {}
+    for seed in range(1, 1201):
+        o = tuple(initial_order(3, seed))
+        counts[o] = counts.get(o, 0) + 1
+    assert len(counts) == 6
+    assert all(150 <= c <= 250 for c in counts.values()), counts

@@ -29,6 +29,18 @@ MUTATIONS = {
                                 "memcpy(k_cache + dst, v_new + src, row);"),
     "copy-on-write copies K only": (
         "memmove(v_cache + (size_t)dst * blk, v_cache + (size_t)src * blk, blk);", ""),
+    "dot product over half the dims": ("for (int c = 0; c < d; ++c) dot += qi[c] * kj[c];",
+                                       "for (int c = 0; c < d / 2; ++c) dot += qi[c] * kj[c];"),
+    "GQA group taken as the KV head count": ("const int group = J->Hq / J->Hkv;",
+                                             "const int group = J->Hkv;"),
+    "store ignores the KV head": (
+        "const size_t dst = (size_t)(((blk * Hkv + h) * bs + off)) * row;",
+        "const size_t dst = (size_t)(((blk * Hkv) * bs + off)) * row;"),
+    "copy direction reversed": (
+        "memmove(k_cache + (size_t)dst * blk, k_cache + (size_t)src * blk, blk);",
+        "memmove(k_cache + (size_t)src * blk, k_cache + (size_t)dst * blk, blk);"),
+    "slot offset from the block index": ("(int64_t)table[j / bs] * bs + j % bs",
+                                         "(int64_t)table[j / bs] * bs + j / bs"),
 }
 
 

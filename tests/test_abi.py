@@ -87,6 +87,17 @@ def test_decode_kernel_for_rejects_bad_sizes(lib, args):
     assert lib.pa_decode_kernel_for(4, 8, 256, 16, 0, None) == 1
 
 
+def test_decode_kernel_for_needs_a_device(lib):
+    """Valid sizes: the choice depends on the device's SM count, so without a
+    CUDA device the call fails cleanly (PA_ERR_CUDA) instead of guessing."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    k = ctypes.c_int(-1)
+    assert lib.pa_decode_kernel_for(64, 8, 256, 16, 0, ctypes.byref(k)) == 3
+    assert k.value == -1 and lib.pa_last_error_string()
+
+
 def test_null_pointers_rejected(lib):
     rc = lib.pa_decode(None, None, None, None, None, 4, None, 2, 4, 4, 64, 16, 8, 0.125, 0, None,
                        0, 1, None)

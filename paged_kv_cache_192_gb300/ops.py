@@ -35,6 +35,17 @@ def _cuda(t: torch.Tensor, name: str, dtype=None):
     return t.data_ptr()
 
 
+def _require(cond: bool, msg: str):
+    """Shape check of a call's tensors (raised, not asserted: the kernels size
+    their reads and writes from these shapes)."""
+    if not cond:
+        raise ValueError(msg)
+
+
+def _pairs_ok(pairs) -> bool:
+    return pairs.numel() == 0 or (pairs.dim() == 2 and pairs.shape[1] == 2)
+
+
 def _stream(stream=None) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
@@ -61,10 +72,14 @@ def check_wait_timeout(stream=None):
 
 def reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None):
     """Store new K/V rows [T][Hkv][d] into their slots of the [NB][Hkv][bs][d] pools."""
+    _require(k_cache.dim() == 4 and k_new.dim() == 3,
+             "pools must be [NB][Hkv][bs][d] and k_new [T][Hkv][d]")
     NB, Hkv, bs, d = k_cache.shape
     T = k_new.shape[0]
-    assert k_new.shape == (T, Hkv, d) and v_new.shape == k_new.shape
-    assert v_cache.shape == k_cache.shape and slot_mapping.shape == (T,)
+    _require(k_new.shape == (T, Hkv, d) and v_new.shape == k_new.shape,
+             f"k_new/v_new must be [T][Hkv][d] = [{T}][{Hkv}][{d}]")
+    _require(v_cache.shape == k_cache.shape, "k_cache and v_cache must have the same shape")
+    _require(slot_mapping.shape == (T,), f"slot_mapping must be [{T}]")
     check(lib().pa_reshape_and_cache(
         _cuda(k_new, "k_new", k_cache.dtype), _cuda(v_new, "v_new", k_cache.dtype),
         _cuda(k_cache, "k_cache"), _cuda(v_cache, "v_cache", k_cache.dtype),
@@ -74,7 +89,10 @@ def reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None)
 
 def copy_blocks(k_cache, v_cache, pairs, stream=None):
     """Copy physical blocks pairs[i][0] -> pairs[i][1] of both pools."""
+    _require(k_cache.dim() == 4, "pools must be [NB][Hkv][bs][d]")
     NB, Hkv, bs, d = k_cache.shape
+    _require(v_cache.shape == k_cache.shape, "k_cache and v_cache must have the same shape")
+    _require(_pairs_ok(pairs), "pairs must be [n][2]")
     n = pairs.shape[0] if pairs.numel() else 0
     check(lib().pa_copy_blocks(
         _cuda(k_cache, "k_cache"), _cuda(v_cache, "v_cache", k_cache.dtype),
@@ -85,10 +103,14 @@ def copy_blocks(k_cache, v_cache, pairs, stream=None):
 def swap_blocks(dst_k, dst_v, src_k, src_v, pairs, stream=None):
     """Copy blocks pairs[i][0] of the source pools into blocks pairs[i][1] of
     the destination pools; either side may be pinned host memory."""
+    _require(src_k.dim() == 4 and dst_k.dim() == 4, "pools must be [NB][Hkv][bs][d]")
     NBs, Hkv, bs, d = src_k.shape
     NBd = dst_k.shape[0]
-    assert dst_k.shape[1:] == src_k.shape[1:] and dst_v.shape == dst_k.shape
-    assert src_v.shape == src_k.shape and src_k.dtype == dst_k.dtype
+    _require(dst_k.shape[1:] == src_k.shape[1:] and dst_v.shape == dst_k.shape,
+             "destination pools must be [NB'][Hkv][bs][d] like the source pools")
+    _require(src_v.shape == src_k.shape, "src_k and src_v must have the same shape")
+    _require(src_k.dtype == dst_k.dtype == src_v.dtype == dst_v.dtype, "pools must share a dtype")
+    _require(_pairs_ok(pairs), "pairs must be [n][2]")
     n = pairs.shape[0] if pairs.numel() else 0
     for name, t in (("dst_k", dst_k), ("dst_v", dst_v), ("src_k", src_k), ("src_v", src_v),
                     ("pairs", pairs)):
@@ -119,12 +141,23 @@ def decode_kernel_for(B, Hkv, max_blocks_per_seq, block_size, partition_tokens=0
     return {_lib.PA_DECODE_PERSISTENT: "persistent", _lib.PA_DECODE_GRID: "grid"}[out.value]
 
 
+def _check_decode_shapes(q, k_cache, v_cache, block_table, context_lens, out):
+    _require(q.dim() == 3 and k_cache.dim() == 4, "q must be [B][Hq][d], pools [NB][Hkv][bs][d]")
+    B, Hq, d = q.shape
+    _require(k_cache.shape[3] == d, f"pools must have head_dim {d} like q")
+    _require(v_cache.shape == k_cache.shape, "k_cache and v_cache must have the same shape")
+    _require(block_table.dim() == 2 and block_table.shape[0] == B,
+             f"block_table must be [{B}][max_blocks_per_seq]")
+    _require(context_lens.shape == (B,), f"context_lens must be [{B}]")
+    _require(out is None or out.shape == q.shape, "out must have the shape of q")
+
+
 def decode(q, k_cache, v_cache, block_table, context_lens, scale=None, partition_tokens=0,
            workspace=None, out=None, stream=None):
     """Paged decode attention; q [B][Hq][d] -> out [B][Hq][d]."""
+    _check_decode_shapes(q, k_cache, v_cache, block_table, context_lens, out)
     B, Hq, d = q.shape
-    NB, Hkv, bs, d2 = k_cache.shape
-    assert d2 == d and block_table.shape[0] == B and context_lens.shape == (B,)
+    NB, Hkv, bs, _ = k_cache.shape
     MB = block_table.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     ws_bytes = decode_workspace_size(B, Hq, d, MB, bs, partition_tokens)
@@ -152,9 +185,9 @@ def decode_noalloc(q, k_cache, v_cache, block_table, context_lens, scale=None,
     """pa_decode_noalloc: as decode, with the split-KV workspace taken from the
     library's fixed device array (nothing is allocated when `out` is given);
     calls that overlap on the GPU race on that array."""
+    _check_decode_shapes(q, k_cache, v_cache, block_table, context_lens, out)
     B, Hq, d = q.shape
-    NB, Hkv, bs, d2 = k_cache.shape
-    assert d2 == d and block_table.shape[0] == B and context_lens.shape == (B,)
+    NB, Hkv, bs, _ = k_cache.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)
@@ -169,10 +202,17 @@ def decode_noalloc(q, k_cache, v_cache, block_table, context_lens, scale=None,
 def prefill_chunk(q, k_cache, v_cache, block_table, query_start, context_lens, max_query_len,
                   scale=None, out=None, stream=None):
     """Causal chunked prefill; q [sum n][Hq][d] -> out [sum n][Hq][d] (bf16)."""
+    _require(q.dim() == 3 and k_cache.dim() == 4 and context_lens.dim() == 1,
+             "q must be [tokens][Hq][d], pools [NB][Hkv][bs][d], context_lens [R]")
     Tq, Hq, d = q.shape
-    NB, Hkv, bs, d2 = k_cache.shape
+    NB, Hkv, bs, _ = k_cache.shape
     R = context_lens.shape[0]
-    assert d2 == d and query_start.shape == (R + 1,) and block_table.shape[0] == R
+    _require(k_cache.shape[3] == d, f"pools must have head_dim {d} like q")
+    _require(v_cache.shape == k_cache.shape, "k_cache and v_cache must have the same shape")
+    _require(query_start.shape == (R + 1,), f"query_start must be [{R + 1}]")
+    _require(block_table.dim() == 2 and block_table.shape[0] == R,
+             f"block_table must be [{R}][max_blocks_per_seq]")
+    _require(out is None or out.shape == q.shape, "out must have the shape of q")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)

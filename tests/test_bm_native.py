@@ -155,3 +155,33 @@ def test_invalid_calls(BM):
         bm.append(9)
     with pytest.raises(PAError):
         bm.block_table([0], 0)
+
+
+def test_copy_on_write_counts_against_the_pool(BM):
+    """A diverging branch's copy of a shared, partly filled block is refused
+    when the pool is empty, and nothing changes (same rule as the model)."""
+    from paged_kv_cache_192_gb300._lib import OutOfBlocks as NativeOOB
+    bm = BM(1, 16)
+    bm.add_seq(0, 4)
+    bm.fork(0, 1)
+    state = (bm.num_free(), bm.seq_blocks(0), bm.seq_blocks(1), bm.refcount(0),
+             bm.seq_len(0), bm.seq_len(1))
+    with pytest.raises(NativeOOB):
+        bm.append(0)
+    with pytest.raises(NativeOOB):
+        bm.append_n(1, 1)
+    assert (bm.num_free(), bm.seq_blocks(0), bm.seq_blocks(1), bm.refcount(0),
+            bm.seq_len(0), bm.seq_len(1)) == state
+    bm.free_seq(1)                      # the last holder then writes in place
+    slot, src, dst = bm.append(0)
+    assert (src, dst) == (-1, -1) and slot == bm.seq_blocks(0)[0] * 16 + 4
+
+
+def test_seeded_order_is_the_models(BM):
+    """The native free list starts in the model's seeded order (the same
+    SplitMix64-driven Fisher-Yates shuffle), block for block."""
+    from oracle.bm_model import initial_order
+    for seed in (1, 2, 99, 2**40 + 3):
+        bm = BM(50, 8, seed=seed)
+        bm.add_seq(0, 50 * 8)
+        assert bm.seq_blocks(0) == initial_order(50, seed)

@@ -47,7 +47,7 @@ typedef struct CUstream_st *pa_stream_t; /* same type as cudaStream_t */
 enum {
     PA_OK = 0,
     PA_ERR_INVALID = 1,     /* bad argument, shape or (validate mode) metadata */
-    PA_ERR_OOM = 2,         /* block manager: not enough free blocks */
+    PA_ERR_OOM = 2,         /* block manager: not enough free blocks or host memory */
     PA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
     PA_ERR_UNSUPPORTED = 4, /* valid request this build has no kernel for */
     PA_ERR_DEVICE = 5       /* pa_device_error found a device-side error */
@@ -294,6 +294,15 @@ int pa_bm_seq_len(const pa_bm *bm, int64_t seq, int64_t *len);
 int pa_bm_seq_blocks(const pa_bm *bm, int64_t seq, int32_t *out, int64_t cap, int64_t *n);
 int pa_bm_refcount(const pa_bm *bm, int64_t block, int *refcount);
 int64_t pa_bm_num_free(const pa_bm *bm);
+
+/*
+ * Host fault injection, for tests of the failure path: from now on the k-th
+ * point at which a block-manager call may allocate host memory (k = 0: the
+ * next one) fails as if memory had run out; the call returns PA_ERR_OOM and
+ * leaves the manager unchanged.  One failure per arming; k < 0 disarms.
+ * Process-wide, not thread safe; never armed unless a caller arms it.
+ */
+void pa_bm_inject_alloc_failure(int64_t k);
 
 #ifdef __cplusplus
 }

@@ -58,6 +58,7 @@ SIGNATURES = {
     "pa_bm_seq_blocks": (_c_int, [_c_vp, _c_i64, _p_i32, _c_i64, _p_i64]),
     "pa_bm_refcount": (_c_int, [_c_vp, _c_i64, ctypes.POINTER(_c_int)]),
     "pa_bm_num_free": (_c_i64, [_c_vp]),
+    "pa_bm_inject_alloc_failure": (None, [_c_i64]),
 }
 
 

@@ -8,6 +8,13 @@ import numpy as np
 from ._lib import check, lib
 
 
+def inject_alloc_failure(k: int):
+    """Test hook (pa_bm_inject_alloc_failure): the k-th host allocation point
+    of the following block-manager calls fails as if host memory ran out
+    (the call raises OutOfBlocks and changes nothing); k < 0 disarms."""
+    lib().pa_bm_inject_alloc_failure(int(k))
+
+
 class BlockManager:
     """Free list, refcounts, fork and copy-on-write over a pool of physical blocks.
 

@@ -20,8 +20,13 @@
 // reused first) whose initial order is 0..n-1 or a SplitMix64-driven
 // Fisher-Yates shuffle; the first branch that appends into a shared, partly
 // filled last block takes the copy; a full shared block is never copied.
-// Every failing call leaves the state unchanged.
+// Every failing call leaves the state unchanged, host allocation failures
+// included: every call allocates what it needs (vector capacity, map nodes)
+// before it changes anything, and no exception leaves the C ABI.
+#include <algorithm>
+#include <atomic>
 #include <cstdint>
+#include <memory>
 #include <new>
 #include <unordered_map>
 #include <utility>
@@ -51,6 +56,8 @@ struct pa_bm {
         ref[b] = 1;
         return b;
     }
+    // never allocates: the stack holds each block at most once and keeps the
+    // capacity of num_blocks it was created with
     void release(int32_t b) {
         if (--ref[b] == 0) free_stack.push_back(b);
     }
@@ -69,6 +76,40 @@ struct pa_bm {
 
 namespace {
 
+// Host fault injection for tests: the k-th allocation point from now on
+// (0 = the next) throws std::bad_alloc as if host memory had run out.
+std::atomic<int64_t> g_alloc_failure{-1};
+
+// Marks a statement that may allocate host memory.
+void alloc_point() {
+    int64_t k = g_alloc_failure.load(std::memory_order_relaxed);
+    if (k < 0) return;
+    g_alloc_failure.store(k - 1, std::memory_order_relaxed);
+    if (k == 0) throw std::bad_alloc();
+}
+
+// Capacity for n elements, growing geometrically (a plain reserve(size + 1)
+// per append would copy the table every time).
+void ensure_capacity(std::vector<int32_t> &v, size_t n) {
+    if (v.capacity() >= n) return;
+    alloc_point();
+    v.reserve(std::max(n, 2 * v.capacity()));
+}
+
+// Runs an entry point's body; host allocation failures become PA_ERR_OOM
+// (the body has changed nothing when one is thrown) and no exception crosses
+// the C ABI.
+template <class F>
+int guarded(const char *what, F &&body) {
+    try {
+        return body();
+    } catch (const std::bad_alloc &) {
+        return pa::fail(PA_ERR_OOM, "%s: host allocation failed", what);
+    } catch (...) {
+        return pa::fail(PA_ERR_INVALID, "%s: unexpected host error", what);
+    }
+}
+
 uint64_t splitmix64(uint64_t &state) {
     state += 0x9E3779B97F4A7C15ull;
     uint64_t z = state;
@@ -77,7 +118,8 @@ uint64_t splitmix64(uint64_t &state) {
     return z ^ (z >> 31);
 }
 
-// Append one token to s; the caller has checked that a block is available.
+// Append one token to s; the caller has checked that a block is available
+// and made room in s.blocks for a new block (nothing here allocates).
 void append_one(pa_bm *bm, pa_bm::Seq &s, int64_t *slot, int64_t *cow_src, int64_t *cow_dst) {
     int64_t src = -1, dst = -1;
     if (s.len % bm->bs == 0) {
@@ -104,23 +146,28 @@ int pa_bm_create(int64_t num_blocks, int block_size, uint64_t seed, pa_bm **out)
     *out = nullptr;
     if (num_blocks <= 0 || num_blocks > INT32_MAX || block_size <= 0)
         return pa::fail(PA_ERR_INVALID, "bm_create: bad sizes");
-    pa_bm *bm = new (std::nothrow) pa_bm();
-    if (!bm) return pa::fail(PA_ERR_OOM, "bm_create: host allocation failed");
-    bm->num_blocks = num_blocks;
-    bm->bs = block_size;
-    std::vector<int32_t> order(num_blocks);
-    for (int64_t i = 0; i < num_blocks; ++i) order[i] = static_cast<int32_t>(i);
-    if (seed) {
-        uint64_t st = seed;
-        for (int64_t i = num_blocks - 1; i > 0; --i) {
-            const uint64_t j = splitmix64(st) % uint64_t(i + 1);
-            std::swap(order[i], order[j]);
+    return guarded("bm_create", [&] {
+        alloc_point();
+        std::unique_ptr<pa_bm> bm(new pa_bm());
+        bm->num_blocks = num_blocks;
+        bm->bs = block_size;
+        alloc_point();
+        std::vector<int32_t> order(num_blocks);
+        for (int64_t i = 0; i < num_blocks; ++i) order[i] = static_cast<int32_t>(i);
+        if (seed) {
+            uint64_t st = seed;
+            for (int64_t i = num_blocks - 1; i > 0; --i) {
+                const uint64_t j = splitmix64(st) % uint64_t(i + 1);
+                std::swap(order[i], order[j]);
+            }
         }
-    }
-    bm->free_stack.assign(order.rbegin(), order.rend());
-    bm->ref.assign(num_blocks, 0);
-    *out = bm;
-    return PA_OK;
+        alloc_point();
+        bm->free_stack.assign(order.rbegin(), order.rend());
+        alloc_point();
+        bm->ref.assign(num_blocks, 0);
+        *out = bm.release();
+        return int(PA_OK);
+    });
 }
 
 void pa_bm_destroy(pa_bm *bm) { delete bm; }
@@ -133,14 +180,19 @@ int pa_bm_add_seq(pa_bm *bm, int64_t seq, int64_t n_tokens, int64_t *slots) {
     if (nblk > int64_t(bm->free_stack.size()))
         return pa::fail(PA_ERR_OOM, "bm_add_seq: %lld blocks needed, %zu free", (long long)nblk,
                         bm->free_stack.size());
-    pa_bm::Seq s;
-    s.blocks.reserve(nblk);
-    for (int64_t i = 0; i < nblk; ++i) s.blocks.push_back(bm->take());
-    s.len = n_tokens;
-    if (slots)
-        for (int64_t j = 0; j < n_tokens; ++j) slots[j] = bm->slot(s, j);
-    bm->seqs.emplace(seq, std::move(s));
-    return PA_OK;
+    return guarded("bm_add_seq", [&] {
+        pa_bm::Seq s;
+        ensure_capacity(s.blocks, size_t(nblk));
+        alloc_point();
+        pa_bm::Seq &dst = bm->seqs.emplace(seq, pa_bm::Seq{}).first->second;
+        // nothing below allocates
+        for (int64_t i = 0; i < nblk; ++i) s.blocks.push_back(bm->take());
+        s.len = n_tokens;
+        if (slots)
+            for (int64_t j = 0; j < n_tokens; ++j) slots[j] = bm->slot(s, j);
+        dst = std::move(s);
+        return int(PA_OK);
+    });
 }
 
 int pa_bm_fork(pa_bm *bm, int64_t parent, int64_t child) {
@@ -149,10 +201,15 @@ int pa_bm_fork(pa_bm *bm, int64_t parent, int64_t child) {
     auto it = bm->seqs.find(parent);
     if (it == bm->seqs.end()) return pa::fail(PA_ERR_INVALID, "bm_fork: unknown parent");
     if (bm->seqs.count(child)) return pa::fail(PA_ERR_INVALID, "bm_fork: child exists");
-    pa_bm::Seq c = it->second;
-    for (int32_t b : c.blocks) ++bm->ref[b];
-    bm->seqs.emplace(child, std::move(c));
-    return PA_OK;
+    return guarded("bm_fork", [&] {
+        alloc_point();
+        pa_bm::Seq c = it->second;
+        alloc_point();
+        // (the insertion may rehash: `it` is not used after it)
+        const pa_bm::Seq &cs = bm->seqs.emplace(child, std::move(c)).first->second;
+        for (int32_t b : cs.blocks) ++bm->ref[b];
+        return int(PA_OK);
+    });
 }
 
 int pa_bm_append(pa_bm *bm, int64_t seq, int64_t *slot, int64_t *cow_src, int64_t *cow_dst) {
@@ -162,8 +219,12 @@ int pa_bm_append(pa_bm *bm, int64_t seq, int64_t *slot, int64_t *cow_src, int64_
     if (it == bm->seqs.end()) return pa::fail(PA_ERR_INVALID, "bm_append: unknown sequence");
     if (bm->needed(it->second, 1) > int64_t(bm->free_stack.size()))
         return pa::fail(PA_ERR_OOM, "bm_append: no free block");
-    append_one(bm, it->second, slot, cow_src, cow_dst);
-    return PA_OK;
+    return guarded("bm_append", [&] {
+        pa_bm::Seq &s = it->second;
+        ensure_capacity(s.blocks, size_t((s.len + 1 + bm->bs - 1) / bm->bs));
+        append_one(bm, s, slot, cow_src, cow_dst);
+        return int(PA_OK);
+    });
 }
 
 int pa_bm_append_n(pa_bm *bm, int64_t seq, int64_t n, int64_t *slots, int64_t *cow_src,
@@ -175,18 +236,22 @@ int pa_bm_append_n(pa_bm *bm, int64_t seq, int64_t n, int64_t *slots, int64_t *c
     if (it == bm->seqs.end()) return pa::fail(PA_ERR_INVALID, "bm_append_n: unknown sequence");
     if (bm->needed(it->second, n) > int64_t(bm->free_stack.size()))
         return pa::fail(PA_ERR_OOM, "bm_append_n: not enough free blocks");
-    int64_t src = -1, dst = -1;
-    for (int64_t i = 0; i < n; ++i) {
-        int64_t a, b;
-        append_one(bm, it->second, &slots[i], &a, &b);
-        if (a >= 0) {
-            src = a;
-            dst = b;
+    return guarded("bm_append_n", [&] {
+        pa_bm::Seq &s = it->second;
+        ensure_capacity(s.blocks, size_t((s.len + n + bm->bs - 1) / bm->bs));
+        int64_t src = -1, dst = -1;
+        for (int64_t i = 0; i < n; ++i) {
+            int64_t a, b;
+            append_one(bm, s, &slots[i], &a, &b);
+            if (a >= 0) {
+                src = a;
+                dst = b;
+            }
         }
-    }
-    if (cow_src) *cow_src = src;
-    if (cow_dst) *cow_dst = dst;
-    return PA_OK;
+        if (cow_src) *cow_src = src;
+        if (cow_dst) *cow_dst = dst;
+        return int(PA_OK);
+    });
 }
 
 int pa_bm_free_seq(pa_bm *bm, int64_t seq) {
@@ -251,5 +316,9 @@ int pa_bm_refcount(const pa_bm *bm, int64_t block, int *refcount) {
 }
 
 int64_t pa_bm_num_free(const pa_bm *bm) { return bm ? int64_t(bm->free_stack.size()) : -1; }
+
+void pa_bm_inject_alloc_failure(int64_t k) {
+    g_alloc_failure.store(k < 0 ? -1 : k, std::memory_order_relaxed);
+}
 
 }  // extern "C"

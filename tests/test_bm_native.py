@@ -185,3 +185,76 @@ def test_seeded_order_is_the_models(BM):
         bm = BM(50, 8, seed=seed)
         bm.add_seq(0, 50 * 8)
         assert bm.seq_blocks(0) == initial_order(50, seed)
+
+
+def _snapshot(bm, seqs):
+    return (bm.num_free(), [(s, bm.seq_len(s), bm.seq_blocks(s)) for s in seqs],
+            [bm.refcount(b) for b in range(bm.num_blocks)])
+
+
+def _apply(m, op):
+    kind, *a = op
+    if kind == "add":
+        return list(m.add_seq(*a))
+    if kind == "fork":
+        return m.fork(*a)
+    if kind == "append":
+        return tuple(m.append(*a))
+    if kind == "append_n":
+        slots, pairs = m.append_n(*a)
+        return list(slots), [tuple(p) for p in pairs]
+    if kind == "free":
+        return m.free_seq(*a)
+    raise AssertionError(kind)
+
+
+def test_host_allocation_failures_leave_state_unchanged(BM):
+    """Host fault injection: every call of a script is failed at each of its
+    host allocation points in turn.  Each failure raises OutOfBlocks with the
+    manager exactly as before (its later allocations still follow the model,
+    so the free-list order is untouched too); then the call runs through and
+    matches the model."""
+    from paged_kv_cache_192_gb300._lib import OutOfBlocks as NativeOOB
+    from paged_kv_cache_192_gb300.block_manager import inject_alloc_failure
+    script = [("add", 0, 40), ("fork", 0, 1), ("append", 1), ("append_n", 0, 37),
+              ("add", 2, 0), ("append", 2), ("fork", 1, 3), ("append", 3), ("free", 0),
+              ("append_n", 3, 20), ("add", 4, 9)]
+    bm, model = BM(64, 8, seed=4), BlockManagerModel(64, 8, seed=4)
+    live = []
+    injected = 0
+    for op in script:
+        k = 0
+        while True:
+            before = _snapshot(bm, live)
+            inject_alloc_failure(k)
+            try:
+                got = _apply(bm, op)
+            except NativeOOB as e:
+                assert "host allocation failed" in str(e)
+                assert _snapshot(bm, live) == before, (op, k)
+                k += 1
+                injected += 1
+                continue
+            finally:
+                inject_alloc_failure(-1)
+            break
+        assert got == _apply(model, op), op
+        if op[0] in ("add", "fork"):
+            live.append(op[-2] if op[0] == "add" else op[2])
+        elif op[0] == "free":
+            live.remove(op[1])
+        _same_state(bm, model, live)
+    assert injected >= len(script)
+
+
+def test_create_fails_cleanly_under_host_allocation_failure(BM):
+    from paged_kv_cache_192_gb300._lib import OutOfBlocks as NativeOOB
+    from paged_kv_cache_192_gb300.block_manager import inject_alloc_failure
+    for k in range(4):
+        inject_alloc_failure(k)
+        try:
+            with pytest.raises(NativeOOB, match="host allocation failed"):
+                BM(32, 16, seed=1)
+        finally:
+            inject_alloc_failure(-1)
+    assert BM(32, 16, seed=1).num_free() == 32

@@ -235,6 +235,15 @@ class Plan:
         raise NotImplementedError
 
 
+def unique_kv_bytes(table, lens, bs, Hkv, d, es):
+    """K and V bytes of the distinct physical blocks that a decode batch reads
+    (each whole (block, KV head) piece once, however many sequences share it)."""
+    used = set()
+    for r, L in enumerate(lens):
+        used.update(np.asarray(table[r][:-(-int(L) // bs)]).tolist())
+    return len(used) * Hkv * bs * d * es * 2
+
+
 def decode_kernel_info(B, Hkv, MB, bs, PT):
     """(name of the decode kernel for the roofline line, launches of one
     pa_decode) for a batch of these sizes."""
@@ -395,10 +404,7 @@ class PrefixPlan(Plan):
         self.ws = torch.zeros(max(self.ws_bytes // 4, 1), dtype=torch.float32, device=dev)
         es = _es(w.dtype)
         self.decode_bytes = decode_bytes(lens, self.Bd, Hq, Hkv, d, bs, w.dtype)
-        used = set()
-        for r, L in enumerate(lens):
-            used.update(table[r, :-(-int(L) // bs)].tolist())
-        unique = len(used) * Hkv * bs * d * es * 2
+        unique = unique_kv_bytes(table, lens, bs, Hkv, d, es)
         # roofline on unique bytes: the shared prompt is read from HBM once and
         # then served from L2 to every sequence that shares it
         logical_kv = int(np.sum(lens)) * 2 * Hkv * d * es

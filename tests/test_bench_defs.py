@@ -81,3 +81,15 @@ def test_reference_arm_prints_the_contract_line(bench, capsys):
     e2e = j["e2e"]
     assert e2e["value"] == j["value"] and e2e["h2d_bytes_per_step"] == 0
     assert e2e["d2h_bytes_per_step"] == 0
+
+
+def test_unique_kv_bytes_counts_shared_blocks_once(bench):
+    """Two sequences sharing a 2-block prompt (blocks 7, 3) plus private
+    blocks: 5 distinct blocks are read; padding entries past a sequence's
+    length do not count."""
+    table = np.array([[7, 3, 9, 0], [7, 3, 4, 11]], dtype=np.int32)
+    lens = [40, 56]          # 16-token blocks: 3 and 4 blocks
+    per_block = 2 * 16 * 64 * 2 * 2   # Hkv * bs * d * es * (K and V)
+    assert bench.unique_kv_bytes(table, lens, 16, 2, 64, 2) == 5 * per_block
+    assert bench.unique_kv_bytes(table, [1, 1], 16, 2, 64, 2) == 1 * per_block
+

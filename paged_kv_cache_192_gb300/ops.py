@@ -71,7 +71,12 @@ def check_wait_timeout(stream=None):
 
 
 def reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None):
-    """Store new K/V rows [T][Hkv][d] into their slots of the [NB][Hkv][bs][d] pools."""
+    """Store new K/V rows into their slots of the pools (pa_reshape_and_cache).
+
+    k_new, v_new: [T][Hkv][d], the pools' dtype.  k_cache, v_cache:
+    [NB][Hkv][bs][d], written in place.  slot_mapping: int64 [T], slot =
+    physical block * bs + offset; a negative slot is padding and is skipped.
+    Bit exact.  Duplicate slots in one call are a caller error."""
     _require(k_cache.dim() == 4 and k_new.dim() == 3,
              "pools must be [NB][Hkv][bs][d] and k_new [T][Hkv][d]")
     NB, Hkv, bs, d = k_cache.shape
@@ -88,7 +93,9 @@ def reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None)
 
 
 def copy_blocks(k_cache, v_cache, pairs, stream=None):
-    """Copy physical blocks pairs[i][0] -> pairs[i][1] of both pools."""
+    """Copy-on-write copies (pa_copy_blocks): for each row (src, dst) of the
+    int64 [n][2] device tensor `pairs`, block dst of both pools becomes a byte
+    copy of block src.  No dst may equal a src or another dst of the call."""
     _require(k_cache.dim() == 4, "pools must be [NB][Hkv][bs][d]")
     NB, Hkv, bs, d = k_cache.shape
     _require(v_cache.shape == k_cache.shape, "k_cache and v_cache must have the same shape")
@@ -154,7 +161,16 @@ def _check_decode_shapes(q, k_cache, v_cache, block_table, context_lens, out):
 
 def decode(q, k_cache, v_cache, block_table, context_lens, scale=None, partition_tokens=0,
            workspace=None, out=None, stream=None):
-    """Paged decode attention; q [B][Hq][d] -> out [B][Hq][d]."""
+    """Paged decode attention (pa_decode): one query token per sequence.
+
+    q: [B][Hq][d]; k_cache, v_cache: [NB][Hkv][bs][d] (same dtype, bf16 or
+    fp32); block_table: int32 [B][max_blocks_per_seq]; context_lens: int32
+    [B], each in [1, max_blocks_per_seq * bs] and counting the newest token.
+    Query head h attends over KV head h // (Hq // Hkv).  scale defaults to
+    1/sqrt(d); partition_tokens (0 = 512) sets the split-KV partitions.
+    workspace (fp32 tensor of at least decode_workspace_size bytes) and out
+    ([B][Hq][d]) are allocated when not given.  Returns out.  Asynchronous on
+    `stream` (default: the current stream)."""
     _check_decode_shapes(q, k_cache, v_cache, block_table, context_lens, out)
     B, Hq, d = q.shape
     NB, Hkv, bs, _ = k_cache.shape
@@ -201,7 +217,14 @@ def decode_noalloc(q, k_cache, v_cache, block_table, context_lens, scale=None,
 
 def prefill_chunk(q, k_cache, v_cache, block_table, query_start, context_lens, max_query_len,
                   scale=None, out=None, stream=None):
-    """Causal chunked prefill; q [sum n][Hq][d] -> out [sum n][Hq][d] (bf16)."""
+    """Causal chunked prefill over paged context (pa_prefill_chunk), bf16.
+
+    R requests; request r owns query rows query_start[r] .. query_start[r+1]
+    of q [sum n][Hq][d], the chunk's newest tokens, whose K/V are already in
+    the pools.  context_lens: int32 [R], prior + new tokens; the query at
+    position P_r + i attends to positions 0 .. P_r + i.  block_table: int32
+    [R][max_blocks_per_seq]; max_query_len bounds the chunks' lengths.
+    Returns out [sum n][Hq][d]."""
     _require(q.dim() == 3 and k_cache.dim() == 4 and context_lens.dim() == 1,
              "q must be [tokens][Hq][d], pools [NB][Hkv][bs][d], context_lens [R]")
     Tq, Hq, d = q.shape

@@ -133,9 +133,13 @@ int pa_swap_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_
                    pa_stream_t stream);
 
 /*
- * pa_decode_workspace_size -- bytes of fp32 workspace pa_decode needs for
- * split-KV partials (0 when no sequence can span more than one partition).
- * partition_tokens as for pa_decode (0 = library default).
+ * pa_decode_workspace_size -- bytes of device workspace pa_decode needs: the
+ * split-KV merge tickets (4 bytes per (sequence, query head), padded to a
+ * multiple of 256 bytes) and the fp32 partials (max, sum and weighted values)
+ * of up to partitions-of-the-table-capacity + 1 segments per (sequence,
+ * query head).  Non-zero for every B > 0 (0 for B = 0).  partition_tokens as
+ * for pa_decode (0 = library default).  PA_ERR_INVALID on bad sizes or when
+ * the size does not fit in size_t.
  */
 int pa_decode_workspace_size(int B, int Hq, int head_dim, int max_blocks_per_seq,
                              int block_size, int partition_tokens, size_t *bytes);
@@ -181,8 +185,16 @@ int pa_decode_kernel_for(int B, int Hkv, int max_blocks_per_seq, int block_size,
  *   context_lens  int32 [B], each in [1, max_blocks_per_seq*block_size]
  *   partition_tokens  0 = default (512), or a positive multiple of both 32
  *                 and block_size
- *   workspace     device buffer of at least pa_decode_workspace_size bytes
- *                 (may be NULL when that size is 0)
+ *   workspace     device buffer of at least pa_decode_workspace_size bytes,
+ *                 16-byte aligned; its contents on entry do not matter (the
+ *                 call clears the tickets it uses, in a small kernel launched
+ *                 ahead of the decode grid) and it holds scratch afterwards.
+ *                 Calls that may overlap on the GPU need separate workspaces.
+ * Launches: a ticket-clearing kernel and the persistent decode grid, or the
+ * grid kernel and a merge kernel (pa_decode_kernel_for).  Each is launched as
+ * a programmatic dependent of the kernel before it in the stream: it may
+ * start while that kernel drains, and waits for that kernel to complete
+ * before it reads any input.
  */
 int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
               const int32_t *block_table, int max_blocks_per_seq, const int32_t *context_lens,

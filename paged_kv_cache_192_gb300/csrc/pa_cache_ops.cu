@@ -16,6 +16,12 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, uint4 *__restrict__ k_cache,
     uint4 *__restrict__ v_cache, const int64_t *__restrict__ slots, int64_t total, int Hkv,
     int bs_log2, int chunks, int64_t num_blocks, int *err) {
+    // Launched as a programmatic dependent: wait for the kernels before it
+    // (they may still read the pool), then let the next kernel in the stream
+    // (typically the decode that reads these rows) start launching; that
+    // kernel waits for this grid to complete before it reads anything.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += stride) {
@@ -151,10 +157,21 @@ int pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cache, vo
     const int chunks = static_cast<int>(head_dim * es / 16);
     const int64_t total = T * Hkv * chunks;
     (void)cudaGetLastError();  // drop a stale error that is not ours
-    reshape_and_cache_kernel<<<grid_for(total, 256), 256, 0, stream>>>(
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, total, Hkv,
-        log2_int(block_size), chunks, num_blocks, pa::device_error_word());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_for(total, 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(
+        &cfg, reshape_and_cache_kernel, static_cast<const uint4 *>(k_new),
+        static_cast<const uint4 *>(v_new), static_cast<uint4 *>(k_cache),
+        static_cast<uint4 *>(v_cache), slot_mapping, total, Hkv, log2_int(block_size), chunks,
+        num_blocks, pa::device_error_word());
+    if (e != cudaSuccess) return pa::cuda_fail(e, "reshape_and_cache launch");
     return pa::check_launch("reshape_and_cache launch");
 }
 

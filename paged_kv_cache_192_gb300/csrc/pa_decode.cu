@@ -37,6 +37,7 @@
 #include <atomic>
 #include <cmath>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "pa_device.cuh"
@@ -122,13 +123,20 @@ struct DecodeParams {
     const int32_t *context_lens;
     float *ws_acc;               // [B][Hq][maxseg][D]
     float *ws_ml;                // [B][Hq][maxseg][2] (max, sum)
-    unsigned long long *ctr;     // [B][Hkv] tickets (persistent kernel)
+    unsigned *ctr;               // [B][Hkv] merge tickets, zeroed by decode_prep_kernel
     int *err;
     int64_t num_blocks;
     int B, Hq, Hkv, bs, bs_log2, MB, PT, max_parts, maxseg;
-    unsigned epoch;              // nonzero, new for every launch
     float qscale;                // scale * log2(e)
 };
+
+// Wait until the kernels this grid was launched behind (as a programmatic
+// dependent) have completed and their writes are visible; a no-op for a grid
+// launched without that attribute.  Every decode grid runs this before it
+// reads any input.
+__device__ __forceinline__ void wait_prior_grids() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -610,29 +618,16 @@ __device__ __forceinline__ void finish_segment(WarpAttn<T, D, GQ> &st, const Dec
     }
     // Release this warp's partial, take a ticket; the segment that completes
     // the item merges it.  The warp barrier orders every lane's stores before
-    // lane 0's (cumulative) release fence; nobody waits on anybody.
+    // lane 0's (cumulative) release fence; nobody waits on anybody.  The
+    // tickets start at zero in every launch (decode_prep_kernel).
     __syncwarp();
     int last = 0;
-    unsigned long long *ctr = p.ctr + static_cast<size_t>(c.b) * p.Hkv + c.hk;
+    unsigned *ctr = p.ctr + static_cast<size_t>(c.b) * p.Hkv + c.hk;
     if (lane == 0) {
         asm volatile("fence.acq_rel.gpu;" ::: "memory");
-        // ticket = (epoch << 32) | count; a stale epoch counts as zero.  Start
-        // from the value the previous launch leaves behind (0).
-        // A failed CAS means another segment's CAS succeeded, so at most
-        // nseg attempts are needed; the bound only guards against corruption.
-        unsigned long long assumed = 0ull;
-        unsigned cnt = 0;
-        bool done = false;
-        for (int tries = 0; tries < 4 * p.maxseg + 8 && !done; ++tries) {
-            const unsigned ep = static_cast<unsigned>(assumed >> 32);
-            cnt = ep == p.epoch ? static_cast<unsigned>(assumed) + 1u : 1u;
-            const unsigned long long old =
-                atomicCAS(ctr, assumed, (static_cast<unsigned long long>(p.epoch) << 32) | cnt);
-            done = old == assumed;
-            assumed = old;
-        }
-        if (!done) pa::record_error(p.err, PA_DEVERR_TIMEOUT);
-        last = done && cnt == static_cast<unsigned>(nseg);
+        const unsigned prev = atomicAdd(ctr, 1u);
+        if (prev >= static_cast<unsigned>(nseg)) pa::record_error(p.err, PA_DEVERR_TIMEOUT);
+        last = prev + 1u == static_cast<unsigned>(nseg);
         if (last) asm volatile("fence.acq_rel.gpu;" ::: "memory");
     }
     last = __shfl_sync(pa::kFull, last, 0);
@@ -640,7 +635,6 @@ __device__ __forceinline__ void finish_segment(WarpAttn<T, D, GQ> &st, const Dec
     __syncwarp();
     if (nseg > 32) {
         merge_many<T, D, GQ>(p, hq0, nseg, lane);
-        if (lane == 0) atomicExch(ctr, 0ull);
         return;
     }
     // Merge (up to 32 segments): lane s < nseg holds segment s's (max, sum) per head; every lane
@@ -695,7 +689,6 @@ __device__ __forceinline__ void finish_segment(WarpAttn<T, D, GQ> &st, const Dec
                 store_pair<T>(out + (hq0 + hb + hh) * D + EL * lane + e, accm[hh][e] * inv[hh],
                               accm[hh][e + 1] * inv[hh]);
     }
-    if (lane == 0) atomicExch(ctr, 0ull);
 }
 
 template <typename T, int D, int GQ>
@@ -711,6 +704,7 @@ __global__ void __launch_bounds__(kWarps * 32, (Cfg<T, D, GQ>::MINB))
     int *scan = reinterpret_cast<int *>(smem + C::OFF_FLAG);
     int32_t *pre = reinterpret_cast<int32_t *>(smem + C::OFF_BT);  // [B+1] tile prefix
     int32_t *lens = pre + p.B + 1;                                  // [B]
+    wait_prior_grids();  // inputs and zeroed tickets are ready past this point
 
     // ---- tiles per sequence and their prefix sums (whole CTA) ---------------
     const int cap = p.MB << p.bs_log2;
@@ -841,6 +835,7 @@ __global__ void __launch_bounds__(kWarps * 32, (Cfg<T, D, GQ>::MINB)) decode_ker
 
     const int part = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int cap = p.MB << p.bs_log2;
+    wait_prior_grids();
     int L = p.context_lens[b];
     if (L > cap || L < 0) {
         if (threadIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
@@ -1056,12 +1051,35 @@ bool partition_ok(int pt, int bs) {
     return pt > 0 && pt <= kMaxPartition && pt % 32 == 0 && pt % bs == 0;
 }
 
-std::atomic<unsigned> g_epoch{0};
+// Zero the merge tickets of the persistent kernel that follows it in the
+// stream.  It waits for the kernels before it first (the workspace may still
+// be in use by them), lets the decode grid launch at once (that grid waits
+// for this one to complete before it reads anything), then clears.
+__global__ void __launch_bounds__(256) decode_prep_kernel(unsigned *ctr, int64_t n) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    wait_prior_grids();
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += int64_t(gridDim.x) * blockDim.x)
+        ctr[i] = 0u;
+}
 
-unsigned next_epoch() {
-    unsigned e = ++g_epoch;
-    while (e == 0) e = ++g_epoch;
-    return e;
+// Launch `kern` as a programmatic dependent of the previous kernel in the
+// stream: its CTAs may start while that kernel drains and wait for it with
+// griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 int sm_count() {
@@ -1093,7 +1111,12 @@ int launch_persistent(const DecodeParams &p, cudaStream_t stream) {
     const int sms = sm_count();
     if (sms <= 0) return pa::fail(PA_ERR_CUDA, "decode: no SM count");
     const int grid = sms * std::max(per_sm, 1);
-    kern<<<grid, kWarps * 32, smem, stream>>>(p);
+    const int64_t nt = int64_t(p.B) * p.Hkv;
+    const int prep_grid = static_cast<int>(std::min<int64_t>((nt + 255) / 256, sms));
+    e = launch_dependent(decode_prep_kernel, dim3(prep_grid), dim3(256), 0, stream, p.ctr, nt);
+    if (e != cudaSuccess) return pa::cuda_fail(e, "decode prep launch");
+    e = launch_dependent(kern, dim3(grid), dim3(kWarps * 32), smem, stream, p);
+    if (e != cudaSuccess) return pa::cuda_fail(e, "decode launch");
     return pa::check_launch("decode launch");
 }
 
@@ -1106,23 +1129,13 @@ int launch_grid(const DecodeParams &p, cudaStream_t stream) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return pa::cuda_fail(e, "decode: shared memory attribute");
-    dim3 grid(p.max_parts, p.Hkv, p.B);
-    kern<<<grid, kWarps * 32, smem, stream>>>(p);
+    // both launches are programmatic dependents: the decode grid's launch
+    // overlaps the previous kernel's tail, the merge kernel's the decode's
+    e = launch_dependent(kern, dim3(p.max_parts, p.Hkv, p.B), dim3(kWarps * 32), smem, stream, p);
+    if (e != cudaSuccess) return pa::cuda_fail(e, "decode launch");
     if (int rc = pa::check_launch("decode launch")) return rc;
     if (p.max_parts > 1) {
-        // programmatic dependent launch: the merge kernel's launch overlaps
-        // the end of decode_kernel instead of following its completion
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(p.Hq, p.B);
-        cfg.blockDim = dim3(D);
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, merge_kernel<T, D>, p);
+        e = launch_dependent(merge_kernel<T, D>, dim3(p.Hq, p.B), dim3(D), 0, stream, p);
         if (e != cudaSuccess) return pa::cuda_fail(e, "decode merge launch");
         if (int rc = pa::check_launch("decode merge launch")) return rc;
     }
@@ -1171,14 +1184,34 @@ int dispatch_gq(int gq, const DecodeParams &p, cudaStream_t s) {
     }
 }
 
-// Workspace: tickets [B][Hq] (u64), then acc [B][Hq][maxseg][D], then
-// (max, sum) [B][Hq][maxseg][2]; maxseg = partitions per sequence + 1 bounds
-// the segments of one item in the persistent kernel and the partitions of the
-// grid kernel.
-size_t workspace_bytes_for(int B, int Hq, int D, int maxseg) {
-    if (B <= 0) return 0;
-    return static_cast<size_t>(B) * Hq *
-           (sizeof(unsigned long long) + static_cast<size_t>(maxseg) * (D + 2) * sizeof(float));
+// Workspace layout: merge tickets u32 [B][Hq] (the persistent kernel uses
+// [B][Hkv] of them) padded to a multiple of 256 bytes, then acc fp32
+// [B][Hq][maxseg][D], then (max, sum) fp32 [B][Hq][maxseg][2]; maxseg =
+// partitions per sequence + 1 bounds the segments of one item in the
+// persistent kernel and the partitions of the grid kernel.  The padding keeps
+// the fp32 regions 256-byte aligned whatever B*Hq is (the merge reads them as
+// float4).  Every product is checked: false when the size does not fit size_t.
+constexpr size_t kWsAlign = 256;
+struct WsLayout {
+    size_t ticket_bytes, acc_bytes, ml_bytes, total;
+};
+
+bool workspace_layout(int64_t B, int64_t Hq, int64_t D, int64_t maxseg, WsLayout *l) {
+    *l = WsLayout{0, 0, 0, 0};
+    if (B <= 0) return true;
+    size_t rows, tick, acc, ml, t;
+    if (__builtin_mul_overflow(static_cast<size_t>(B), static_cast<size_t>(Hq), &rows) ||
+        __builtin_mul_overflow(rows, sizeof(unsigned), &tick) ||
+        __builtin_add_overflow(tick, kWsAlign - 1, &tick))
+        return false;
+    tick -= tick % kWsAlign;
+    if (__builtin_mul_overflow(rows, static_cast<size_t>(maxseg), &rows) ||
+        __builtin_mul_overflow(rows, static_cast<size_t>(D) * sizeof(float), &acc) ||
+        __builtin_mul_overflow(rows, 2 * sizeof(float), &ml) ||
+        __builtin_add_overflow(tick, acc, &t) || __builtin_add_overflow(t, ml, &t))
+        return false;
+    *l = WsLayout{tick, acc, ml, t};
+    return true;
 }
 
 }  // namespace
@@ -1196,8 +1229,11 @@ int pa_decode_workspace_size(int B, int Hq, int head_dim, int max_blocks_per_seq
     if (!partition_ok(pt, block_size))
         return pa::fail(PA_ERR_INVALID, "workspace_size: bad partition_tokens %d", pt);
     const int64_t cap = int64_t(max_blocks_per_seq) * block_size;
-    const int maxseg = static_cast<int>((cap + pt - 1) / pt) + 1;
-    *bytes = workspace_bytes_for(B, Hq, head_dim, maxseg);
+    const int64_t maxseg = (cap + pt - 1) / pt + 1;
+    WsLayout l;
+    if (!workspace_layout(B, Hq, head_dim, maxseg, &l))
+        return pa::fail(PA_ERR_INVALID, "workspace_size: size does not fit in size_t");
+    *bytes = l.total;
     return PA_OK;
 }
 
@@ -1252,7 +1288,10 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
         return pa::fail(PA_ERR_INVALID, "decode: q, out and pools must be 16-byte aligned");
     const int64_t cap = int64_t(max_blocks_per_seq) * block_size;
     const int max_parts = static_cast<int>((cap + pt - 1) / pt);
-    const size_t need = workspace_bytes_for(B, Hq, head_dim, max_parts + 1);
+    WsLayout wl;
+    if (!workspace_layout(B, Hq, head_dim, int64_t(max_parts) + 1, &wl))
+        return pa::fail(PA_ERR_INVALID, "decode: workspace size does not fit in size_t");
+    const size_t need = wl.total;
     if (need > workspace_bytes || !workspace)
         return pa::fail(PA_ERR_INVALID, "decode: workspace needs %zu bytes, got %zu", need,
                         workspace_bytes);
@@ -1283,9 +1322,10 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     p.v_cache = static_cast<const uint8_t *>(v_cache);
     p.block_table = block_table;
     p.context_lens = context_lens;
-    p.ctr = static_cast<unsigned long long *>(workspace);
-    p.ws_acc = reinterpret_cast<float *>(p.ctr + size_t(B) * Hq);
-    p.ws_ml = p.ws_acc + size_t(B) * Hq * (max_parts + 1) * head_dim;
+    p.ctr = static_cast<unsigned *>(workspace);
+    p.ws_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + wl.ticket_bytes);
+    p.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) + wl.ticket_bytes +
+                                        wl.acc_bytes);
     p.err = pa::device_error_word();
     p.num_blocks = num_blocks;
     p.B = B;
@@ -1297,7 +1337,6 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     p.PT = pt;
     p.max_parts = max_parts + 1;  // slot stride of both kernels
     p.maxseg = max_parts + 1;
-    p.epoch = next_epoch();
     p.qscale = scale * kLog2e;
     const int gq = Hq / Hkv;
     if (dtype == PA_BF16)
@@ -1324,8 +1363,9 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
 // device (with that device current) looks up its address with
 // cudaGetSymbolAddress and caches it; make that first call before any stream
 // capture.  All calls on a device share the array and it keeps the contents
-// of the last call; nothing in it needs to start at zero (every partial is
-// written before it is read in the same call).  Calls that overlap on the GPU
+// of the last call; nothing in it needs to start at zero (the merge tickets
+// are cleared by each call before use, and every partial is written before
+// it is read in the same call).  Calls that overlap on the GPU
 // (different streams, or host threads racing) race on the array: serialize
 // them.
 // ---------------------------------------------------------------------------

@@ -75,3 +75,61 @@ def kv_utilization(lens, block_size, reserve_len=None):
     if reserve_len is not None:
         contiguous = used / float(len(lens) * int(reserve_len))
     return paged, contiguous
+
+
+def place_prefix_forks(pf, bm_seed, extra_blocks=None):
+    """Run the fork step of a shared-prefix batch through the native block
+    manager and return where everything lands.
+
+    The system prompt is added once; every user forks it (its prompt blocks
+    are shared, refcount B+1) and appends its private history except the
+    newest token; the parents each fork a child; then every sequence appends
+    one token in ascending id order (users, then children), so a parent whose
+    last block is partly filled takes the copy-on-write copy of it and its
+    child writes into the shared original ("Apa itu PagedAttention?", section
+    "Cara kerja PagedAttention", item 3).
+
+    Returns a dict: num_blocks, table [B+forks][MB] int32, lens [B+forks],
+    pairs (copy-on-write (src, dst) list), prompt_slots [P], hist_rows and
+    hist_slots (the users' private histories: rows of ``pf.base.k`` and their
+    slots), new_slots [B+forks] and the new rows k_new/v_new [B+forks][Hkv][d].
+    """
+    import torch
+
+    from .block_manager import BlockManager
+    w = pf.base
+    P, suffix, bs = w.extra["prefix"], w.extra["suffix"], w.bs
+    B, nf = w.B, len(pf.parents)
+    offs = w.kv_offsets
+    need = P // bs + sum(-(-int(x) // bs) for x in suffix)
+    NB = int(np.ceil(1.2 * need)) + (2 * nf if extra_blocks is None else extra_blocks)
+    bm = BlockManager(NB, bs, seed=bm_seed)
+    system = 1 << 40
+    prompt_slots = bm.add_seq(system, P)
+    hist_slots, hist_rows = [], []
+    for s_ in range(B):
+        bm.fork(system, s_)
+        sl, _ = bm.append_n(s_, int(suffix[s_]) - 1)
+        hist_slots.append(sl)
+        hist_rows.append(np.arange(offs[s_] + P, offs[s_] + w.lens[s_] - 1))
+    children = [(1 << 41) + i for i in range(nf)]
+    for par, ch in zip(pf.parents, children):
+        bm.fork(int(par), ch)
+    order = list(range(B)) + children
+    new_slots, pairs = [], []
+    for seq in order:
+        slot, a, b = bm.append(seq)
+        new_slots.append(slot)
+        if a >= 0:
+            pairs.append((a, b))
+    MB = max(len(bm.seq_blocks(s_)) for s_ in order)
+    last = torch.from_numpy(offs + w.lens - 1)
+    out = dict(num_blocks=NB, table=bm.block_table(order, MB),
+               lens=np.array([bm.seq_len(s_) for s_ in order], dtype=np.int64),
+               pairs=pairs, prompt_slots=prompt_slots,
+               hist_rows=np.concatenate(hist_rows).astype(np.int64),
+               hist_slots=np.concatenate(hist_slots).astype(np.int64),
+               new_slots=np.asarray(new_slots, dtype=np.int64),
+               k_new=torch.cat([w.k[last], pf.k_child]),
+               v_new=torch.cat([w.v[last], pf.v_child]), bm=bm)
+    return out

@@ -204,6 +204,59 @@ def prefix_workload(seed=0, B=None, prefix=None, suffix_range=None, device="cpu"
     return w
 
 
+@dataclass
+class PrefixForks:
+    """The shared-prefix batch at its fork step (parallel sampling).
+
+    ``base`` is the pre-fork batch of prefix_workload: B users sharing one
+    system prompt, each with a private suffix whose last token is the newest
+    one.  ``parents`` (seeded, sorted) each fork one child; every child then
+    appends its own new token (``k_child``/``v_child``, query ``q_child``)
+    while its parent appends the parent's newest token.  Child i's logical
+    history is therefore its parent's history without the newest token,
+    followed by the child's own token.
+    """
+
+    base: Workload
+    parents: np.ndarray          # [forks] user index of each child's parent
+    k_child: torch.Tensor        # [forks][Hkv][d]
+    v_child: torch.Tensor
+    q_child: torch.Tensor        # [forks][Hq][d]
+
+    def logical(self) -> Workload:
+        """All B + forks sequences (users, then children) as one decode batch
+        of logical histories; ``table`` is left empty (the block manager
+        places the blocks)."""
+        w = self.base
+        offs = w.kv_offsets
+        ks, vs, lens = [w.k], [w.v], list(w.lens)
+        for i, par in enumerate(self.parents):
+            lo, n = int(offs[par]), int(w.lens[par])
+            ks += [w.k[lo:lo + n - 1], self.k_child[i:i + 1]]
+            vs += [w.v[lo:lo + n - 1], self.v_child[i:i + 1]]
+            lens.append(n)
+        return Workload("prefix-forks", w.Hq, w.Hkv, w.d, w.bs, w.dtype,
+                        np.asarray(lens, dtype=np.int64), np.ones(len(lens), np.int64),
+                        torch.cat([w.q, self.q_child]), torch.cat(ks), torch.cat(vs),
+                        np.zeros((len(lens), 0), dtype=np.int32), 0)
+
+
+def prefix_fork_workload(seed=0, B=None, forks=None, device="cpu"):
+    """Shared-prefix batch plus its fork step: ``forks`` parents drawn with
+    numpy PCG64(seed+6) without replacement; the children's new K/V rows and
+    queries from a torch generator seeded with seed+7, N(0,1) rounded to the
+    config's dtype."""
+    cfg = CONFIGS["prefix"]
+    w = prefix_workload(seed=seed, B=B, device=device)
+    nf = cfg["forks"] if forks is None else forks
+    parents = np.sort(np.random.default_rng(seed + 6).choice(w.B, size=nf, replace=False))
+    gen = torch.Generator().manual_seed(seed + 7)
+    k_child = _values((nf, w.Hkv, w.d), w.dtype, gen, device)
+    v_child = _values((nf, w.Hkv, w.d), w.dtype, gen, device)
+    q_child = _values((nf, w.Hq, w.d), w.dtype, gen, device)
+    return PrefixForks(w, parents, k_child, v_child, q_child)
+
+
 def mixed_workload(seed=0, B=None, R=None, chunk=None, priors=None, device="cpu"):
     """Continuous batch: B decode sequences plus R chunked-prefill requests.
 

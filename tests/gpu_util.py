@@ -45,3 +45,11 @@ def oracle_decode(w, seqs=None, nthreads=None):
     v = torch.cat(vs).double().numpy()
     q = w.q[torch.from_numpy(seqs)].double().numpy()
     return oracle.decode(q, k, v, w.lens[seqs], 1.0 / np.sqrt(w.d), nthreads)
+
+
+def oracle_decode_all(w, chunk=8, nthreads=None):
+    """fp64 oracle for every sequence of the batch, a few sequences at a time
+    (bounds the host memory of the float64 copies of long histories)."""
+    parts = [oracle_decode(w, np.arange(i, min(i + chunk, w.B)), nthreads)
+             for i in range(0, w.B, chunk)]
+    return np.concatenate(parts)

@@ -42,13 +42,35 @@ def test_version(lib):
     assert lib.pa_version() == 1
 
 
+def _ticket_bytes(rows):
+    return -(-rows * 4 // 256) * 256
+
+
 def test_workspace_size_host_only(lib):
     from paged_kv_cache_192_gb300 import ops
     # 8B-shaped: 64 seqs, 32 heads, d 128, 256 blocks of 16 -> 8 partitions of
-    # 512 + 1 segment slots per (sequence, head), plus one 8-byte ticket each
-    assert ops.decode_workspace_size(64, 32, 128, 256, 16, 512) == 64 * 32 * (8 + 9 * 130 * 4)
-    assert ops.decode_workspace_size(4, 4, 64, 4, 16, 0) == 4 * 4 * (8 + 2 * 66 * 4)
+    # 512 + 1 segment slots per (sequence, head), after a 4-byte ticket per
+    # (sequence, head) padded to a multiple of 256 bytes
+    assert ops.decode_workspace_size(64, 32, 128, 256, 16, 512) == (
+        _ticket_bytes(64 * 32) + 64 * 32 * 9 * 130 * 4)
+    assert ops.decode_workspace_size(4, 4, 64, 4, 16, 0) == _ticket_bytes(16) + 16 * 2 * 66 * 4
     assert ops.decode_workspace_size(0, 4, 64, 4, 16, 0) == 0
+    # odd B x Hq: the fp32 partials still start 256 bytes into the buffer
+    assert ops.decode_workspace_size(5, 3, 128, 8, 16, 64) == 256 + 15 * 3 * 130 * 4
+
+
+def test_workspace_size_overflow_is_rejected(lib):
+    """Sizes whose workspace does not fit in size_t are refused, not wrapped
+    into a small number that a caller (or the fixed no-alloc scratch) would
+    accept."""
+    out = ctypes.c_size_t(0)
+    big = 2 ** 31 - 1
+    rc = lib.pa_decode_workspace_size(big, big, 128, 2 ** 26, 16, 32, ctypes.byref(out))
+    assert rc == 1 and b"size_t" in lib.pa_last_error_string()
+    # the largest table capacity (2^30 tokens) at the largest batch pa_decode
+    # takes still fits
+    assert lib.pa_decode_workspace_size(65535, 8, 128, 2 ** 26, 16, 32, ctypes.byref(out)) == 0
+    assert out.value > 2 ** 40
 
 
 @pytest.mark.parametrize("kw,code", [

@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import compare, device_inputs, oracle_decode
+from gpu_util import compare, device_inputs, oracle_decode, oracle_decode_all
 from paged_kv_cache_192_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -29,7 +29,8 @@ def kernel_of(w, partition_tokens=0):
 
 def run(w, partition_tokens=0, seqs=None, poison=True, kernel=None):
     """Decode the batch on the GPU and the oracle; `kernel` ("persistent" or
-    "grid") asserts which decode kernel the batch runs on."""
+    "grid") asserts which decode kernel the batch runs on.  With seqs=None
+    every sequence is compared."""
     if kernel is not None:
         assert kernel_of(w, partition_tokens) == kernel
     k_cache, v_cache, table, lens = device_inputs(w, DEV, poison)
@@ -38,8 +39,10 @@ def run(w, partition_tokens=0, seqs=None, poison=True, kernel=None):
     torch.cuda.synchronize()
     assert ops().device_error() == 0
     got = out.double().cpu().numpy()
-    ref = oracle_decode(w, seqs)
-    if seqs is not None:
+    if seqs is None:
+        ref = oracle_decode_all(w)
+    else:
+        ref = oracle_decode(w, seqs)
         got = got[np.asarray(seqs)]
     return got, ref, out
 
@@ -60,13 +63,12 @@ def test_8b_config_full_size():
     compare(got, ref, torch.bfloat16, "8b")
 
 
-def test_70b_config_full_size_sampled():
-    """Llama-3-70B-shaped long context (L ~ U[16k,32k], 64/8 heads, 32-token
-    blocks, 512-token partitions); the GPU runs the full batch, the oracle
-    checks 3 seeded sequences element by element."""
+def test_70b_config_full_size():
+    """Llama-3-70B-shaped long context (32 sequences, L ~ U[16k,32k], 64/8
+    heads, 32-token blocks, 512-token partitions): every output element of
+    all 32 sequences against the oracle."""
     w = synth.decode_workload("70b", seed=0)
-    seqs = synth.sample_indices(w.B, 3, seed=0)
-    got, ref, _ = run(w, partition_tokens=512, seqs=seqs, kernel="persistent")
+    got, ref, _ = run(w, partition_tokens=512, kernel="persistent")
     compare(got, ref, torch.bfloat16, "70b")
 
 
@@ -249,9 +251,97 @@ def test_shared_prefix_equals_private_copies():
 
 
 def test_prefix_config_full_size():
-    """Shared-prefix config: 256 sequences, 1024 shared tokens, suffix ~U[1,512];
-    oracle on 16 sampled sequences."""
+    """Shared-prefix config before its forks: 256 sequences, 1024 shared
+    tokens, suffix ~U[1,512]; every sequence against the oracle."""
     w = synth.prefix_workload(seed=0)
-    seqs = synth.sample_indices(w.B, 16, seed=1)
-    got, ref, _ = run(w, seqs=seqs)
+    got, ref, _ = run(w)
     compare(got, ref, torch.bfloat16, "prefix")
+
+
+def test_prefix_fork_step_full_size():
+    """The shared-prefix config's defining step at full size: 256 users share a
+    1024-token prompt (refcount 257 on its blocks), 64 of them fork a child,
+    every sequence appends one token through the native block manager (parents
+    whose last block is partly filled take a copy-on-write copy), then
+    pa_copy_blocks, pa_reshape_and_cache of the 320 new tokens and pa_decode
+    of all 320 sequences.  Each child's newest token must be in its own
+    history and its parent's must not: every output against the oracle on the
+    logical histories ("Apa itu PagedAttention?", section "Cara kerja
+    PagedAttention", item 3; nalar.dev, section "Sharing blok dapat
+    menghindari duplikasi state KV")."""
+    from paged_kv_cache_192_gb300 import layout
+    pf = synth.prefix_fork_workload(seed=0)
+    w = pf.base
+    st = layout.place_prefix_forks(pf, bm_seed=5)
+    NB, P = st["num_blocks"], w.extra["prefix"]
+    k_cache, v_cache = layout.alloc_pools(NB, w.Hkv, w.bs, w.d, w.dtype, DEV)
+    ops().reshape_and_cache(w.k[:P].to(DEV), w.v[:P].to(DEV), k_cache, v_cache,
+                            torch.from_numpy(st["prompt_slots"]).to(DEV))
+    rows = torch.from_numpy(st["hist_rows"])
+    ops().reshape_and_cache(w.k[rows].to(DEV), w.v[rows].to(DEV), k_cache, v_cache,
+                            torch.from_numpy(st["hist_slots"]).to(DEV))
+    n_cow = sum(1 for par in pf.parents if int(w.lens[par]) % w.bs != 0)
+    assert len(st["pairs"]) == n_cow > 0
+    ops().copy_blocks(k_cache, v_cache, torch.tensor(st["pairs"], dtype=torch.int64, device=DEV))
+    ops().reshape_and_cache(st["k_new"].to(DEV), st["v_new"].to(DEV), k_cache, v_cache,
+                            torch.from_numpy(st["new_slots"]).to(DEV))
+    lw = pf.logical()
+    assert np.array_equal(lw.lens, st["lens"])
+    q = lw.q.to(DEV)
+    table = torch.from_numpy(st["table"]).to(DEV)
+    lens = torch.from_numpy(st["lens"].astype(np.int32)).to(DEV)
+    out = ops().decode(q, k_cache, v_cache, table, lens)
+    torch.cuda.synchronize()
+    assert ops().device_error() == 0
+    compare(out.double().cpu().numpy(), oracle_decode_all(lw), torch.bfloat16, "prefix forks")
+    # every prompt block is still shared by all 320 sequences (+ the prompt)
+    bm = st["bm"]
+    assert all(bm.refcount(b) == lw.B + 1 for b in st["table"][0, :P // w.bs])
+
+
+WORKSPACE_GARBAGE_SCRIPT = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1]); sys.path.insert(0, sys.argv[1] + "/tests")
+from gpu_util import compare, device_inputs, oracle_decode_all
+from paged_kv_cache_192_gb300 import ops, synth
+w = synth.decode_workload("8b", seed=0)
+assert ops.decode_kernel_for(w.B, w.Hkv, w.max_blocks, w.bs, 512) == "persistent"
+k_cache, v_cache, table, lens = device_inputs(w, "cuda")
+nbytes = ops.decode_workspace_size(w.B, w.Hq, w.d, w.max_blocks, w.bs, 512)
+ws = torch.full((nbytes // 8,), (1 << 32) | 7, dtype=torch.int64, device="cuda")
+ref = oracle_decode_all(w)
+for call in range(2):
+    out = ops.decode(w.q.to("cuda"), k_cache, v_cache, table, lens, partition_tokens=512,
+                     workspace=ws)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    compare(out.double().cpu().numpy(), ref, torch.bfloat16, "garbage workspace call %d" % call)
+    ws.fill_((1 << 32) | 7)
+print("ok")
+"""
+
+
+def test_workspace_contents_do_not_matter_fresh_process():
+    """A split batch (64 sequences of the 8B shape, items split over several
+    warps) decoded in a fresh process with every workspace word set to
+    (1 << 32) | 7 beforehand -- a stale 'ticket' pattern -- still matches the
+    oracle, twice: the call clears the tickets it uses before the decode grid
+    reads them."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", WORKSPACE_GARBAGE_SCRIPT, root], cwd=root,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
+
+
+@pytest.mark.parametrize("max_blocks,kernel", [(8, "grid"), (600, "persistent")])
+def test_odd_query_row_count(max_blocks, kernel):
+    """B x Hq odd (5 sequences x 3 query heads, 3 KV heads, d 128) with split
+    sequences on both kernels: the workspace's fp32 partials stay aligned for
+    the merge's vector loads whatever the number of tickets before them."""
+    lens = [1, 100, 127, 128, 128] if kernel == "grid" else [1, 100, 700, 2000, 5000]
+    w = synth.decode_workload("8b", seed=31, lens=lens, Hq=3, Hkv=3, max_blocks=max_blocks)
+    got, ref, _ = run(w, partition_tokens=64, kernel=kernel)
+    compare(got, ref, torch.bfloat16, f"odd rows {kernel}")

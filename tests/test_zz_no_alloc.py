@@ -5,7 +5,8 @@ a fixed array inside the library instead of a caller buffer.
 
 Called through the C ABI; its output must match pa_decode with a caller
 workspace, within the bf16 tolerance of the other tests, on two calls in a
-row (the second call reuses the array the first one left behind).  This file
+row (the second call reuses the array the first one left behind), and both
+must match the fp64 oracle.  This file
 is collected last so a failure here cannot hide the others; it also passes
 when run alone in a fresh process.
 """
@@ -16,7 +17,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import TOL, device_inputs
+from gpu_util import TOL, compare, device_inputs, oracle_decode_all
 from paged_kv_cache_192_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -57,6 +58,9 @@ def test_noalloc_matches_decode_twice(lib):
         got, exp = out.double().cpu().numpy(), ref.double().cpu().numpy()
         assert np.isfinite(got).all()
         assert np.all(np.abs(got - exp) <= atol + rtol * np.abs(exp))
+        oracle_out = oracle_decode_all(w)
+        compare(got, oracle_out, torch.bfloat16, "noalloc vs oracle")
+        compare(exp, oracle_out, torch.bfloat16, "decode vs oracle")
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch(lib):

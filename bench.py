@@ -244,13 +244,14 @@ def unique_kv_bytes(table, lens, bs, Hkv, d, es):
     return len(used) * Hkv * bs * d * es * 2
 
 
-def decode_kernel_info(B, Hkv, MB, bs, PT):
+def decode_kernel_info(B, Hq, Hkv, d, MB, bs, NB, PT):
     """(name of the decode kernel for the roofline line, launches of one
-    pa_decode) for a batch of these sizes."""
+    pa_decode) for a bf16 batch of these sizes."""
     from paged_kv_cache_192_gb300 import ops
     if ops.decode_kernel_for(B, Hkv, MB, bs, PT) == "persistent":
+        tile = ops.decode_tile_for(Hq, Hkv, d, bs, NB).replace("_", "-")
         return ("pa_decode (decode_prep_kernel clearing the merge tickets, then "
-                "decode_persistent_kernel with the split-KV merge inside)", 2)
+                f"decode_persistent_kernel, {tile} tile, split-KV merge inside)", 2)
     return "pa_decode (decode_kernel, then merge_kernel)", 2
 
 
@@ -295,7 +296,8 @@ class DecodePlan(Plan):
         self.outputs = {"out": torch.empty_like(self.inputs["q"])}
         self.PT = args.partition
         self.ws_bytes = ops.decode_workspace_size(w.B, w.Hq, w.d, w.max_blocks, w.bs, self.PT)
-        self.decode_kernel, n_dec = decode_kernel_info(w.B, w.Hkv, w.max_blocks, w.bs, self.PT)
+        self.decode_kernel, n_dec = decode_kernel_info(w.B, w.Hq, w.Hkv, w.d, w.max_blocks, w.bs,
+                                                        w.num_blocks, self.PT)
         self.ws = torch.zeros(max(self.ws_bytes // 4, 1), dtype=torch.float32, device=dev)
         self.decode_bytes = decode_bytes(w.lens, w.B, w.Hq, w.Hkv, w.d, w.bs, w.dtype)
         self.step_bytes = self.decode_bytes + store_bytes(w.B, w.Hkv, w.d, w.dtype)
@@ -373,7 +375,7 @@ class PrefixPlan(Plan):
         self.outputs = {"out": torch.empty_like(self.inputs["q"])}
         self.PT = args.partition
         self.ws_bytes = ops.decode_workspace_size(self.Bd, Hq, d, MB, bs, self.PT)
-        self.decode_kernel, n_dec = decode_kernel_info(self.Bd, Hkv, MB, bs, self.PT)
+        self.decode_kernel, n_dec = decode_kernel_info(self.Bd, Hq, Hkv, d, MB, bs, NB, self.PT)
         self.ws = torch.zeros(max(self.ws_bytes // 4, 1), dtype=torch.float32, device=dev)
         es = _es(w.dtype)
         self.decode_bytes = decode_bytes(lens, self.Bd, Hq, Hkv, d, bs, w.dtype)
@@ -468,7 +470,8 @@ class MixedPlan(Plan):
         self.PT = args.partition
         self.ws_bytes = ops.decode_workspace_size(dec.B, dec.Hq, dec.d, dec.max_blocks, dec.bs,
                                                   self.PT)
-        self.decode_kernel, n_dec = decode_kernel_info(dec.B, dec.Hkv, dec.max_blocks, dec.bs,
+        self.decode_kernel, n_dec = decode_kernel_info(dec.B, dec.Hq, dec.Hkv, dec.d,
+                                                       dec.max_blocks, dec.bs, dec.num_blocks,
                                                        self.PT)
         self.ws = torch.zeros(max(self.ws_bytes // 4, 1), dtype=torch.float32, device=dev)
         self.decode_bytes = decode_bytes(dec.lens, dec.B, dec.Hq, dec.Hkv, dec.d, dec.bs,

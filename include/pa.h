@@ -168,6 +168,26 @@ enum { PA_DECODE_PERSISTENT = 1, PA_DECODE_GRID = 2 };
 int pa_decode_kernel_for(int B, int Hkv, int max_blocks_per_seq, int block_size,
                          int partition_tokens, int *kernel);
 
+/* per-tile math of the persistent decode kernel (pa_decode_tile_for) */
+enum { PA_DECODE_TILE_CUDA_CORE = 1, PA_DECODE_TILE_TENSOR_CORE = 2 };
+
+/*
+ * pa_decode_tile_for -- how the persistent decode kernel computes a tile of
+ * one (sequence, KV head) for these shapes (the grid kernel always uses the
+ * CUDA-core tile):
+ *   PA_DECODE_TILE_TENSOR_CORE  bf16 with groups of 4 or 8 query heads per KV
+ *       head (and num_blocks * Hkv * block_size < 2^31): 16-token tiles by
+ *       2D tensor copies (128-byte swizzle); scores and the weighted sum of
+ *       values by warp-level bf16 tensor-core MMAs with fp32 accumulation
+ *       (the group's heads are the N = 8 columns; softmax weights enter as a
+ *       bf16 hi + lo pair);
+ *   PA_DECODE_TILE_CUDA_CORE    every other case: packed fp32 FMAs and warp
+ *       shuffles.
+ * Both meet the same error bound.  PA_ERR_INVALID on bad shapes.
+ */
+int pa_decode_tile_for(int Hq, int Hkv, int head_dim, int block_size, int64_t num_blocks,
+                       int dtype, int *tile);
+
 /*
  * pa_decode -- paged decode attention: one query token per sequence.
  * For sequence b with context length L = context_lens[b] (the newest token,

@@ -14,6 +14,7 @@ PA_OK, PA_ERR_INVALID, PA_ERR_OOM, PA_ERR_CUDA, PA_ERR_UNSUPPORTED, PA_ERR_DEVIC
 PA_BF16, PA_F32 = 0, 1
 PA_DEVERR_BAD_BLOCK, PA_DEVERR_TIMEOUT = 1, 2
 PA_DECODE_PERSISTENT, PA_DECODE_GRID = 1, 2
+PA_DECODE_TILE_CUDA_CORE, PA_DECODE_TILE_TENSOR_CORE = 1, 2
 
 _c_int, _c_i64, _c_sz, _c_vp, _c_f = (ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
                                       ctypes.c_void_p, ctypes.c_float)
@@ -37,6 +38,8 @@ SIGNATURES = {
                                           ctypes.POINTER(_c_sz)]),
     "pa_decode_kernel_for": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int,
                                       ctypes.POINTER(_c_int)]),
+    "pa_decode_tile_for": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_i64, _c_int,
+                                    ctypes.POINTER(_c_int)]),
     "pa_decode": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_int,
                            _c_int, _c_int, _c_int, _c_i64, _c_f, _c_int, _c_vp, _c_sz, _c_int,
                            _c_vp]),

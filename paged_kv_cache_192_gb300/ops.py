@@ -148,6 +148,16 @@ def decode_kernel_for(B, Hkv, max_blocks_per_seq, block_size, partition_tokens=0
     return {_lib.PA_DECODE_PERSISTENT: "persistent", _lib.PA_DECODE_GRID: "grid"}[out.value]
 
 
+def decode_tile_for(Hq, Hkv, head_dim, block_size, num_blocks, dtype=torch.bfloat16) -> str:
+    """Tile the persistent decode kernel uses for these shapes: "tensor_core"
+    (bf16, groups of 4 or 8 heads) or "cuda_core"."""
+    out = ctypes.c_int(0)
+    check(lib().pa_decode_tile_for(Hq, Hkv, head_dim, block_size, num_blocks,
+                                   _DTYPES[dtype], ctypes.byref(out)))
+    return {_lib.PA_DECODE_TILE_CUDA_CORE: "cuda_core",
+            _lib.PA_DECODE_TILE_TENSOR_CORE: "tensor_core"}[out.value]
+
+
 def _check_decode_shapes(q, k_cache, v_cache, block_table, context_lens, out):
     _require(q.dim() == 3 and k_cache.dim() == 4, "q must be [B][Hq][d], pools [NB][Hkv][bs][d]")
     B, Hq, d = q.shape

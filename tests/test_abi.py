@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from conftest import ROOT
 
@@ -146,3 +147,20 @@ def test_misaligned_pool_rejected(lib):
                                   ctypes.c_void_p(16), ctypes.c_void_p(16), 1, 8, 4, 16, 64, 0,
                                   None)
     assert rc == 1 and b"aligned" in lib.pa_last_error_string()
+
+
+def test_decode_tile_for_host_only(lib):
+    """The tensor-core tile serves bf16 groups of 4 and 8 heads; fp32, groups
+    of 1 and 2, and pools too large for 32-bit tensor-copy coordinates use the
+    CUDA-core tile (a host rule, no device needed)."""
+    from paged_kv_cache_192_gb300 import ops
+    assert ops.decode_tile_for(32, 8, 128, 16, 10358) == "tensor_core"   # 8B shape
+    assert ops.decode_tile_for(64, 8, 128, 32, 30000) == "tensor_core"   # 70B shape
+    assert ops.decode_tile_for(16, 2, 64, 8, 100) == "tensor_core"
+    assert ops.decode_tile_for(32, 8, 128, 16, 10358, torch.float32) == "cuda_core"
+    assert ops.decode_tile_for(8, 4, 128, 16, 100) == "cuda_core"
+    assert ops.decode_tile_for(4, 4, 128, 16, 100) == "cuda_core"
+    assert ops.decode_tile_for(32, 8, 128, 16, 2 ** 24) == "cuda_core"  # 2^31 pool rows
+    out = ctypes.c_int(0)
+    assert lib.pa_decode_tile_for(12, 8, 128, 16, 100, 0, ctypes.byref(out)) == 1
+    assert lib.pa_decode_tile_for(32, 8, 96, 16, 100, 0, ctypes.byref(out)) == 1

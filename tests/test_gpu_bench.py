@@ -28,7 +28,7 @@ def test_default_bench_line(capsys):
     e2e = j["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert j["gpu_launches"] == 3 * 20  # store, ticket clear, decode
-    assert "decode_persistent_kernel" in j["roofline"]["kernel"]
+    assert "decode_persistent_kernel, tensor-core tile" in j["roofline"]["kernel"]
     assert "sm_mhz" in j["clocks"] and "reasons" in j["clocks"]
     cb = j["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1

@@ -59,6 +59,7 @@ def test_8b_config_full_size():
     """Llama-3-8B-shaped: 64 sequences, L ~ U[128,4096], 32/8 heads, d 128, bf16,
     shuffled 1.2x pool; every output element against the oracle."""
     w = synth.decode_workload("8b", seed=0)
+    assert ops().decode_tile_for(w.Hq, w.Hkv, w.d, w.bs, w.num_blocks) == "tensor_core"
     got, ref, _ = run(w, kernel="persistent")
     compare(got, ref, torch.bfloat16, "8b")
 
@@ -68,6 +69,7 @@ def test_70b_config_full_size():
     heads, 32-token blocks, 512-token partitions): every output element of
     all 32 sequences against the oracle."""
     w = synth.decode_workload("70b", seed=0)
+    assert ops().decode_tile_for(w.Hq, w.Hkv, w.d, w.bs, w.num_blocks) == "tensor_core"
     got, ref, _ = run(w, partition_tokens=512, kernel="persistent")
     compare(got, ref, torch.bfloat16, "70b")
 
@@ -100,13 +102,14 @@ def test_shapes_ragged_persistent(dtype, d, Hq, Hkv, bs):
     compare(got, ref, dtype, f"ragged x3 d{d} {Hq}/{Hkv} bs{bs}")
 
 
-@pytest.mark.parametrize("B,kernel", [(4, "grid"), (64, "persistent")])
-def test_placement_invariance_bit_identical(B, kernel):
+@pytest.mark.parametrize("B,kernel,Hq", [(4, "grid", 32), (64, "persistent", 32),
+                                         (64, "persistent", 64)])
+def test_placement_invariance_bit_identical(B, kernel, Hq):
     """Two different physical placements of the same logical K/V give
     bit-identical outputs (the reduction order follows logical positions)
-    on both decode kernels."""
-    w1 = synth.decode_workload("8b", seed=5, B=B)
-    w2 = synth.decode_workload("8b", seed=5, B=B)
+    on both decode kernels and on the tensor-core tile (groups of 8)."""
+    w1 = synth.decode_workload("8b", seed=5, B=B, Hq=Hq)
+    w2 = synth.decode_workload("8b", seed=5, B=B, Hq=Hq)
     rng = np.random.default_rng(99)
     perm = rng.permutation(w2.num_blocks).astype(np.int32)
     w2.table = perm[w1.table]
@@ -200,13 +203,14 @@ def test_dominant_key_selects_its_value():
     compare(got, ref, torch.bfloat16, "dominant")
 
 
-@pytest.mark.parametrize("nseq,kernel", [(1, "grid"), (64, "persistent")])
-def test_bad_block_id_is_recorded_not_faulted(nseq, kernel):
+@pytest.mark.parametrize("nseq,kernel,Hq", [(1, "grid", 32), (64, "persistent", 32),
+                                             (64, "persistent", 64)])
+def test_bad_block_id_is_recorded_not_faulted(nseq, kernel, Hq):
     """An out-of-pool table entry is replaced by block 0 in the kernel and
     reported in the device error word (no out-of-bounds access), on both
-    decode kernels."""
+    decode kernels and on the tensor-core tile (groups of 8)."""
     from paged_kv_cache_192_gb300._lib import PA_DEVERR_BAD_BLOCK
-    w = synth.decode_workload("8b", seed=10, lens=[40] * nseq)
+    w = synth.decode_workload("8b", seed=10, lens=[40] * nseq, Hq=Hq)
     assert kernel_of(w) == kernel
     k_cache, v_cache, table, lens = device_inputs(w, DEV)
     table[0, 1] = w.num_blocks + 5

@@ -250,8 +250,8 @@ def decode_kernel_info(B, Hq, Hkv, d, MB, bs, NB, PT):
     from paged_kv_cache_192_gb300 import ops
     if ops.decode_kernel_for(B, Hkv, MB, bs, PT) == "persistent":
         tile = ops.decode_tile_for(Hq, Hkv, d, bs, NB).replace("_", "-")
-        return ("pa_decode (decode_prep_kernel clearing the merge tickets, then "
-                f"decode_persistent_kernel, {tile} tile, split-KV merge inside)", 2)
+        return (f"pa_decode (decode_persistent_kernel, {tile} tile, then "
+                "partial_merge_kernel merging split items)", 2)
     return "pa_decode (decode_kernel, then merge_kernel)", 2
 
 
@@ -374,8 +374,24 @@ class PrefixPlan(Plan):
             "pairs": torch.tensor(pairs if pairs else [[0, 0]], dtype=torch.int64, device=dev)}
         self.outputs = {"out": torch.empty_like(self.inputs["q"])}
         self.PT = args.partition
-        self.ws_bytes = ops.decode_workspace_size(self.Bd, Hq, d, MB, bs, self.PT)
-        self.decode_kernel, n_dec = decode_kernel_info(self.Bd, Hq, Hkv, d, MB, bs, NB, self.PT)
+        # every sequence takes the 1024-token system prompt from one group's
+        # shared blocks (the children's parent suffix blocks stay private reads)
+        self.shared = args.prefix_path == "shared"
+        Bd = B + nf
+        self.inputs.update({
+            "shared_len": torch.full((Bd,), P, dtype=torch.int32, device=dev),
+            "group_start": torch.tensor([0, Bd], dtype=torch.int32, device=dev),
+            "group_seqs": torch.arange(Bd, dtype=torch.int32, device=dev)})
+        self.P = P
+        if self.shared:
+            self.ws_bytes = ops.decode_shared_workspace_size(Bd, Hq, d, MB, bs, self.PT, P)
+            name, n_dec = decode_kernel_info(Bd, Hq, Hkv, d, MB, bs, NB, self.PT)
+            self.decode_kernel = ("pa_decode_shared (prefix_kernel: the shared prompt once per "
+                                  "KV head for all members on tensor cores; then " + name + ")")
+            n_dec += 1
+        else:
+            self.ws_bytes = ops.decode_workspace_size(Bd, Hq, d, MB, bs, self.PT)
+            self.decode_kernel, n_dec = decode_kernel_info(Bd, Hq, Hkv, d, MB, bs, NB, self.PT)
         self.ws = torch.zeros(max(self.ws_bytes // 4, 1), dtype=torch.float32, device=dev)
         es = _es(w.dtype)
         self.decode_bytes = decode_bytes(lens, self.Bd, Hq, Hkv, d, bs, w.dtype)
@@ -394,7 +410,9 @@ class PrefixPlan(Plan):
         self.config = {"B": self.Bd, "sequences": f"{B} sharing a {P}-token prompt + {nf} forks",
                        "suffix_len": "U[1,512]", "Hq": Hq, "Hkv": Hkv, "head_dim": d,
                        "block_size": bs, "pool_blocks": NB, "partition_tokens": self.PT,
-                       "cow_pairs": self.npairs}
+                       "cow_pairs": self.npairs,
+                       "decode": ("pa_decode_shared, one group of all sequences over the "
+                                  f"{P}-token prompt" if self.shared else "pa_decode")}
         self.oracle_sample = lambda n, seed, threads=None: time_oracle_decode(w, n, seed, threads)
 
     def run(self, i, L, sp, ev=None, src=None, dst=None):
@@ -409,11 +427,20 @@ class PrefixPlan(Plan):
                                      self.Hkv, self.bs, self.d, PA_BF16, sp))
         if ev:
             ev["decode"][0].record()
-        check(L.pa_decode((dst or self.outputs)["out"].data_ptr(), x["q"].data_ptr(), kc.data_ptr(),
-                          vc.data_ptr(), x["table"].data_ptr(), self.MB, x["lens"].data_ptr(),
-                          self.Bd, self.Hq, self.Hkv, self.d, self.bs, self.NB,
-                          1.0 / math.sqrt(self.d), self.PT, self.ws.data_ptr(), self.ws_bytes,
-                          PA_BF16, sp))
+        if self.shared:
+            check(L.pa_decode_shared(
+                (dst or self.outputs)["out"].data_ptr(), x["q"].data_ptr(), kc.data_ptr(),
+                vc.data_ptr(), x["table"].data_ptr(), self.MB, x["lens"].data_ptr(), self.Bd,
+                self.Hq, self.Hkv, self.d, self.bs, self.NB, 1.0 / math.sqrt(self.d), self.PT,
+                x["shared_len"].data_ptr(), x["group_start"].data_ptr(),
+                x["group_seqs"].data_ptr(), 1, self.Bd, self.Bd, self.P, self.ws.data_ptr(),
+                self.ws_bytes, PA_BF16, sp))
+        else:
+            check(L.pa_decode((dst or self.outputs)["out"].data_ptr(), x["q"].data_ptr(),
+                              kc.data_ptr(), vc.data_ptr(), x["table"].data_ptr(), self.MB,
+                              x["lens"].data_ptr(), self.Bd, self.Hq, self.Hkv, self.d, self.bs,
+                              self.NB, 1.0 / math.sqrt(self.d), self.PT, self.ws.data_ptr(),
+                              self.ws_bytes, PA_BF16, sp))
         if ev:
             ev["decode"][1].record()
 
@@ -796,6 +823,9 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0,
                     help="override the decode workload's batch size (small profiling cases "
                          "of the same shape)")
+    ap.add_argument("--prefix-path", choices=["shared", "plain"], default="shared",
+                    help="prefix workload: decode with the shared-prefix groups (pa_decode_shared) "
+                         "or every sequence whole (pa_decode)")
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pools", type=int, default=N_POOLS, help="pools rotated between steps")

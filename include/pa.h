@@ -134,7 +134,7 @@ int pa_swap_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_
 
 /*
  * pa_decode_workspace_size -- bytes of device workspace pa_decode needs: the
- * split-KV merge tickets (4 bytes per (sequence, query head), padded to a
+ * per-item partial counts (4 bytes per (sequence, query head), padded to a
  * multiple of 256 bytes) and the fp32 partials (max, sum and weighted values)
  * of up to partitions-of-the-table-capacity + 1 segments per (sequence,
  * query head).  Non-zero for every B > 0 (0 for B = 0).  partition_tokens as
@@ -206,21 +206,74 @@ int pa_decode_tile_for(int Hq, int Hkv, int head_dim, int block_size, int64_t nu
  *   partition_tokens  0 = default (512), or a positive multiple of both 32
  *                 and block_size
  *   workspace     device buffer of at least pa_decode_workspace_size bytes,
- *                 16-byte aligned; its contents on entry do not matter (the
- *                 call clears the tickets it uses, in a small kernel launched
- *                 ahead of the decode grid) and it holds scratch afterwards.
- *                 Calls that may overlap on the GPU need separate workspaces.
- * Launches: a ticket-clearing kernel and the persistent decode grid, or the
- * grid kernel and a merge kernel (pa_decode_kernel_for).  Each is launched as
- * a programmatic dependent of the kernel before it in the stream: it may
- * start while that kernel drains, and waits for that kernel to complete
- * before it reads any input.
+ *                 16-byte aligned; its contents on entry do not matter (every
+ *                 partial and per-item count is written before it is read)
+ *                 and it holds scratch afterwards.  Calls that may overlap on
+ *                 the GPU need separate workspaces.
+ * Launches: the decode grid (persistent or grid kernel, pa_decode_kernel_for)
+ * and a kernel that merges the partials of items split across warps or
+ * partitions.  Each is launched as a programmatic dependent of the kernel
+ * before it in the stream: it may start while that kernel drains, and waits
+ * for that kernel to complete before it reads any input.
  */
 int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
               const int32_t *block_table, int max_blocks_per_seq, const int32_t *context_lens,
               int B, int Hq, int Hkv, int head_dim, int block_size, int64_t num_blocks,
               float scale, int partition_tokens, void *workspace, size_t workspace_bytes,
               int dtype, pa_stream_t stream);
+
+/*
+ * pa_decode_shared -- pa_decode for a batch in which groups of sequences share
+ * the physical blocks of a common prefix: a system prompt, or the history of
+ * parallel-sampling branches forked from one parent.  A shared block is one
+ * physical copy that serves every sequence referencing it ("PagedAttention:
+ * memetakan blok KV logis ke memori fisik tidak kontigu", section "Sharing
+ * blok dapat menghindari duplikasi state KV"; "Apa itu PagedAttention?",
+ * section "Cara kerja PagedAttention", item 3).  Here the shared part is also
+ * READ once per (group, KV head): a prefix kernel streams the group's shared
+ * blocks once through shared memory and computes the attention partials
+ * (max, sum, weighted values) of every member's query heads against them on
+ * tensor cores; the decode then covers each member's private tokens only and
+ * merges the two parts by log-sum-exp.
+ * Same arguments and result as pa_decode (within the same error bound: the
+ * sums are taken in another order, so the bits may differ from pa_decode's),
+ * plus the groups:
+ *   shared_len    int32 [B] device: tokens at the start of sequence b covered by
+ *                 its group's shared blocks; a positive multiple of block_size
+ *                 below context_lens[b] for a member, 0 for a sequence in no
+ *                 group.  All members of a group have the same value and the
+ *                 same first shared_len / block_size block-table entries (the
+ *                 first member's row is read for the shared blocks).
+ *   group_start   int32 [G+1] device: the members of group g are
+ *                 group_seqs[group_start[g] .. group_start[g+1]).
+ *   group_seqs    int32 [num_members] device: batch rows of the members; a
+ *                 sequence belongs to at most one group.
+ *   G, num_members, max_group_size, max_shared_len: host ints bounding the
+ *                 arrays (max_group_size >= every group's size,
+ *                 max_shared_len >= every shared_len).
+ *   workspace     at least pa_decode_shared_workspace_size bytes.
+ * Validate mode checks every rule above.  Calls that cannot take the shared
+ * path (fp32, batches that pa_decode_kernel_for sends to the grid kernel,
+ * pools of 2^31 rows or more) decode every sequence whole, which gives the
+ * same result.  Launches: the prefix kernel, then pa_decode's two.
+ * Outside validate mode, a member whose own shared_len is not a positive
+ * multiple of block_size below its context length is decoded whole and
+ * PA_DEVERR_BAD_BLOCK is recorded; members that disagree with their group's
+ * first member (another shared_len or other shared blocks) give undefined
+ * output (PA_DEVERR_BAD_BLOCK is recorded for a differing shared_len; other
+ * blocks are only caught by validate mode).
+ */
+int pa_decode_shared_workspace_size(int B, int Hq, int head_dim, int max_blocks_per_seq,
+                                    int block_size, int partition_tokens, int max_shared_len,
+                                    size_t *bytes);
+int pa_decode_shared(void *out, const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_table, int max_blocks_per_seq,
+                     const int32_t *context_lens, int B, int Hq, int Hkv, int head_dim,
+                     int block_size, int64_t num_blocks, float scale, int partition_tokens,
+                     const int32_t *shared_len, const int32_t *group_start,
+                     const int32_t *group_seqs, int G, int num_members, int max_group_size,
+                     int max_shared_len, void *workspace, size_t workspace_bytes, int dtype,
+                     pa_stream_t stream);
 
 /*
  * pa_decode_noalloc -- pa_decode for callers that cannot allocate device

@@ -14,17 +14,19 @@
 //  * Default kernel (decode_persistent_kernel): a persistent grid of 2 CTAs
 //    of 4 warps per SM; every warp owns an equal, contiguous range of units across all
 //    items (perfect balance) and streams its tiles through its own ring of NST
-//    shared-memory stages.  One lane issues a bulk copy (cp.async.bulk,
-//    non-tensor TMA) per contiguous (block, KV head) piece of K and of V,
-//    completing on an mbarrier; the block-table entry of the next tile is
-//    loaded one tile ahead.  When a warp's range ends inside an item, the
+//    shared-memory stages.  One lane issues the copies of a tile, completing
+//    on an mbarrier: a bulk copy (cp.async.bulk, non-tensor TMA) per
+//    contiguous (block, KV head) piece, or 2D tensor copies with the 128-byte
+//    swizzle for the tensor-core tile; the block-table entry of the next tile
+//    is loaded one tile ahead.  When a warp's range ends inside an item, the
 //    item's ranges (segments) write partial (max, sum, acc) to the workspace
-//    and the last one to arrive (an atomic ticket; nobody waits) merges them
-//    by log-sum-exp: split-KV without a second launch.
+//    and partial_merge_kernel, a programmatic dependent launch, merges them
+//    by log-sum-exp (with the shared-prefix partials of pa_decode_shared).
 //  * Grid kernel for very large batches and for batches of little work
 //    (decode_kernel): one CTA per (sequence, KV head, partition), merged by
 //    merge_kernel, a programmatic dependent launch.
-//  * Per tile: a token row is split over G lanes in 16-byte chunks
+//  * Per tile, tensor-core tile (bf16, groups of 4 or 8 heads): see MmaAttn.
+//  * Per tile, CUDA-core tile: a token row is split over G lanes in 16-byte chunks
 //    (conflict-free shared loads); QK partial dots of S steps x GQ heads are
 //    reduced across the G lanes by a transpose-reduce (each round halves the
 //    values a lane carries), leaving each (token, head) score in one lane;
@@ -128,12 +130,15 @@ struct DecodeParams {
     const uint8_t *v_cache;
     const int32_t *block_table;
     const int32_t *context_lens;
-    float *ws_acc;               // [B][Hq][maxseg][D]
-    float *ws_ml;                // [B][Hq][maxseg][2] (max, sum)
-    unsigned *ctr;               // [B][Hkv] merge tickets, zeroed by decode_prep_kernel
+    float *ws_acc;               // [B][Hq][rowslots][D]
+    float *ws_ml;                // [B][Hq][rowslots][2] (max, sum)
+    unsigned *meta;              // [B][Hkv] partials per item (persistent kernel)
     int *err;
+    const int32_t *shared_len;   // [B] tokens covered by a shared-prefix partial, or NULL
     int64_t num_blocks;
     int B, Hq, Hkv, bs, bs_log2, MB, PT, max_parts, maxseg;
+    int rowslots;                // partial slots per (sequence, query head)
+    int pslot0, npfx;            // shared-prefix partials: slots pslot0 .. pslot0+npfx-1
     float qscale;                // scale * log2(e)
 };
 
@@ -476,7 +481,7 @@ struct MmaCfg {
     static constexpr int OFF_FLAG = OFF_BAR + kWarps * NST * 8;
     static constexpr int OFF_BT = OFF_FLAG + 16;
     static constexpr int KS = D / 16;           // k-steps of QK^T = m-tiles of PV
-    static_assert(D % 64 == 0 && GQ <= 8 && GQ % 2 == 0, "tensor-core tile shape");
+    static_assert(D % 64 == 0 && GQ <= 8 && 8 % GQ == 0, "tensor-core tile shape");
     static_assert(HALF % 1024 == 0 && STAGE % 1024 == 0, "swizzle atoms must stay aligned");
 };
 
@@ -525,6 +530,22 @@ struct MmaAttn {
                 const uint32_t *row = reinterpret_cast<const uint32_t *>(qb + g * D + 16 * k);
                 b0 = __ldg(row + t);
                 b1 = __ldg(row + t + 4);
+            }
+            qf[k][0] = b0;
+            qf[k][1] = b1;
+        }
+    }
+
+    // Column g of the products reads q row `row` (NULL: a zero column).
+    __device__ __forceinline__ void load_q_row(const __nv_bfloat16 *row, float qscale_) {
+        qscale = qscale_;
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+            uint32_t b0 = 0u, b1 = 0u;
+            if (row) {
+                const uint32_t *r = reinterpret_cast<const uint32_t *>(row + 16 * k);
+                b0 = __ldg(r + t);
+                b1 = __ldg(r + t + 4);
             }
             qf[k][0] = b0;
             qf[k][1] = b1;
@@ -610,7 +631,9 @@ struct MmaAttn {
 
     // Softmax sums of this lane's heads 2t, 2t+1 (reduced over the 8 lanes
     // of each column) into lh[0], lh[1].
-    __device__ __forceinline__ void reduce(float (&lh)[GQ]) const {
+    template <int N>
+    __device__ __forceinline__ void reduce(float (&lh)[N]) const {
+        static_assert(N >= 2, "two columns per lane");
         float l0 = lsum[0], l1 = lsum[1];
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
@@ -622,6 +645,7 @@ struct MmaAttn {
     }
 
     __device__ __forceinline__ void store_out(__nv_bfloat16 *outh, const float (&lh)[GQ]) {
+        static_assert(GQ % 2 == 0, "a lane's two columns are heads of one sequence");
         const float2 l = make_float2(lh[0], lh[1]);
         if (2 * t >= GQ) return;
         const float i0 = 1.f / l.x, i1 = 1.f / l.y;
@@ -638,6 +662,7 @@ struct MmaAttn {
     __device__ __forceinline__ void store_partial(float *acc_dst, size_t head_stride,
                                                   float *ml_dst, size_t ml_stride,
                                                   const float (&lh)[GQ]) {
+        static_assert(GQ % 2 == 0, "a lane's two columns are heads of one sequence");
         const float2 l = make_float2(lh[0], lh[1]);
         if (2 * t >= GQ) return;
         float *a0 = acc_dst + (2 * t) * head_stride + g, *a1 = a0 + head_stride;
@@ -661,13 +686,17 @@ struct MmaAttn {
 // ---------------------------------------------------------------------------
 struct Cursor {
     int b, hk, t, nt, L;  // item (b, hk), tile t of nt tiles, context length L
+    int s0;               // first token the item's tiles cover (shared prefix excluded)
 };
 
+__device__ __forceinline__ int first_token(const Cursor &c, int TT) { return c.s0 + c.t * TT; }
+
 // Tables of the persistent kernel in shared memory: tile prefix over the
-// sequences ([B+1]) and clamped context lengths ([B]).
+// sequences ([B+1]), clamped context lengths ([B]) and first tokens ([B]).
 struct BatchTables {
     const int32_t *pre;
     const int32_t *lens;
+    const int32_t *starts;
 };
 
 // Cursor at unit u: the largest b with Hkv*pre[b] <= u, then (hk, t).
@@ -682,6 +711,7 @@ __device__ __forceinline__ Cursor locate_unit(int64_t u, const BatchTables &bt, 
     c.b = lo;
     c.nt = bt.pre[lo + 1] - bt.pre[lo];
     c.L = bt.lens[lo];
+    c.s0 = bt.starts[lo];
     const int64_t rem = u - int64_t(Hkv) * bt.pre[lo];
     c.hk = static_cast<int>(rem / c.nt);
     c.t = static_cast<int>(rem - int64_t(c.hk) * c.nt);
@@ -700,6 +730,7 @@ __device__ __forceinline__ Cursor next_unit(Cursor c, const BatchTables &bt, int
             if (c.b < B) {
                 c.nt = bt.pre[c.b + 1] - bt.pre[c.b];
                 c.L = bt.lens[c.b];
+                c.s0 = bt.starts[c.b];
             }
         }
     }
@@ -708,7 +739,8 @@ __device__ __forceinline__ Cursor next_unit(Cursor c, const BatchTables &bt, int
 
 template <int TT>
 __device__ __forceinline__ int block_entry(const DecodeParams &p, const Cursor &c, int j) {
-    return __ldg(p.block_table + static_cast<size_t>(c.b) * p.MB + ((c.t * TT) >> p.bs_log2) + j);
+    return __ldg(p.block_table + static_cast<size_t>(c.b) * p.MB +
+                 (first_token(c, TT) >> p.bs_log2) + j);
 }
 
 __device__ __forceinline__ int checked_block(const DecodeParams &p, int v) {
@@ -726,7 +758,7 @@ __device__ __forceinline__ void produce_tile(const DecodeParams &p, const Cursor
     using C = Cfg<T, D, GQ>;
     uint8_t *dk = stage;
     uint8_t *dv = stage + C::TILE;
-    const int tok = c.t * C::TT;
+    const int tok = first_token(c, C::TT);
     if (C::TT <= p.bs) {
         const int r0 = tok & (p.bs - 1);
         const size_t off = ((static_cast<size_t>(blk) * p.Hkv + c.hk) * p.bs + r0) * C::ROW;
@@ -760,7 +792,7 @@ __device__ __forceinline__ void produce_tile_tma(const DecodeParams &p, const Cu
                                                  const CUtensorMap *vmap) {
     using C = MmaCfg<D, GQ>;
     const uint32_t sk = pa::smem_u32(stage), sv = sk + C::TILE;
-    const int tok = c.t * C::TT;
+    const int tok = first_token(c, C::TT);
     if (C::TT <= p.bs) {
         const int y = (blk * p.Hkv + c.hk) * p.bs + (tok & (p.bs - 1));
         pa::mbar_arrive_expect_tx(bar, 2 * C::TILE);
@@ -793,7 +825,7 @@ template <typename T, int D, int GQ>
 __device__ __forceinline__ void produce_tile_lanes(const DecodeParams &p, const Cursor &c, int blk,
                                                    uint8_t *stage, uint64_t *bar, int lane) {
     using C = Cfg<T, D, GQ>;
-    const int tok = c.t * C::TT;
+    const int tok = first_token(c, C::TT);
     const uint32_t sk = pa::smem_u32(stage);
 #pragma unroll
     for (int k = 0; k < C::TILE / 16 / 32; ++k) {
@@ -831,44 +863,18 @@ __device__ __forceinline__ void prefetch_q(const DecodeParams &p, const Cursor &
 // Merge of an item spread over more than 32 warps (a few very long
 // sequences): the weights are recomputed from loads instead of travelling
 // by shuffle.  Kept out of line so the common path's code is unaffected.
-template <typename T, int D, int GQ>
-__device__ __noinline__ void merge_many(const DecodeParams &p, size_t hq0, int nseg, int lane) {
-    constexpr int EL = D / 32;
-    T *out = static_cast<T *>(p.out);
-    for (int h = 0; h < GQ; ++h) {
-        const size_t sb = (hq0 + h) * p.maxseg;
-        const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + sb;
-        float M = -INFINITY;
-        for (int sg = lane; sg < nseg; sg += 32) M = fmaxf(M, __ldcg(&ml[sg]).x);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(pa::kFull, M, o));
-        float den = 0.f;
-        for (int sg = lane; sg < nseg; sg += 32) {
-            const float2 v = __ldcg(&ml[sg]);
-            den += exp2f(v.x - M) * v.y;
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(pa::kFull, den, o);
-        float acc[EL];
-#pragma unroll
-        for (int e = 0; e < EL; ++e) acc[e] = 0.f;
-        const float *src = p.ws_acc + sb * D + EL * lane;
-#pragma unroll 4
-        for (int sg = 0; sg < nseg; ++sg) {
-            const float f = exp2f(__ldcg(&ml[sg]).x - M);
-#pragma unroll
-            for (int e = 0; e < EL; ++e) acc[e] += f * __ldcg(src + sg * D + e);
-        }
-        const float inv = 1.f / den;
-#pragma unroll
-        for (int e = 0; e < EL; e += 2)
-            store_pair<T>(out + (hq0 + h) * D + EL * lane + e, acc[e] * inv, acc[e + 1] * inv);
-    }
+// Slot of the i-th partial of an item with nseg segments: its segments,
+// then the shared-prefix partials.
+__device__ __forceinline__ int slot_of(const DecodeParams &p, int i, int nseg) {
+    return i < nseg ? i : p.pslot0 + (i - nseg);
 }
 
-// End of this warp's segment of item c: write the output (the whole item is
-// in this warp's range) or a partial, and merge the item's partials if this
-// segment is the last of them to finish.
+// End of this warp's segment of item c.  An item that lies whole in this
+// warp's range (and has no shared-prefix partials) is written out directly;
+// otherwise the segment writes its partial (max, sum, unnormalised weighted
+// values) to its slot and partial_merge_kernel, launched behind this grid,
+// merges the item's partials.  The item's first segment records how many
+// there are.  No segment waits for, or signals, any other.
 template <typename T, int D, int GQ, typename St>
 __device__ __forceinline__ void finish_segment(St &st, const DecodeParams &p,
                                                const BatchTables &bt, const Cursor &c,
@@ -879,89 +885,181 @@ __device__ __forceinline__ void finish_segment(St &st, const DecodeParams &p,
     const int64_t wa = ia / per, wb = (ia + c.nt - 1) / per;
     const int nseg = static_cast<int>(wb - wa + 1), seg = static_cast<int>(w - wa);
     const size_t hq0 = static_cast<size_t>(c.b) * p.Hq + c.hk * GQ;
-    T *out = static_cast<T *>(p.out);
-    if (nseg == 1) {
-        st.store_out(out + hq0 * D, lh);
+    // an item that starts after a shared prefix also merges the prefix partials
+    const int npre = c.s0 > 0 ? p.npfx : 0;
+    const bool whole = nseg == 1 && npre == 0;
+    if (seg == 0 && lane == 0)
+        p.meta[static_cast<size_t>(c.b) * p.Hkv + c.hk] =
+            whole ? 0u : static_cast<unsigned>(nseg) | (static_cast<unsigned>(npre) << 16);
+    if (whole) {
+        st.store_out(static_cast<T *>(p.out) + hq0 * D, lh);
         return;
     }
     if (seg < 0 || seg >= p.maxseg) {  // cannot happen with maxseg from the host
         if (lane == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
         return;
     }
-    st.store_partial(p.ws_acc + (hq0 * p.maxseg + seg) * D, size_t(p.maxseg) * D,
-                     p.ws_ml + 2 * (hq0 * p.maxseg + seg), size_t(p.maxseg) * 2, lh);
-    // Release this warp's partial, take a ticket; the segment that completes
-    // the item merges it.  The warp barrier orders every lane's stores before
-    // lane 0's (cumulative) release fence; nobody waits on anybody.  The
-    // tickets start at zero in every launch (decode_prep_kernel).
-    __syncwarp();
-    int last = 0;
-    unsigned *ctr = p.ctr + static_cast<size_t>(c.b) * p.Hkv + c.hk;
-    if (lane == 0) {
-        asm volatile("fence.acq_rel.gpu;" ::: "memory");
-        const unsigned prev = atomicAdd(ctr, 1u);
-        if (prev >= static_cast<unsigned>(nseg)) pa::record_error(p.err, PA_DEVERR_TIMEOUT);
-        last = prev + 1u == static_cast<unsigned>(nseg);
-        if (last) asm volatile("fence.acq_rel.gpu;" ::: "memory");
-    }
-    last = __shfl_sync(pa::kFull, last, 0);
-    if (!last) return;
-    __syncwarp();
-    if (nseg > 32) {
-        merge_many<T, D, GQ>(p, hq0, nseg, lane);
+    st.store_partial(p.ws_acc + (hq0 * p.rowslots + seg) * D, size_t(p.rowslots) * D,
+                     p.ws_ml + 2 * (hq0 * p.rowslots + seg), size_t(p.rowslots) * 2, lh);
+}
+
+// ---------------------------------------------------------------------------
+// Shared-prefix partials (bf16, tensor core).  Members of a group share the
+// physical blocks of their first S tokens ("PagedAttention: memetakan blok KV
+// logis ke memori fisik tidak kontigu", section "Sharing blok dapat
+// menghindari duplikasi state KV": one physical copy serves every sequence
+// that references it), so those blocks are read once per (group, KV head,
+// token chunk, CTA of members) instead of once per member.  One CTA: a
+// loader warp streams 16-token K/V tiles of the chunk (2D tensor copies,
+// through the first member's block table) into a ring shared by
+// kPfxWarps consumer warps; each consumer runs the tensor-core tile with its
+// 8 columns = 8 / GQ members x GQ heads, and writes the chunk's partial
+// (max, sum, unnormalised weighted values) of every (member, head) to its
+// prefix slot.  The decode then covers only tokens S .. L-1 of each member
+// and merges these partials with its own by log-sum-exp.
+// ---------------------------------------------------------------------------
+#ifndef PA_PFX_WARPS
+#define PA_PFX_WARPS 8
+#endif
+#ifndef PA_PFX_STAGES
+#define PA_PFX_STAGES 4
+#endif
+constexpr int kPfxWarps = PA_PFX_WARPS;  // consumer warps per CTA (plus one loader warp)
+constexpr int kPfxNST = PA_PFX_STAGES;   // K/V ring stages shared by the CTA
+
+struct PrefixParams {
+    const int32_t *group_start;  // [G+1] member ranges into group_seqs
+    const int32_t *group_seqs;   // [num_members] batch rows of the members
+    int G, nc, num_members;      // groups, token chunks per group, group_seqs length
+};
+
+template <int D>
+constexpr size_t prefix_smem_bytes() {
+    return kPfxNST * MmaCfg<D, 8>::STAGE + 2 * kPfxNST * 8 + 16 + 1024;
+}
+
+template <int D, int GQ>
+__global__ void __launch_bounds__((kPfxWarps + 1) * 32)
+    prefix_kernel(const DecodeParams p, const PrefixParams pp,
+                  const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap vmap) {
+    using C = MmaCfg<D, GQ>;
+    constexpr int MPW = 8 / GQ;              // members per consumer warp
+    constexpr int MPC = kPfxWarps * MPW;     // members per CTA
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kPfxNST * C::STAGE);
+    uint64_t *empty = full + kPfxNST;
+    volatile int *fail = reinterpret_cast<volatile int *>(empty + kPfxNST);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hk = blockIdx.y, g = blockIdx.z / pp.nc, chunk = blockIdx.z % pp.nc;
+    wait_prior_grids();
+
+    int mbeg = pp.group_start[g], mend = pp.group_start[g + 1];
+    if (mbeg < 0 || mend > pp.num_members || mbeg > mend) {
+        if (threadIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
         return;
     }
-    // Merge (up to 32 segments): lane s < nseg holds segment s's (max, sum) per head; every lane
-    // owns D/32 output elements; all loads are independent (issued ahead).
-    // Heads go in groups of up to 4 so the accumulators stay in registers.
-    constexpr int EL = D / 32;
-    constexpr int HB = GQ < 4 ? GQ : 4;
-#pragma unroll 1
-    for (int hb = 0; hb < GQ; hb += HB) {
-        float wsh[HB], inv[HB], accm[HB][EL];
-#pragma unroll
-        for (int hh = 0; hh < HB; ++hh) {
-            const size_t sb = (hq0 + hb + hh) * p.maxseg;
-            float2 ml = make_float2(-INFINITY, 0.f);
-            if (lane < nseg)
-                ml = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + 2 * (sb + lane)));
-            float M = ml.x;
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(pa::kFull, M, o));
-            wsh[hh] = lane < nseg ? exp2f(ml.x - M) : 0.f;
-            float den = wsh[hh] * ml.y;
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(pa::kFull, den, o);
-            inv[hh] = 1.f / den;
-#pragma unroll
-            for (int e = 0; e < EL; ++e) accm[hh][e] = 0.f;
+    const int m0 = mbeg + blockIdx.x * MPC;
+    if (m0 >= mend) return;  // uniform over the CTA
+    // the first member's block-table row holds the shared blocks
+    const int b0 = pp.group_seqs[mbeg];
+    int S = 0;
+    if (b0 >= 0 && b0 < p.B) {
+        S = p.shared_len[b0];
+        const int L0 = p.context_lens[b0];
+        if (S < 0 || S >= L0 || (S & (p.bs - 1)) || S > (p.MB << p.bs_log2)) S = 0;
+    }
+    if (S == 0 && threadIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+    const int ch = ((S + 15) / 16 + pp.nc - 1) / pp.nc * 16;  // tokens per chunk
+    const int t_lo = min(S, chunk * ch), t_hi = min(S, t_lo + ch);
+    const int ntiles = (t_hi - t_lo + 15) / 16;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kPfxNST; ++i) {
+            pa::mbar_init(&full[i], 1);
+            pa::mbar_init(&empty[i], kPfxWarps);
         }
-        constexpr int kUnr = GQ >= 8 ? 2 : 4;
-#pragma unroll kUnr
-        for (int sgi = 0; sgi < nseg; ++sgi) {
-#pragma unroll
-            for (int hh = 0; hh < HB; ++hh) {
-                const float wv = __shfl_sync(pa::kFull, wsh[hh], sgi);
-                const float *src = p.ws_acc + ((hq0 + hb + hh) * p.maxseg + sgi) * D + EL * lane;
-                if constexpr (EL == 4) {
-                    const float4 a = __ldcg(reinterpret_cast<const float4 *>(src));
-                    accm[hh][0] += wv * a.x;
-                    accm[hh][1] += wv * a.y;
-                    accm[hh][2] += wv * a.z;
-                    accm[hh][3] += wv * a.w;
-                } else {
-                    const float2 a = __ldcg(reinterpret_cast<const float2 *>(src));
-                    accm[hh][0] += wv * a.x;
-                    accm[hh][1] += wv * a.y;
+        *fail = 0;
+        pa::fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kPfxWarps) {
+        // ---- loader ------------------------------------------------------
+        if (lane == 0 && ntiles > 0) {
+            Cursor c{b0, hk, 0, ntiles, t_hi, t_lo};
+            int issued = 0;
+            for (int i = 0; i < ntiles; ++i) {
+                const int st = i % kPfxNST;
+                if (i >= kPfxNST && !pa::mbar_wait(&empty[st], ((i / kPfxNST) - 1) & 1)) {
+                    pa::record_error(p.err, PA_DEVERR_TIMEOUT);
+                    *fail = 1;
+                    break;
                 }
+                c.t = i;
+                produce_tile_tma<D, GQ>(p, c, checked_block(p, block_entry<16>(p, c, 0)),
+                                        smem + st * C::STAGE, &full[st], &kmap, &vmap);
+                issued = i + 1;
             }
+            // every copy must have landed before the CTA may exit
+            for (int i = max(0, issued - kPfxNST); i < issued; ++i)
+                (void)pa::mbar_wait(&full[i % kPfxNST], (i / kPfxNST) & 1);
         }
+        return;
+    }
+
+    // ---- consumers ---------------------------------------------------------
+    MmaAttn<D, GQ> st;
+    st.init(lane);
+    st.reset();
+    // this lane's column g: member m0 + warp * MPW + g / GQ, head g % GQ
+    auto col_row = [&](int col) -> int64_t {
+        const int m = m0 + warp * MPW + col / GQ;
+        if (m >= mend) return -1;
+        const int b = pp.group_seqs[m];
+        if (b < 0 || b >= p.B || p.shared_len[b] != S || S == 0) {
+            pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);  // not a consistent member
+            return -1;
+        }
+        return static_cast<int64_t>(b) * p.Hq + hk * GQ + col % GQ;
+    };
+    const int64_t qrow = col_row(st.g);
+    st.load_q_row(qrow >= 0 ? static_cast<const __nv_bfloat16 *>(p.q) + qrow * D : nullptr,
+                  p.qscale);
+    for (int i = 0; i < ntiles; ++i) {
+        const int sti = i % kPfxNST;
+        const bool ok = __all_sync(pa::kFull, pa::mbar_wait(&full[sti], (i / kPfxNST) & 1));
+        if (!ok || *fail) {
+            if (lane == 0) pa::record_error(p.err, PA_DEVERR_TIMEOUT);
+            break;
+        }
+        const uint32_t kaddr = pa::smem_u32(smem + sti * C::STAGE);
+        st.tile(kaddr, kaddr + C::TILE, min(16, t_hi - (t_lo + 16 * i)), nullptr, nullptr);
+        __syncwarp();
+        if (lane == 0) {
+            pa::fence_proxy_async();
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(pa::smem_u32(&empty[sti]))
+                         : "memory");
+        }
+    }
+    // ---- partials of this lane's columns 2t, 2t+1 -----------------------------
+    float lh[2];
+    st.reduce(lh);
 #pragma unroll
-        for (int hh = 0; hh < HB; ++hh)
+    for (int j = 0; j < 2; ++j) {
+        const int64_t row = col_row(2 * st.t + j);
+        if (row < 0) continue;
+        const size_t slot = static_cast<size_t>(row) * p.rowslots + p.pslot0 + chunk;
+        float *a = p.ws_acc + slot * D + st.g;
 #pragma unroll
-            for (int e = 0; e < EL; e += 2)
-                store_pair<T>(out + (hq0 + hb + hh) * D + EL * lane + e, accm[hh][e] * inv[hh],
-                              accm[hh][e + 1] * inv[hh]);
+        for (int m = 0; m < C::KS; ++m) {
+            a[16 * m] = st.acc[m][j];
+            a[16 * m + 8] = st.acc[m][2 + j];
+        }
+        if (st.g == 0)
+            *reinterpret_cast<float2 *>(p.ws_ml + 2 * slot) = make_float2(st.m_run[j], lh[j]);
     }
 }
 
@@ -995,7 +1093,8 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
     int *scan = reinterpret_cast<int *>(smem + C::OFF_FLAG);
     int32_t *pre = reinterpret_cast<int32_t *>(smem + C::OFF_BT);  // [B+1] tile prefix
     int32_t *lens = pre + p.B + 1;                                  // [B]
-    wait_prior_grids();  // inputs and zeroed tickets are ready past this point
+    int32_t *starts = lens + p.B;                                   // [B]
+    wait_prior_grids();  // inputs are ready past this point
     constexpr bool kLanes = PA_DECODE_LOADER != 0 && !MMA;
 
     // ---- tiles per sequence and their prefix sums (whole CTA) ---------------
@@ -1010,8 +1109,16 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
                 if (blockIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
                 L = L < 1 ? 0 : cap;
             }
+            // tokens before S are covered by the sequence's shared-prefix
+            // partials (a multiple of the block size, below L; else none)
+            int S = p.shared_len ? p.shared_len[b] : 0;
+            if (S < 0 || S >= L || (S & (p.bs - 1))) {
+                if (S != 0 && blockIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+                S = 0;
+            }
             lens[b] = L;
-            nt = (L + C::TT - 1) / C::TT;
+            starts[b] = S;
+            nt = (L - S + C::TT - 1) / C::TT;
         }
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -1035,7 +1142,7 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
         pa::fence_barrier_init();
     }
     __syncthreads();
-    const BatchTables bt{pre, lens};
+    const BatchTables bt{pre, lens, starts};
 
     // ---- this warp's range of units ------------------------------------------
     const int64_t U = int64_t(p.Hkv) * pre[p.B];
@@ -1088,7 +1195,7 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
             st.load_q(qbase + (static_cast<size_t>(cc.b) * p.Hq + cc.hk * GQ) * D, p.qscale);
         }
         const uint32_t kaddr = pa::smem_u32(ring + s * C::STAGE);
-        st.tile(kaddr, kaddr + C::TILE, min(C::TT, cc.L - cc.t * C::TT), pbuf, sbuf);
+        st.tile(kaddr, kaddr + C::TILE, min(C::TT, cc.L - first_token(cc, C::TT)), pbuf, sbuf);
         __syncwarp();
         if (i + C::NST < my_n) {
             if constexpr (MMA) {
@@ -1339,6 +1446,49 @@ __global__ void __launch_bounds__(D) merge_kernel(const DecodeParams p) {
                        num / den);
 }
 
+// Merge of the persistent kernel's partials: one warp per (sequence,
+// query head) of item blockIdx.x = b * Hkv + hk merges the item's segment
+// partials and its shared-prefix partials by log-sum-exp.  Launched as a
+// programmatic dependent of the decode grid; waits for it before reading.
+template <typename T, int D, int GQ>
+__global__ void __launch_bounds__(GQ * 32) partial_merge_kernel(const DecodeParams p) {
+    constexpr int EL = D / 32;
+    const int item = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    wait_prior_grids();
+    const unsigned meta = __ldcg(p.meta + item);
+    const int nseg = static_cast<int>(meta & 0xffffu), ns = nseg + static_cast<int>(meta >> 16);
+    if (ns == 0) return;  // written out by the decode
+    const size_t row = static_cast<size_t>(item / p.Hkv) * p.Hq + (item % p.Hkv) * GQ + h;
+    const size_t sb = row * p.rowslots;
+    const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + sb;
+    float M = -INFINITY;
+    for (int sg = lane; sg < ns; sg += 32) M = fmaxf(M, __ldcg(&ml[slot_of(p, sg, nseg)]).x);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(pa::kFull, M, o));
+    float den = 0.f;
+    for (int sg = lane; sg < ns; sg += 32) {
+        const float2 v = __ldcg(&ml[slot_of(p, sg, nseg)]);
+        den += exp2f(v.x - M) * v.y;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(pa::kFull, den, o);
+    float acc[EL];
+#pragma unroll
+    for (int e = 0; e < EL; ++e) acc[e] = 0.f;
+    const float *src = p.ws_acc + sb * D + EL * lane;
+#pragma unroll 4
+    for (int sg = 0; sg < ns; ++sg) {
+        const int sl = slot_of(p, sg, nseg);
+        const float f = exp2f(__ldcg(&ml[sl]).x - M);
+#pragma unroll
+        for (int e = 0; e < EL; ++e) acc[e] += f * __ldcg(src + sl * D + e);
+    }
+    const float inv = 1.f / den;
+    T *out = static_cast<T *>(p.out) + row * D + EL * lane;
+#pragma unroll
+    for (int e = 0; e < EL; e += 2) store_pair<T>(out + e, acc[e] * inv, acc[e + 1] * inv);
+}
+
 int log2_int(int x) {
     int l = 0;
     while ((1 << l) < x) ++l;
@@ -1351,18 +1501,6 @@ int resolve_partition(int partition_tokens) {
 
 bool partition_ok(int pt, int bs) {
     return pt > 0 && pt <= kMaxPartition && pt % 32 == 0 && pt % bs == 0;
-}
-
-// Zero the merge tickets of the persistent kernel that follows it in the
-// stream.  It waits for the kernels before it first (the workspace may still
-// be in use by them), lets the decode grid launch at once (that grid waits
-// for this one to complete before it reads anything), then clears.
-__global__ void __launch_bounds__(256) decode_prep_kernel(unsigned *ctr, int64_t n) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    wait_prior_grids();
-    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-         i += int64_t(gridDim.x) * blockDim.x)
-        ctr[i] = 0u;
 }
 
 // Launch `kern` as a programmatic dependent of the previous kernel in the
@@ -1395,7 +1533,7 @@ int sm_count() {
 template <typename T, int D, int GQ, bool MMA>
 int launch_persistent(const DecodeParams &p, cudaStream_t stream) {
     using C = typename AttnOf<T, D, GQ, MMA>::type::C;
-    const size_t smem = C::OFF_BT + sizeof(int32_t) * (2 * p.B + 1) + (MMA ? 1024 : 0);
+    const size_t smem = C::OFF_BT + sizeof(int32_t) * (3 * p.B + 1) + (MMA ? 1024 : 0);
     auto kern = decode_persistent_kernel<T, D, GQ, MMA>;
     CUtensorMap kmap{}, vmap{};
     if constexpr (MMA) {
@@ -1420,13 +1558,14 @@ int launch_persistent(const DecodeParams &p, cudaStream_t stream) {
     const int sms = sm_count();
     if (sms <= 0) return pa::fail(PA_ERR_CUDA, "decode: no SM count");
     const int grid = sms * std::max(per_sm, 1);
-    const int64_t nt = int64_t(p.B) * p.Hkv;
-    const int prep_grid = static_cast<int>(std::min<int64_t>((nt + 255) / 256, sms));
-    e = launch_dependent(decode_prep_kernel, dim3(prep_grid), dim3(256), 0, stream, p.ctr, nt);
-    if (e != cudaSuccess) return pa::cuda_fail(e, "decode prep launch");
     e = launch_dependent(kern, dim3(grid), dim3(kWarps * 32), smem, stream, p, kmap, vmap);
     if (e != cudaSuccess) return pa::cuda_fail(e, "decode launch");
-    return pa::check_launch("decode launch");
+    if (int rc = pa::check_launch("decode launch")) return rc;
+    const int64_t items = int64_t(p.B) * p.Hkv;
+    e = launch_dependent(partial_merge_kernel<T, D, GQ>, dim3(static_cast<unsigned>(items)),
+                         dim3(GQ * 32), 0, stream, p);
+    if (e != cudaSuccess) return pa::cuda_fail(e, "decode merge launch");
+    return pa::check_launch("decode merge launch");
 }
 
 // The tensor-core tile serves bf16 groups of 4 or 8 heads whose pool rows
@@ -1488,8 +1627,43 @@ int kernel_for(int B, int Hkv, int MB, int bs_log2, int partitions, int sms) {
     return 4 * grid_ctas <= 7ll * sms * kMinCtas * kWarps ? PA_DECODE_GRID : PA_DECODE_PERSISTENT;
 }
 
+template <int D, int GQ>
+int launch_prefix(const DecodeParams &p, const PrefixParams &pp, int max_group_size,
+                  cudaStream_t stream) {
+    constexpr int MPC = kPfxWarps * (8 / GQ);
+    CUtensorMap kmap{}, vmap{};
+    const int64_t rows = p.num_blocks * p.Hkv * p.bs;
+    const int box = std::min(MmaCfg<D, GQ>::TT, p.bs);
+    if (int rc = pa::pool_tensor_map(&kmap, p.k_cache, rows, D, box)) return rc;
+    if (int rc = pa::pool_tensor_map(&vmap, p.v_cache, rows, D, box)) return rc;
+    const size_t smem = prefix_smem_bytes<D>();
+    auto kern = prefix_kernel<D, GQ>;
+    (void)cudaGetLastError();
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return pa::cuda_fail(e, "decode_shared: shared memory attribute");
+    const dim3 grid((max_group_size + MPC - 1) / MPC, p.Hkv, pp.G * pp.nc);
+    e = launch_dependent(kern, grid, dim3((kPfxWarps + 1) * 32), smem, stream, p, pp, kmap, vmap);
+    if (e != cudaSuccess) return pa::cuda_fail(e, "decode_shared: prefix launch");
+    return pa::check_launch("decode_shared: prefix launch");
+}
+
+// Shared-prefix work of a call (pa_decode_shared), or none.
+struct SharedPlan {
+    PrefixParams pp;
+    int max_group_size;
+};
+
 template <typename T, int D, int GQ>
-int launch(const DecodeParams &p, cudaStream_t stream) {
+int launch(const DecodeParams &p, const SharedPlan *sp, cudaStream_t stream) {
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        if (sp) {  // the host checked: bf16, persistent kernel, 32-bit pool rows
+            if (int rc = launch_prefix<D, GQ>(p, sp->pp, sp->max_group_size, stream)) return rc;
+            if constexpr (GQ % 2 == 0 && GQ >= PA_DECODE_MMA_MIN_GQ)
+                if (use_mma<T, GQ>(p)) return launch_persistent<T, D, GQ, true>(p, stream);
+            return launch_persistent<T, D, GQ, false>(p, stream);
+        }
+    }
     const int sms = sm_count();
     if (sms <= 0) return pa::fail(PA_ERR_CUDA, "decode: no SM count");
     if (kernel_for(p.B, p.Hkv, p.MB, p.bs_log2, p.max_parts - 1, sms) != PA_DECODE_PERSISTENT)
@@ -1501,18 +1675,18 @@ int launch(const DecodeParams &p, cudaStream_t stream) {
 }
 
 template <typename T, int D>
-int dispatch_gq(int gq, const DecodeParams &p, cudaStream_t s) {
+int dispatch_gq(int gq, const DecodeParams &p, const SharedPlan *sp, cudaStream_t s) {
     switch (gq) {
-        case 1: return launch<T, D, 1>(p, s);
-        case 2: return launch<T, D, 2>(p, s);
-        case 4: return launch<T, D, 4>(p, s);
-        case 8: return launch<T, D, 8>(p, s);
+        case 1: return launch<T, D, 1>(p, sp, s);
+        case 2: return launch<T, D, 2>(p, sp, s);
+        case 4: return launch<T, D, 4>(p, sp, s);
+        case 8: return launch<T, D, 8>(p, sp, s);
         default: return pa::fail(PA_ERR_UNSUPPORTED, "decode: Hq/Hkv=%d unsupported", gq);
     }
 }
 
-// Workspace layout: merge tickets u32 [B][Hq] (the persistent kernel uses
-// [B][Hkv] of them) padded to a multiple of 256 bytes, then acc fp32
+// Workspace layout: per-item partial counts u32 [B][Hq] (the persistent
+// kernel uses [B][Hkv] of them) padded to a multiple of 256 bytes, then acc fp32
 // [B][Hq][maxseg][D], then (max, sum) fp32 [B][Hq][maxseg][2]; maxseg =
 // partitions per sequence + 1 bounds the segments of one item in the
 // persistent kernel and the partitions of the grid kernel.  The padding keeps
@@ -1520,7 +1694,7 @@ int dispatch_gq(int gq, const DecodeParams &p, cudaStream_t s) {
 // float4).  Every product is checked: false when the size does not fit size_t.
 constexpr size_t kWsAlign = 256;
 struct WsLayout {
-    size_t ticket_bytes, acc_bytes, ml_bytes, total;
+    size_t meta_bytes, acc_bytes, ml_bytes, total;
 };
 
 bool workspace_layout(int64_t B, int64_t Hq, int64_t D, int64_t maxseg, WsLayout *l) {
@@ -1594,12 +1768,72 @@ int pa_decode_tile_for(int Hq, int Hkv, int head_dim, int block_size, int64_t nu
     return PA_OK;
 }
 
-int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
-              const int32_t *block_table, int max_blocks_per_seq, const int32_t *context_lens,
-              int B, int Hq, int Hkv, int head_dim, int block_size, int64_t num_blocks,
-              float scale, int partition_tokens, void *workspace, size_t workspace_bytes,
-              int dtype, pa_stream_t stream) {
-    pa::clear_error();
+}  // extern "C"
+
+namespace {
+
+// Groups of a pa_decode_shared call (NULL for pa_decode).
+struct SharedArgs {
+    const int32_t *shared_len, *group_start, *group_seqs;
+    int G, num_members, max_group_size, max_shared_len;
+};
+
+constexpr int kPfxChunkMin = 256;  // tokens: the prefix slots bound is max_shared_len / this
+
+int prefix_slots_for(int max_shared_len) {
+    return max_shared_len > 0 ? (max_shared_len + kPfxChunkMin - 1) / kPfxChunkMin : 0;
+}
+
+int validate_groups(const SharedArgs &sh, const int32_t *context_lens, const int32_t *block_table,
+                    int B, int MB, int bs, cudaStream_t stream) {
+    std::vector<int32_t> lens(B), S(B), gs(sh.G + 1), mem(sh.num_members),
+        table(size_t(B) * MB);
+    if (int rc = pa::fetch(lens.data(), context_lens, B * sizeof(int32_t), stream)) return rc;
+    if (int rc = pa::fetch(S.data(), sh.shared_len, B * sizeof(int32_t), stream)) return rc;
+    if (int rc = pa::fetch(gs.data(), sh.group_start, gs.size() * sizeof(int32_t), stream))
+        return rc;
+    if (sh.num_members > 0)
+        if (int rc = pa::fetch(mem.data(), sh.group_seqs, mem.size() * sizeof(int32_t), stream))
+            return rc;
+    if (int rc = pa::fetch(table.data(), block_table, table.size() * sizeof(int32_t), stream))
+        return rc;
+    std::vector<int> group_of(B, -1);
+    for (int g = 0; g < sh.G; ++g) {
+        if (gs[g] < 0 || gs[g + 1] < gs[g] || gs[g + 1] > sh.num_members)
+            return pa::fail(PA_ERR_INVALID, "validate: group_start[%d..%d] out of range", g, g + 1);
+        if (gs[g + 1] - gs[g] > sh.max_group_size)
+            return pa::fail(PA_ERR_INVALID, "validate: group %d larger than max_group_size", g);
+        for (int m = gs[g]; m < gs[g + 1]; ++m) {
+            const int b = mem[m];
+            if (b < 0 || b >= B) return pa::fail(PA_ERR_INVALID, "validate: member %d not in batch", b);
+            if (group_of[b] >= 0)
+                return pa::fail(PA_ERR_INVALID, "validate: sequence %d in two groups", b);
+            group_of[b] = g;
+            const int b0 = mem[gs[g]];
+            if (S[b] != S[b0] || S[b] <= 0 || S[b] % bs || S[b] >= lens[b] ||
+                S[b] > sh.max_shared_len)
+                return pa::fail(PA_ERR_INVALID,
+                                "validate: shared_len[%d]=%d (group %d: positive, a multiple of "
+                                "block_size, below the context length, equal in the group)",
+                                b, S[b], g);
+            for (int i = 0; i < S[b] / bs; ++i)
+                if (table[size_t(b) * MB + i] != table[size_t(b0) * MB + i])
+                    return pa::fail(PA_ERR_INVALID,
+                                    "validate: sequence %d does not share block %d of group %d", b,
+                                    i, g);
+        }
+    }
+    for (int b = 0; b < B; ++b)
+        if (group_of[b] < 0 && S[b] != 0)
+            return pa::fail(PA_ERR_INVALID, "validate: shared_len[%d] != 0 outside any group", b);
+    return PA_OK;
+}
+
+int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
+                const int32_t *block_table, int max_blocks_per_seq, const int32_t *context_lens,
+                int B, int Hq, int Hkv, int head_dim, int block_size, int64_t num_blocks,
+                float scale, int partition_tokens, const SharedArgs *sh, void *workspace,
+                size_t workspace_bytes, int dtype, cudaStream_t stream) {
     if (dtype != PA_BF16 && dtype != PA_F32) return pa::fail(PA_ERR_INVALID, "decode: bad dtype");
     if (B < 0 || B > 65535 || Hq <= 0 || Hkv <= 0 || Hkv > 65535 || Hq % Hkv || num_blocks <= 0 ||
         max_blocks_per_seq <= 0)
@@ -1628,8 +1862,9 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
         return pa::fail(PA_ERR_INVALID, "decode: q, out and pools must be 16-byte aligned");
     const int64_t cap = int64_t(max_blocks_per_seq) * block_size;
     const int max_parts = static_cast<int>((cap + pt - 1) / pt);
+    const int npslot = sh ? prefix_slots_for(sh->max_shared_len) : 0;
     WsLayout wl;
-    if (!workspace_layout(B, Hq, head_dim, int64_t(max_parts) + 1, &wl))
+    if (!workspace_layout(B, Hq, head_dim, int64_t(max_parts) + 1 + npslot, &wl))
         return pa::fail(PA_ERR_INVALID, "decode: workspace size does not fit in size_t");
     const size_t need = wl.total;
     if (need > workspace_bytes || !workspace)
@@ -1654,6 +1889,10 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
                                     b, i, v);
             }
         }
+        if (sh)
+            if (int rc = validate_groups(*sh, context_lens, block_table, B, max_blocks_per_seq,
+                                         block_size, stream))
+                return rc;
     }
     DecodeParams p{};
     p.out = out;
@@ -1662,9 +1901,9 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     p.v_cache = static_cast<const uint8_t *>(v_cache);
     p.block_table = block_table;
     p.context_lens = context_lens;
-    p.ctr = static_cast<unsigned *>(workspace);
-    p.ws_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + wl.ticket_bytes);
-    p.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) + wl.ticket_bytes +
+    p.meta = static_cast<unsigned *>(workspace);
+    p.ws_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + wl.meta_bytes);
+    p.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) + wl.meta_bytes +
                                         wl.acc_bytes);
     p.err = pa::device_error_word();
     p.num_blocks = num_blocks;
@@ -1675,16 +1914,105 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     p.bs_log2 = log2_int(block_size);
     p.MB = max_blocks_per_seq;
     p.PT = pt;
-    p.max_parts = max_parts + 1;  // slot stride of both kernels
+    p.max_parts = max_parts + 1;  // slot stride of the grid kernel
     p.maxseg = max_parts + 1;
+    p.rowslots = max_parts + 1 + npslot;  // slot stride of the persistent kernel
+    p.shared_len = nullptr;
+    p.pslot0 = max_parts + 1;
+    p.npfx = 0;
     p.qscale = scale * kLog2e;
     const int gq = Hq / Hkv;
+    // Shared-prefix path: bf16 batches that run on the persistent kernel and
+    // whose pool rows fit 32-bit tensor-copy coordinates; other calls decode
+    // every sequence whole (the same result: the groups only save reads).
+    SharedPlan plan{};
+    const SharedPlan *sp = nullptr;
+    if (sh && sh->G > 0 && npslot > 0 && dtype == PA_BF16 &&
+        num_blocks * Hkv * block_size <= int64_t(INT32_MAX)) {
+        const int sms = sm_count();
+        if (sms <= 0) return pa::fail(PA_ERR_CUDA, "decode_shared: no SM count");
+        if (kernel_for(B, Hkv, max_blocks_per_seq, p.bs_log2, max_parts, sms) ==
+            PA_DECODE_PERSISTENT) {
+            const int mpc = kPfxWarps * (8 / gq);
+            const int64_t ctas = int64_t((sh->max_group_size + mpc - 1) / mpc) * Hkv * sh->G;
+            const int64_t want = (2 * int64_t(sms) + ctas - 1) / std::max<int64_t>(ctas, 1);
+            plan.pp.group_start = sh->group_start;
+            plan.pp.group_seqs = sh->group_seqs;
+            plan.pp.G = sh->G;
+            plan.pp.num_members = sh->num_members;
+            plan.pp.nc = static_cast<int>(std::min<int64_t>(std::max<int64_t>(want, 1), npslot));
+            plan.max_group_size = sh->max_group_size;
+            if (int64_t(plan.pp.G) * plan.pp.nc > 65535)
+                return pa::fail(PA_ERR_UNSUPPORTED, "decode_shared: too many groups");
+            p.shared_len = sh->shared_len;
+            p.npfx = plan.pp.nc;
+            sp = &plan;
+        }
+    }
     if (dtype == PA_BF16)
-        return head_dim == 128 ? dispatch_gq<__nv_bfloat16, 128>(gq, p, stream)
-                               : dispatch_gq<__nv_bfloat16, 64>(gq, p, stream);
-    return head_dim == 128 ? dispatch_gq<float, 128>(gq, p, stream)
-                           : dispatch_gq<float, 64>(gq, p, stream);
+        return head_dim == 128 ? dispatch_gq<__nv_bfloat16, 128>(gq, p, sp, stream)
+                               : dispatch_gq<__nv_bfloat16, 64>(gq, p, sp, stream);
+    return head_dim == 128 ? dispatch_gq<float, 128>(gq, p, nullptr, stream)
+                           : dispatch_gq<float, 64>(gq, p, nullptr, stream);
 }
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_table, int max_blocks_per_seq, const int32_t *context_lens,
+              int B, int Hq, int Hkv, int head_dim, int block_size, int64_t num_blocks,
+              float scale, int partition_tokens, void *workspace, size_t workspace_bytes,
+              int dtype, pa_stream_t stream) {
+    pa::clear_error();
+    return decode_impl(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, B,
+                       Hq, Hkv, head_dim, block_size, num_blocks, scale, partition_tokens, nullptr,
+                       workspace, workspace_bytes, dtype, stream);
+}
+
+int pa_decode_shared_workspace_size(int B, int Hq, int head_dim, int max_blocks_per_seq,
+                                    int block_size, int partition_tokens, int max_shared_len,
+                                    size_t *bytes) {
+    pa::clear_error();
+    if (!bytes) return pa::fail(PA_ERR_INVALID, "shared_workspace_size: bytes is NULL");
+    if (B < 0 || Hq <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 || max_shared_len < 0 ||
+        !pa::pow2_in(block_size, 8, 128))
+        return pa::fail(PA_ERR_INVALID, "shared_workspace_size: bad sizes");
+    const int pt = resolve_partition(partition_tokens);
+    if (!partition_ok(pt, block_size))
+        return pa::fail(PA_ERR_INVALID, "shared_workspace_size: bad partition_tokens %d", pt);
+    const int64_t cap = int64_t(max_blocks_per_seq) * block_size;
+    const int64_t slots = (cap + pt - 1) / pt + 1 + prefix_slots_for(max_shared_len);
+    WsLayout l;
+    if (!workspace_layout(B, Hq, head_dim, slots, &l))
+        return pa::fail(PA_ERR_INVALID, "shared_workspace_size: size does not fit in size_t");
+    *bytes = l.total;
+    return PA_OK;
+}
+
+int pa_decode_shared(void *out, const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_table, int max_blocks_per_seq,
+                     const int32_t *context_lens, int B, int Hq, int Hkv, int head_dim,
+                     int block_size, int64_t num_blocks, float scale, int partition_tokens,
+                     const int32_t *shared_len, const int32_t *group_start,
+                     const int32_t *group_seqs, int G, int num_members, int max_group_size,
+                     int max_shared_len, void *workspace, size_t workspace_bytes, int dtype,
+                     pa_stream_t stream) {
+    pa::clear_error();
+    if (G < 0 || num_members < 0 || max_group_size < 0 || max_shared_len < 0)
+        return pa::fail(PA_ERR_INVALID, "decode_shared: bad group sizes");
+    if (G > 0 && (!shared_len || !group_start || (num_members > 0 && !group_seqs)))
+        return pa::fail(PA_ERR_INVALID, "decode_shared: NULL group array");
+    if (max_shared_len > (int64_t(max_blocks_per_seq) * block_size))
+        return pa::fail(PA_ERR_INVALID, "decode_shared: max_shared_len beyond the table");
+    const SharedArgs sh{shared_len, group_start, group_seqs, G,
+                        num_members, max_group_size, max_shared_len};
+    return decode_impl(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, B,
+                       Hq, Hkv, head_dim, block_size, num_blocks, scale, partition_tokens, &sh,
+                       workspace, workspace_bytes, dtype, stream);
+}
+
 
 }  // extern "C"
 // ---------------------------------------------------------------------------
@@ -1703,9 +2031,9 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
 // device (with that device current) looks up its address with
 // cudaGetSymbolAddress and caches it; make that first call before any stream
 // capture.  All calls on a device share the array and it keeps the contents
-// of the last call; nothing in it needs to start at zero (the merge tickets
-// are cleared by each call before use, and every partial is written before
-// it is read in the same call).  Calls that overlap on the GPU
+// of the last call; nothing in it needs to start at zero (every partial
+// and per-item count is written before it is read in the same call).  Calls
+// that overlap on the GPU
 // (different streams, or host threads racing) race on the array: serialize
 // them.
 // ---------------------------------------------------------------------------

@@ -201,6 +201,53 @@ def decode(q, k_cache, v_cache, block_table, context_lens, scale=None, partition
     return out
 
 
+def decode_shared_workspace_size(B, Hq, head_dim, max_blocks_per_seq, block_size,
+                                 partition_tokens=0, max_shared_len=0):
+    out = ctypes.c_size_t(0)
+    check(lib().pa_decode_shared_workspace_size(B, Hq, head_dim, max_blocks_per_seq, block_size,
+                                                partition_tokens, max_shared_len,
+                                                ctypes.byref(out)))
+    return out.value
+
+
+def decode_shared(q, k_cache, v_cache, block_table, context_lens, shared_len, group_start,
+                  group_seqs, max_group_size, max_shared_len, scale=None, partition_tokens=0,
+                  workspace=None, out=None, stream=None):
+    """Paged decode of a batch whose groups share prefix blocks (pa_decode_shared).
+
+    As decode, plus: shared_len int32 [B] (tokens each sequence takes from its
+    group's shared blocks, 0 outside any group), group_start int32 [G+1] and
+    group_seqs int32 [members] (CSR member lists of the groups), and host
+    bounds max_group_size and max_shared_len.  The shared blocks of each group
+    are read once per KV head for all members; the result equals decode's
+    within the error bound."""
+    _check_decode_shapes(q, k_cache, v_cache, block_table, context_lens, out)
+    B, Hq, d = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    MB = block_table.shape[1]
+    _require(shared_len.shape == (B,), f"shared_len must be [{B}]")
+    _require(group_start.dim() == 1 and group_start.numel() >= 1, "group_start must be [G+1]")
+    G = group_start.numel() - 1
+    M = group_seqs.numel()
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    ws_bytes = decode_shared_workspace_size(B, Hq, d, MB, bs, partition_tokens, max_shared_len)
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes // 4, dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(lib().pa_decode_shared(
+        _cuda(out, "out", q.dtype), _cuda(q, "q", k_cache.dtype), _cuda(k_cache, "k_cache"),
+        _cuda(v_cache, "v_cache", k_cache.dtype), _cuda(block_table, "block_table", torch.int32),
+        MB, _cuda(context_lens, "context_lens", torch.int32), B, Hq, Hkv, d, bs, NB, scale,
+        partition_tokens, _cuda(shared_len, "shared_len", torch.int32),
+        _cuda(group_start, "group_start", torch.int32),
+        _cuda(group_seqs, "group_seqs", torch.int32) if M else None, G, M, int(max_group_size),
+        int(max_shared_len), ws_ptr, ws_len, _dt(q), _stream(stream)))
+    return out
+
+
 def decode_noalloc_capacity() -> int:
     """Bytes of the library's fixed decode scratch (pa_decode_noalloc)."""
     return int(lib().pa_decode_noalloc_capacity())

@@ -257,6 +257,78 @@ def prefix_fork_workload(seed=0, B=None, forks=None, device="cpu"):
     return PrefixForks(w, parents, k_child, v_child, q_child)
 
 
+def shared_groups_workload(groups, singles=0, seed=0, suffix_range=(1, 300), Hq=32, Hkv=8,
+                           d=128, bs=16, dtype=torch.bfloat16, device="cpu"):
+    """Decode batch with groups of sequences that share prefix blocks.
+
+    groups: list of (prefix_len, members); prefix_len a multiple of bs.
+    Each member's history is its group's prefix followed by a private suffix
+    (uniform in suffix_range, numpy PCG64(seed)); ``singles`` more sequences
+    share nothing (lengths uniform in [1, 2 * suffix_range[1]]).  The batch
+    order is a seeded permutation (PCG64(seed+3)), so members of a group are
+    not adjacent.  Values: torch generator seed+1, N(0,1) rounded to dtype
+    (q, then per group the prefix K/V, then the private K/V of every sequence
+    in batch order).  Placement: PCG64(seed+2) permutation of a pool 1.2x the
+    distinct blocks; a group's prefix blocks appear once in the pool and in
+    every member's table row.
+
+    extra: shared_len [B] (the group's prefix_len for a member, else 0),
+    group_start [G+1], group_seqs (batch rows of the members, group by group),
+    max_group_size, max_shared_len."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lo, hi = suffix_range
+    rows = []  # (group or -1, prefix_len, private_len)
+    for g, (P, n) in enumerate(groups):
+        assert P % bs == 0 and P > 0
+        for L in rng.integers(lo, hi + 1, size=n):
+            rows.append((g, P, int(L)))
+    for L in rng.integers(1, 2 * hi + 1, size=singles):
+        rows.append((-1, 0, int(L)))
+    order = np.random.Generator(np.random.PCG64(seed + 3)).permutation(len(rows))
+    rows = [rows[i] for i in order]
+    B = len(rows)
+    gen = torch.Generator().manual_seed(seed + 1)
+    q = _values((B, Hq, d), dtype, gen, device)
+    pk = [_values((P, Hkv, d), dtype, gen, device) for P, _ in groups]
+    pv = [_values((P, Hkv, d), dtype, gen, device) for P, _ in groups]
+    priv_k = [_values((L, Hkv, d), dtype, gen, device) for _, _, L in rows]
+    priv_v = [_values((L, Hkv, d), dtype, gen, device) for _, _, L in rows]
+    ks, vs, lens = [], [], []
+    for (g, P, L), k_, v_ in zip(rows, priv_k, priv_v):
+        ks += ([pk[g]] if g >= 0 else []) + [k_]
+        vs += ([pv[g]] if g >= 0 else []) + [v_]
+        lens.append(P + L)
+    lens = np.asarray(lens, dtype=np.int64)
+    n_pre = [P // bs for P, _ in groups]
+    n_priv = [-(-L // bs) for _, _, L in rows]
+    num_blocks = pool_size(n_pre + n_priv)
+    perm = np.random.Generator(np.random.PCG64(seed + 2)).permutation(num_blocks)
+    mb = max((P // bs if g >= 0 else 0) + -(-L // bs) for g, P, L in rows)
+    table = np.zeros((B, mb), dtype=np.int32)
+    pos = 0
+    pre_ids = []
+    for nb in n_pre:
+        pre_ids.append(perm[pos:pos + nb])
+        pos += nb
+    for r, (g, P, L) in enumerate(rows):
+        k0 = 0
+        if g >= 0:
+            table[r, :P // bs] = pre_ids[g]
+            k0 = P // bs
+        table[r, k0:k0 + n_priv[r]] = perm[pos:pos + n_priv[r]]
+        pos += n_priv[r]
+    shared_len = np.array([P if g >= 0 else 0 for g, P, _ in rows], dtype=np.int32)
+    members = [[r for r, row in enumerate(rows) if row[0] == g] for g in range(len(groups))]
+    group_start = np.concatenate([[0], np.cumsum([len(m) for m in members])]).astype(np.int32)
+    group_seqs = np.array([r for m in members for r in m], dtype=np.int32)
+    w = Workload("shared-groups", Hq, Hkv, d, bs, dtype, lens, np.ones(B, np.int64), q,
+                 torch.cat(ks), torch.cat(vs), table, num_blocks)
+    w.extra.update(shared_len=shared_len, group_start=group_start, group_seqs=group_seqs,
+                   max_group_size=max((n for _, n in groups), default=0),
+                   max_shared_len=max((P for P, _ in groups), default=0))
+    return w
+
+
 def mixed_workload(seed=0, B=None, R=None, chunk=None, priors=None, device="cpu"):
     """Continuous batch: B decode sequences plus R chunked-prefill requests.
 

@@ -43,18 +43,18 @@ def test_version(lib):
     assert lib.pa_version() == 1
 
 
-def _ticket_bytes(rows):
+def _count_bytes(rows):
     return -(-rows * 4 // 256) * 256
 
 
 def test_workspace_size_host_only(lib):
     from paged_kv_cache_192_gb300 import ops
     # 8B-shaped: 64 seqs, 32 heads, d 128, 256 blocks of 16 -> 8 partitions of
-    # 512 + 1 segment slots per (sequence, head), after a 4-byte ticket per
+    # 512 + 1 segment slots per (sequence, head), after a 4-byte partial count per
     # (sequence, head) padded to a multiple of 256 bytes
     assert ops.decode_workspace_size(64, 32, 128, 256, 16, 512) == (
-        _ticket_bytes(64 * 32) + 64 * 32 * 9 * 130 * 4)
-    assert ops.decode_workspace_size(4, 4, 64, 4, 16, 0) == _ticket_bytes(16) + 16 * 2 * 66 * 4
+        _count_bytes(64 * 32) + 64 * 32 * 9 * 130 * 4)
+    assert ops.decode_workspace_size(4, 4, 64, 4, 16, 0) == _count_bytes(16) + 16 * 2 * 66 * 4
     assert ops.decode_workspace_size(0, 4, 64, 4, 16, 0) == 0
     # odd B x Hq: the fp32 partials still start 256 bytes into the buffer
     assert ops.decode_workspace_size(5, 3, 128, 8, 16, 64) == 256 + 15 * 3 * 130 * 4

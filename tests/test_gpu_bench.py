@@ -27,7 +27,7 @@ def test_default_bench_line(capsys):
     assert 0 < r["frac"] < 1.5 and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
     e2e = j["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
-    assert j["gpu_launches"] == 3 * 20  # store, ticket clear, decode
+    assert j["gpu_launches"] == 3 * 20  # store, decode, merge of split items
     assert "decode_persistent_kernel, tensor-core tile" in j["roofline"]["kernel"]
     assert "sm_mhz" in j["clocks"] and "reasons" in j["clocks"]
     cb = j["cpu_baseline"]

@@ -328,9 +328,9 @@ print("ok")
 def test_workspace_contents_do_not_matter_fresh_process():
     """A split batch (64 sequences of the 8B shape, items split over several
     warps) decoded in a fresh process with every workspace word set to
-    (1 << 32) | 7 beforehand -- a stale 'ticket' pattern -- still matches the
-    oracle, twice: the call clears the tickets it uses before the decode grid
-    reads them."""
+    (1 << 32) | 7 beforehand (stale counts and partials) still matches the
+    oracle, twice: every per-item count and partial is written before it is
+    read."""
     import os
     import subprocess
     import sys
@@ -344,7 +344,8 @@ def test_workspace_contents_do_not_matter_fresh_process():
 def test_odd_query_row_count(max_blocks, kernel):
     """B x Hq odd (5 sequences x 3 query heads, 3 KV heads, d 128) with split
     sequences on both kernels: the workspace's fp32 partials stay aligned for
-    the merge's vector loads whatever the number of tickets before them."""
+    the merge's vector loads whatever the number of per-item counts before
+    them."""
     lens = [1, 100, 127, 128, 128] if kernel == "grid" else [1, 100, 700, 2000, 5000]
     w = synth.decode_workload("8b", seed=31, lens=lens, Hq=3, Hkv=3, max_blocks=max_blocks)
     got, ref, _ = run(w, partition_tokens=64, kernel=kernel)

@@ -1461,27 +1461,46 @@ __global__ void __launch_bounds__(GQ * 32) partial_merge_kernel(const DecodePara
     const size_t row = static_cast<size_t>(item / p.Hkv) * p.Hq + (item % p.Hkv) * GQ + h;
     const size_t sb = row * p.rowslots;
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + sb;
-    float M = -INFINITY;
-    for (int sg = lane; sg < ns; sg += 32) M = fmaxf(M, __ldcg(&ml[slot_of(p, sg, nseg)]).x);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(pa::kFull, M, o));
-    float den = 0.f;
-    for (int sg = lane; sg < ns; sg += 32) {
-        const float2 v = __ldcg(&ml[slot_of(p, sg, nseg)]);
-        den += exp2f(v.x - M) * v.y;
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(pa::kFull, den, o);
+    const float *src = p.ws_acc + sb * D + EL * lane;
     float acc[EL];
 #pragma unroll
     for (int e = 0; e < EL; ++e) acc[e] = 0.f;
-    const float *src = p.ws_acc + sb * D + EL * lane;
-#pragma unroll 4
-    for (int sg = 0; sg < ns; ++sg) {
-        const int sl = slot_of(p, sg, nseg);
-        const float f = exp2f(__ldcg(&ml[sl]).x - M);
+    float den = 0.f, M = -INFINITY;
+    // 32 partials at a time: lane s holds partial s's (max, sum); the weights
+    // travel by shuffle and every acc load is issued independently
+    for (int base = 0; base < ns; base += 32) {
+        const int k = min(32, ns - base);
+        float2 v = make_float2(-INFINITY, 0.f);
+        if (lane < k) v = __ldcg(&ml[slot_of(p, base + lane, nseg)]);
+        float Mc = v.x;
 #pragma unroll
-        for (int e = 0; e < EL; ++e) acc[e] += f * __ldcg(src + sl * D + e);
+        for (int o = 16; o >= 1; o >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(pa::kFull, Mc, o));
+        const float Mn = fmaxf(M, Mc);
+        const float rescale = M == -INFINITY ? 0.f : exp2f(M - Mn);
+        M = Mn;
+        const float wl = lane < k ? exp2f(v.x - M) : 0.f;
+        float d = wl * v.y;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(pa::kFull, d, o);
+        den = den * rescale + d;
+#pragma unroll
+        for (int e = 0; e < EL; ++e) acc[e] *= rescale;
+#pragma unroll 8
+        for (int i = 0; i < k; ++i) {
+            const float f = __shfl_sync(pa::kFull, wl, i);
+            const float *sp = src + static_cast<size_t>(slot_of(p, base + i, nseg)) * D;
+            if constexpr (EL == 4) {
+                const float4 a = __ldcg(reinterpret_cast<const float4 *>(sp));
+                acc[0] += f * a.x;
+                acc[1] += f * a.y;
+                acc[2] += f * a.z;
+                acc[3] += f * a.w;
+            } else {
+                const float2 a = __ldcg(reinterpret_cast<const float2 *>(sp));
+                acc[0] += f * a.x;
+                acc[1] += f * a.y;
+            }
+        }
     }
     const float inv = 1.f / den;
     T *out = static_cast<T *>(p.out) + row * D + EL * lane;
@@ -1652,13 +1671,46 @@ int launch_prefix(const DecodeParams &p, const PrefixParams &pp, int max_group_s
 struct SharedPlan {
     PrefixParams pp;
     int max_group_size;
+    bool tc;  // tcgen05 prefill kernel in prefix mode, else prefix_kernel
 };
+
+int launch_prefix_any(const DecodeParams &p, const SharedPlan &sp, int D, cudaStream_t stream) {
+    pa::PrefixTcArgs a{};
+    a.q = p.q;
+    a.k_cache = p.k_cache;
+    a.v_cache = p.v_cache;
+    a.block_table = p.block_table;
+    a.context_lens = p.context_lens;
+    a.group_start = sp.pp.group_start;
+    a.group_seqs = sp.pp.group_seqs;
+    a.shared_len = p.shared_len;
+    a.acc = p.ws_acc;
+    a.ml = p.ws_ml;
+    a.err = p.err;
+    a.num_blocks = p.num_blocks;
+    a.B = p.B;
+    a.Hq = p.Hq;
+    a.Hkv = p.Hkv;
+    a.D = D;
+    a.bs = p.bs;
+    a.MB = p.MB;
+    a.G = sp.pp.G;
+    a.nc = sp.pp.nc;
+    a.max_group_size = sp.max_group_size;
+    a.num_members = sp.pp.num_members;
+    a.rowslots = p.rowslots;
+    a.pslot0 = p.pslot0;
+    a.qscale = p.qscale;
+    return pa::launch_prefix_tc(a, stream);
+}
 
 template <typename T, int D, int GQ>
 int launch(const DecodeParams &p, const SharedPlan *sp, cudaStream_t stream) {
     if constexpr (std::is_same<T, __nv_bfloat16>::value) {
         if (sp) {  // the host checked: bf16, persistent kernel, 32-bit pool rows
-            if (int rc = launch_prefix<D, GQ>(p, sp->pp, sp->max_group_size, stream)) return rc;
+            if (int rc = sp->tc ? launch_prefix_any(p, *sp, D, stream)
+                                : launch_prefix<D, GQ>(p, sp->pp, sp->max_group_size, stream))
+                return rc;
             if constexpr (GQ % 2 == 0 && GQ >= PA_DECODE_MMA_MIN_GQ)
                 if (use_mma<T, GQ>(p)) return launch_persistent<T, D, GQ, true>(p, stream);
             return launch_persistent<T, D, GQ, false>(p, stream);
@@ -1933,9 +1985,19 @@ int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cac
         if (sms <= 0) return pa::fail(PA_ERR_CUDA, "decode_shared: no SM count");
         if (kernel_for(B, Hkv, max_blocks_per_seq, p.bs_log2, max_parts, sms) ==
             PA_DECODE_PERSISTENT) {
-            const int mpc = kPfxWarps * (8 / gq);
+            // prefix work on the tcgen05 prefill kernel (one CTA of 256 (member,
+            // head) rows per SM; token chunks until about one wave), else on
+            // the warp-level prefix_kernel (two waves of smaller CTAs)
+            // (a chunk of the prefill kernel spans at most 512 * block_size + 64
+            // tokens: within its 1024-entry block-table slice)
+            const int nc_min = (sh->max_shared_len + 512 * block_size - 1) / (512 * block_size);
+            plan.tc = nc_min <= npslot && pa::prefix_tc_ok(block_size, num_blocks, Hkv,
+                                                           512 * block_size + 64);
+            const int mpc = plan.tc ? pa::prefix_tc_members(gq) : kPfxWarps * (8 / gq);
             const int64_t ctas = int64_t((sh->max_group_size + mpc - 1) / mpc) * Hkv * sh->G;
-            const int64_t want = (2 * int64_t(sms) + ctas - 1) / std::max<int64_t>(ctas, 1);
+            int64_t want = plan.tc ? int64_t(sms) / std::max<int64_t>(ctas, 1)
+                                   : (2 * int64_t(sms) + ctas - 1) / std::max<int64_t>(ctas, 1);
+            if (plan.tc) want = std::max<int64_t>(want, nc_min);
             plan.pp.group_start = sh->group_start;
             plan.pp.group_seqs = sh->group_seqs;
             plan.pp.G = sh->G;

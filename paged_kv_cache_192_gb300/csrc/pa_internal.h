@@ -41,6 +41,26 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline bool pow2_in(int x, int lo, int hi) { return x >= lo && x <= hi && (x & (x - 1)) == 0; }
 
+// Shared-prefix partials on the tcgen05 prefill kernel (pa_decode_shared):
+// for every group, member tile of prefix_tc_members(Hq / Hkv) members, KV
+// head and token chunk, one CTA computes the (max, sum, unnormalised O)
+// partial of each (member, query head) over the chunk of the group's shared
+// tokens and writes it to slot pslot0 + chunk of the member's decode
+// workspace row.  Launched as a programmatic dependent of the previous kernel.
+struct PrefixTcArgs {
+    const void *q, *k_cache, *v_cache;
+    const int32_t *block_table, *context_lens, *group_start, *group_seqs, *shared_len;
+    float *acc, *ml;
+    int *err;
+    int64_t num_blocks;
+    int B, Hq, Hkv, D, bs, MB, G, nc, max_group_size, num_members, rowslots, pslot0;
+    float qscale;  // softmax scale * log2(e)
+};
+inline int prefix_tc_members(int gq) { return 256 / gq; }
+// Block sizes 8..64, 32-bit pool rows and chunks of at most 1024 blocks.
+bool prefix_tc_ok(int bs, int64_t num_blocks, int Hkv, int max_chunk_tokens);
+int launch_prefix_tc(const PrefixTcArgs &a, cudaStream_t stream);
+
 // Copy `bytes` of device memory to a host buffer, synchronizing `stream`
 // (validate mode only).
 int fetch(void *host, const void *dev, size_t bytes, cudaStream_t stream);

@@ -23,6 +23,7 @@
 #include <cuda.h>
 
 #include <atomic>
+#include <type_traits>
 #include <cmath>
 #include <vector>
 
@@ -49,6 +50,13 @@ struct PrefillParams {
     int64_t num_blocks;
     int R, Hq, Hkv, bs, bs_log2, MB, max_query_len;
     float qscale;
+    // shared-prefix mode of prefill_tc2_kernel (pa::launch_prefix_tc): rows are
+    // (group member, query head) pairs of a decode batch, all attending to
+    // the group's shared tokens [t_lo, t_hi) of one token chunk; the result is
+    // a log-sum-exp partial in the decode workspace
+    const int32_t *pfx_group_start, *pfx_group_seqs, *pfx_shared_len;
+    float *pfx_acc, *pfx_ml;
+    int pfx_G, pfx_nc, pfx_nmt, pfx_members, pfx_rowslots, pfx_pslot0, pfx_B;
 };
 
 // Swizzled address of 16-byte chunk `c` of row `r` in a tile of rows of
@@ -626,7 +634,8 @@ struct Tc2Layout {
     static constexpr int OFF_SLOT = OFF_BAR + 8 * N_BAR;
     static constexpr int OFF_BT = OFF_SLOT + 16;
     static constexpr int BT_MAX = 1024;
-    static constexpr int SMEM = OFF_BT + 4 * BT_MAX + 1024;
+    static constexpr int OFF_ROWS = OFF_BT + 4 * BT_MAX;  // prefix mode: row of each of 256
+    static constexpr int SMEM = OFF_ROWS + 8 * 256 + 1024;
 };
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
@@ -642,7 +651,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(pa::smem_u32(bar)) : "memory");
 }
 
-template <int D, int GQ>
+template <int D, int GQ, bool PFX>
 __global__ void __launch_bounds__(kT2Threads, 1)
     prefill_tc2_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap) {
@@ -663,64 +672,129 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     volatile int *fail = reinterpret_cast<volatile int *>(smem + Lay::OFF_SLOT + 4);
     int32_t *bt_s = reinterpret_cast<int32_t *>(smem + Lay::OFF_BT);
 
-    // Work item: the (request, query tile) pair of rank blockIdx.x / Hkv when
-    // all pairs are ordered by decreasing number of K/V tiles (longest
-    // first, so the biggest items do not form the tail), KV head
-    // blockIdx.x % Hkv.  Pairs that do not exist (t0 >= n) cost -1.
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nqt = (p.max_query_len + QTOK - 1) / QTOK;
-    const int npairs = p.R * nqt;
-    int *pick = reinterpret_cast<int *>(smem + Lay::OFF_SLOT + 8);
-    auto cost = [&](int pair) {
-        const int rr = pair / nqt, tq = (pair % nqt) * QTOK;
-        const int nr = p.query_start[rr + 1] - p.query_start[rr];
-        if (tq >= nr) return -1;
-        const int Pr = p.context_lens[rr] - nr;
-        return (Pr + tq + QTOK + kT2KT - 1) / kT2KT;
-    };
-    const int want = blockIdx.x / p.Hkv, hk = blockIdx.x % p.Hkv;
-    int pair = want;  // natural order when there are too many pairs to rank
-    if (npairs <= kT2RankMax) {
-        int *costs = reinterpret_cast<int *>(smem + Lay::OFF_BT);  // reused below
-        for (int i = tid; i < npairs; i += kT2Threads) costs[i] = cost(i);
-        if (tid == 0) *pick = -1;
-        __syncthreads();
-        for (int i = tid; i < npairs; i += kT2Threads) {
-            const int ci = costs[i];
-            int rank = 0;
-            for (int j = 0; j < npairs; ++j) {
-                const int cj = costs[j];
-                rank += (cj > ci || (cj == ci && j < i)) ? 1 : 0;
-            }
-            if (rank == want) *pick = i;
+    // launched as a programmatic dependent in prefix mode: inputs are ready
+    // past this point (a no-op otherwise)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    int hk, kv_end, ntiles, nblk;
+    const int32_t *bt_g;
+    int qs = 0, n = 0, t0 = 0, P = 0;            // chunked-prefill work item
+    int pm0 = 0, pmend = 0, pS = 0, pchunk = 0;  // prefix-mode work item
+    if constexpr (PFX) {
+        // blockIdx.x = ((group * member tiles + member tile) * chunks + chunk)
+        //              * Hkv + KV head
+        hk = blockIdx.x % p.Hkv;
+        int rest = blockIdx.x / p.Hkv;
+        pchunk = rest % p.pfx_nc;
+        rest /= p.pfx_nc;
+        const int mt = rest % p.pfx_nmt, g = rest / p.pfx_nmt;
+        const int mbeg = p.pfx_group_start[g], mend = p.pfx_group_start[g + 1];
+        if (mbeg < 0 || mend > p.pfx_members || mbeg > mend) {
+            if (tid == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+            return;
         }
-        __syncthreads();
-        pair = *pick;
+        pm0 = mbeg + mt * QTOK;
+        pmend = mend;
+        if (pm0 >= mend) return;
+        const int b0 = p.pfx_group_seqs[mbeg];  // its table row holds the shared blocks
+        if (b0 >= 0 && b0 < p.pfx_B) {
+            pS = p.pfx_shared_len[b0];
+            const int L0 = p.context_lens[b0];
+            if (pS < 0 || pS >= L0 || (pS & (p.bs - 1)) || pS > (p.MB << p.bs_log2)) pS = 0;
+        }
+        if (pS == 0) {
+            if (tid == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+            return;
+        }
+        const int ch = ((pS + kT2KT - 1) / kT2KT + p.pfx_nc - 1) / p.pfx_nc * kT2KT;
+        const int t_lo = min(pS, pchunk * ch), t_hi = min(pS, t_lo + ch);
+        kv_end = t_hi - t_lo;  // token indices below are relative to t_lo
+        ntiles = (kv_end + kT2KT - 1) / kT2KT;
+        nblk = (kv_end + p.bs - 1) >> p.bs_log2;
+        bt_g = p.block_table + static_cast<size_t>(b0) * p.MB + (t_lo >> p.bs_log2);
+    } else {
+        // Work item: the (request, query tile) pair of rank blockIdx.x / Hkv when
+        // all pairs are ordered by decreasing number of K/V tiles (longest
+        // first, so the biggest items do not form the tail), KV head
+        // blockIdx.x % Hkv.  Pairs that do not exist (t0 >= n) cost -1.
+        const int nqt = (p.max_query_len + QTOK - 1) / QTOK;
+        const int npairs = p.R * nqt;
+        int *pick = reinterpret_cast<int *>(smem + Lay::OFF_SLOT + 8);
+        auto cost = [&](int pair) {
+            const int rr = pair / nqt, tq = (pair % nqt) * QTOK;
+            const int nr = p.query_start[rr + 1] - p.query_start[rr];
+            if (tq >= nr) return -1;
+            const int Pr = p.context_lens[rr] - nr;
+            return (Pr + tq + QTOK + kT2KT - 1) / kT2KT;
+        };
+        const int want = blockIdx.x / p.Hkv;
+        hk = blockIdx.x % p.Hkv;
+        int pair = want;  // natural order when there are too many pairs to rank
+        if (npairs <= kT2RankMax) {
+            int *costs = reinterpret_cast<int *>(smem + Lay::OFF_BT);  // reused below
+            for (int i = tid; i < npairs; i += kT2Threads) costs[i] = cost(i);
+            if (tid == 0) *pick = -1;
+            __syncthreads();
+            for (int i = tid; i < npairs; i += kT2Threads) {
+                const int ci = costs[i];
+                int rank = 0;
+                for (int j = 0; j < npairs; ++j) {
+                    const int cj = costs[j];
+                    rank += (cj > ci || (cj == ci && j < i)) ? 1 : 0;
+                }
+                if (rank == want) *pick = i;
+            }
+            __syncthreads();
+            pair = *pick;
+        }
+        if (pair < 0) return;
+        const int r = pair / nqt, qt = pair % nqt;
+        qs = p.query_start[r];
+        n = p.query_start[r + 1] - qs;
+        t0 = qt * QTOK;
+        if (t0 >= n) return;
+        const int cap = p.MB << p.bs_log2;
+        const int L = p.context_lens[r];
+        if (L > cap || L < n) {
+            if (threadIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+            return;
+        }
+        P = L - n;
+        kv_end = min(L, P + t0 + QTOK);
+        ntiles = (kv_end + kT2KT - 1) / kT2KT;
+        nblk = (kv_end + p.bs - 1) >> p.bs_log2;
+        bt_g = p.block_table + static_cast<size_t>(r) * p.MB;
     }
-    if (pair < 0) return;
-    const int r = pair / nqt, qt = pair % nqt;
-    const int qs = p.query_start[r];
-    const int n = p.query_start[r + 1] - qs;
-    const int t0 = qt * QTOK;
-    if (t0 >= n) return;
-    const int cap = p.MB << p.bs_log2;
-    const int L = p.context_lens[r];
-    if (L > cap || L < n) {
-        if (threadIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
-        return;
-    }
-    const int P = L - n;
-    const int kv_end = min(L, P + t0 + QTOK);
-    const int ntiles = (kv_end + kT2KT - 1) / kT2KT;
-    const int nblk = (kv_end + p.bs - 1) >> p.bs_log2;
     if (nblk > Lay::BT_MAX) {  // the host routes such requests elsewhere
         if (tid == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
         return;
     }
+    // prefix mode: the decode-workspace row of CTA row m (-1: no member)
+    auto pfx_row = [&](int m) -> int64_t {
+        const int mem = pm0 + m / GQ;
+        if (mem >= pmend) return -1;
+        const int b = p.pfx_group_seqs[mem];
+        if (b < 0 || b >= p.pfx_B || p.pfx_shared_len[b] != pS) return -1;
+        return static_cast<int64_t>(b) * p.Hq + hk * GQ + m % GQ;
+    };
+    if constexpr (PFX) {
+        if (ntiles == 0) {
+            // a chunk past this group's prefix: neutral partials (weight 0)
+            for (int m = tid; m < 256; m += kT2Threads) {
+                const int64_t row = pfx_row(m);
+                if (row < 0) continue;
+                const size_t slot = static_cast<size_t>(row) * p.pfx_rowslots + p.pfx_pslot0 + pchunk;
+                *reinterpret_cast<float2 *>(p.pfx_ml + 2 * slot) = make_float2(-INFINITY, 0.f);
+                for (int c = 0; c < D; c += 4)
+                    *reinterpret_cast<float4 *>(p.pfx_acc + slot * D + c) =
+                        make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            return;
+        }
+    }
 
     // ---- set-up: block-table slice, barriers, TMEM; then the loader starts
     // while warps 0-8 bring in the Q tiles (cp.async) ------------------------------
-    const int32_t *bt_g = p.block_table + static_cast<size_t>(r) * p.MB;
     for (int i = tid; i < nblk; i += kT2Threads) {
         int b = bt_g[i];
         if (b < 0 || b >= p.num_blocks) {
@@ -728,6 +802,10 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             b = 0;
         }
         bt_s[i] = b;
+    }
+    int64_t *rows_s = reinterpret_cast<int64_t *>(smem + Lay::OFF_ROWS);
+    if constexpr (PFX) {
+        for (int m = tid; m < 256; m += kT2Threads) rows_s[m] = pfx_row(m);
     }
     if (tid == 0) {
         for (int i = 0; i < kT2NST; ++i) {
@@ -753,11 +831,18 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         constexpr int kQThreads = kT2Threads - 32;
         for (int idx = tid; idx < 256 * CH; idx += kQThreads) {
             const int m = idx / CH, c = idx % CH;  // row m of the CTA's 256
-            const int t = t0 + m / GQ;
-            const bool valid = t < n;
-            const __nv_bfloat16 *src =
-                p.q + (static_cast<size_t>(qs + (valid ? t : 0)) * p.Hq + hk * GQ + m % GQ) * D +
-                c * 8;
+            bool valid;
+            const __nv_bfloat16 *src;
+            if constexpr (PFX) {
+                const int64_t row = rows_s[m];
+                valid = row >= 0;
+                src = p.q + (valid ? row : 0) * D + c * 8;
+            } else {
+                const int t = t0 + m / GQ;
+                valid = t < n;
+                src = p.q + (static_cast<size_t>(qs + (valid ? t : 0)) * p.Hq + hk * GQ + m % GQ) * D +
+                      c * 8;
+            }
             const uint32_t tile = sq + (m >> 7) * (128 * D * 2);
             cp_async16(tile + pa::tc::sw128(m & 127, c * 8, 128), src, valid);
         }
@@ -877,7 +962,8 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const uint32_t o_col = wg * 128;
         const int m = wg * 128 + row;
-        const int pos = P + min(t0 + m / GQ, n - 1);
+        // last key position this row sees (prefix mode: every key of the chunk)
+        const int pos = PFX ? kv_end - 1 : P + min(t0 + m / GQ, n - 1);
         const float qs2 = p.qscale;  // softmax scale in log2 units
         float m_used = -INFINITY, lsum = 0.f;
         bool ok = true;
@@ -973,7 +1059,30 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             if (lane == 0) mbar_arrive(&p_full[wg]);
         }
         if (ok) ok = pa::mbar_wait(&o_done[wg], (ntiles - 1) & 1);
-        if (ok) {
+        if (ok && PFX) {
+            // partial of this (member, head) row over the chunk: unnormalised
+            // O, running max and sum, into its prefix slot
+            pa::tc::fence_after();
+            const int64_t prow = rows_s[m];
+            const size_t slot =
+                static_cast<size_t>(prow < 0 ? 0 : prow) * p.pfx_rowslots + p.pfx_pslot0 + pchunk;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o[32];
+                pa::tc::ld32(lane_base + o_col + c0, o);
+                pa::tc::wait_ld();
+                if (prow >= 0) {
+                    float *dst = p.pfx_acc + slot * D + c0;
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        *reinterpret_cast<float4 *>(dst + c) =
+                            make_float4(__uint_as_float(o[c]), __uint_as_float(o[c + 1]),
+                                        __uint_as_float(o[c + 2]), __uint_as_float(o[c + 3]));
+                }
+            }
+            if (prow >= 0)
+                *reinterpret_cast<float2 *>(p.pfx_ml + 2 * slot) = make_float2(m_used, lsum);
+        } else if (ok) {
             pa::tc::fence_after();
             const int t = t0 + m / GQ;
             const float inv = 1.f / lsum;
@@ -1071,7 +1180,7 @@ int launch_tc2(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
     if (int rc = pa::pool_tensor_map(&kmap, p.k_cache, rows, D, p.bs)) return rc;
     if (int rc = pa::pool_tensor_map(&vmap, p.v_cache, rows, D, p.bs)) return rc;
     const size_t smem = Tc2Layout<D>::SMEM;
-    auto kern = prefill_tc2_kernel<D, GQ>;
+    auto kern = prefill_tc2_kernel<D, GQ, false>;
     static std::atomic<uint64_t> attr_done{0};
     if (int rc = set_smem_once(kern, smem, &attr_done)) return rc;
     (void)cudaGetLastError();
@@ -1114,7 +1223,89 @@ int dispatch_gq(int gq, const PrefillParams &p, int mq, cudaStream_t s) {
     }
 }
 
+template <int D, int GQ>
+int launch_prefix_tc_t(const pa::PrefixTcArgs &a, cudaStream_t stream) {
+    PrefillParams p{};
+    p.q = static_cast<const __nv_bfloat16 *>(a.q);
+    p.k_cache = static_cast<const uint8_t *>(a.k_cache);
+    p.v_cache = static_cast<const uint8_t *>(a.v_cache);
+    p.block_table = a.block_table;
+    p.context_lens = a.context_lens;
+    p.err = a.err;
+    p.num_blocks = a.num_blocks;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.bs = a.bs;
+    p.bs_log2 = log2_int(a.bs);
+    p.MB = a.MB;
+    p.qscale = a.qscale;
+    p.pfx_group_start = a.group_start;
+    p.pfx_group_seqs = a.group_seqs;
+    p.pfx_shared_len = a.shared_len;
+    p.pfx_acc = a.acc;
+    p.pfx_ml = a.ml;
+    p.pfx_G = a.G;
+    p.pfx_nc = a.nc;
+    constexpr int qtok = 256 / GQ;
+    p.pfx_nmt = (a.max_group_size + qtok - 1) / qtok;
+    p.pfx_members = a.num_members;
+    p.pfx_rowslots = a.rowslots;
+    p.pfx_pslot0 = a.pslot0;
+    p.pfx_B = a.B;
+    const int64_t rows = (a.num_blocks * a.Hkv) << p.bs_log2;
+    CUtensorMap kmap, vmap;
+    if (int rc = pa::pool_tensor_map(&kmap, a.k_cache, rows, D, a.bs)) return rc;
+    if (int rc = pa::pool_tensor_map(&vmap, a.v_cache, rows, D, a.bs)) return rc;
+    const size_t smem = Tc2Layout<D>::SMEM;
+    auto kern = prefill_tc2_kernel<D, GQ, true>;
+    static std::atomic<uint64_t> attr_done{0};
+    if (int rc = set_smem_once(kern, smem, &attr_done)) return rc;
+    const int64_t ctas = int64_t(p.pfx_nmt) * a.G * a.nc * a.Hkv;
+    if (ctas > 0x7fffffff) return pa::fail(PA_ERR_INVALID, "decode_shared: prefix grid too large");
+    if (ctas == 0) return PA_OK;
+    (void)cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(kT2Threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p, kmap, vmap);
+    if (e != cudaSuccess) return pa::cuda_fail(e, "decode_shared: prefix launch");
+    return pa::check_launch("decode_shared: prefix launch");
+}
+
 }  // namespace
+
+namespace pa {
+
+bool prefix_tc_ok(int bs, int64_t num_blocks, int Hkv, int max_chunk_tokens) {
+    return bs >= 8 && bs <= 64 && (num_blocks * Hkv * bs) < (int64_t(1) << 31) &&
+           (max_chunk_tokens + bs - 1) / bs <= Tc2Layout<128>::BT_MAX;
+}
+
+int launch_prefix_tc(const PrefixTcArgs &a, cudaStream_t stream) {
+    const int gq = a.Hq / a.Hkv;
+    auto pick = [&](auto d) -> int {
+        constexpr int D = decltype(d)::value;
+        switch (gq) {
+            case 1: return launch_prefix_tc_t<D, 1>(a, stream);
+            case 2: return launch_prefix_tc_t<D, 2>(a, stream);
+            case 4: return launch_prefix_tc_t<D, 4>(a, stream);
+            case 8: return launch_prefix_tc_t<D, 8>(a, stream);
+            default: return pa::fail(PA_ERR_UNSUPPORTED, "decode_shared: Hq/Hkv=%d", gq);
+        }
+    };
+    if (a.D == 128) return pick(std::integral_constant<int, 128>{});
+    if (a.D == 64) return pick(std::integral_constant<int, 64>{});
+    return pa::fail(PA_ERR_UNSUPPORTED, "decode_shared: head_dim %d", a.D);
+}
+
+}  // namespace pa
 
 extern "C" int pa_prefill_chunk(void *out, const void *q, const void *k_cache, const void *v_cache,
                                 const int32_t *block_table, int max_blocks_per_seq,

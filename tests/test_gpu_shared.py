@@ -176,3 +176,14 @@ def test_shared_small_batch_and_fp32_decode_whole():
     wf = synth.shared_groups_workload([(64, 4)], singles=120, seed=10, dtype=torch.float32)
     out, plain = run_shared(wf, partition_tokens=64)
     assert torch.equal(out, plain)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (16, 2)])
+def test_shared_groups_large_blocks_warp_level_prefix(Hq, Hkv):
+    """128-token blocks: the prefix partials come from the warp-level
+    tensor-core prefix kernel (the tcgen05 prefill kernel takes blocks of
+    8..64 tokens); every output against the oracle."""
+    w = synth.shared_groups_workload([(4 * 128, 9), (2 * 128, 5)], singles=300, seed=40 + Hq,
+                                     Hq=Hq, Hkv=Hkv, bs=128)
+    out, _ = run_shared(w, partition_tokens=128)
+    compare(out.double().cpu().numpy(), oracle_decode_all(w), torch.bfloat16, f"bs128 {Hq}/{Hkv}")

@@ -280,9 +280,22 @@ class DecodePlan(Plan):
                 pos += nb_
             w.table = table
         self.w = w
+        self.contig = args.layout == "contiguous"
+        # contiguous control: every sequence reserves the config's maximum length
+        self.max_len = -(-synth.CONFIGS[name]["len_range"][1] // 32) * 32
         for _ in range(args.pools):
-            kc, vc = layout.alloc_pools(w.num_blocks, w.Hkv, w.bs, w.d, w.dtype, dev, poison=False)
-            layout.fill_pools(kc, vc, w.k, w.v, w.table, w.lens, w.bs)
+            if self.contig:
+                kc = torch.zeros(w.B, w.Hkv, self.max_len, w.d, dtype=w.dtype, device=dev)
+                vc = torch.zeros_like(kc)
+                offs = w.kv_offsets
+                for b_ in range(w.B):
+                    L_ = int(w.lens[b_])
+                    kc[b_, :, :L_] = w.k[offs[b_]:offs[b_] + L_].to(dev).transpose(0, 1)
+                    vc[b_, :, :L_] = w.v[offs[b_]:offs[b_] + L_].to(dev).transpose(0, 1)
+            else:
+                kc, vc = layout.alloc_pools(w.num_blocks, w.Hkv, w.bs, w.d, w.dtype, dev,
+                                            poison=False)
+                layout.fill_pools(kc, vc, w.k, w.v, w.table, w.lens, w.bs)
             self.pools.append((kc, vc))
         if w.k.is_cuda:  # keep only the pools on the device
             w.k, w.v, w.q = w.k.cpu(), w.v.cpu(), w.q.cpu()
@@ -298,16 +311,31 @@ class DecodePlan(Plan):
         self.ws_bytes = ops.decode_workspace_size(w.B, w.Hq, w.d, w.max_blocks, w.bs, self.PT)
         self.decode_kernel, n_dec = decode_kernel_info(w.B, w.Hq, w.Hkv, w.d, w.max_blocks, w.bs,
                                                         w.num_blocks, self.PT)
-        self.ws = torch.zeros(max(self.ws_bytes // 4, 1), dtype=torch.float32, device=dev)
         self.decode_bytes = decode_bytes(w.lens, w.B, w.Hq, w.Hkv, w.d, w.bs, w.dtype)
         self.step_bytes = self.decode_bytes + store_bytes(w.B, w.Hkv, w.d, w.dtype)
-        self.tokens = w.B
         self.launches = 1 + n_dec
+        if self.contig:
+            # the same decode over contiguous reservations: no table, no store
+            self.ws_bytes = ops.decode_contiguous_workspace_size(w.B, w.Hq, w.d, self.max_len,
+                                                                 self.PT)
+            self.decode_kernel = ("pa_decode_contiguous (decode_persistent_kernel over "
+                                  f"[B][Hkv][{self.max_len}][d] reservations, then "
+                                  "partial_merge_kernel)")
+            self.decode_bytes -= int(sum(-(-int(L) // w.bs) for L in w.lens)) * 4
+            self.step_bytes = self.decode_bytes
+            self.launches = 2
+            self.inputs = {k_: self.inputs[k_] for k_ in ("q", "lens")}
+        self.ws = torch.zeros(max(self.ws_bytes // 4, 1), dtype=torch.float32, device=dev)
+        self.tokens = w.B
         lo, hi = synth.CONFIGS[name]["len_range"]
         self.config = {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d, "block_size": w.bs,
                        "context_len": f"U[{lo},{hi}] seed {args.seed}",
                        "total_context_tokens": int(w.lens.sum()), "pool_blocks": w.num_blocks,
                        "partition_tokens": self.PT, "placement": args.placement}
+        if self.contig:
+            self.config.update(layout=f"contiguous [B][Hkv][{self.max_len}][d] reservations "
+                                      "(paging-overhead control; step = decode only)",
+                               placement=None, pool_blocks=None)
         paged, contig = layout.kv_utilization(w.lens, w.bs, hi)
         self.extra = {"kv_utilization_paged": round(paged, 4),
                       f"kv_utilization_contiguous_reserve_{hi}": round(contig, 4),
@@ -318,6 +346,17 @@ class DecodePlan(Plan):
         from paged_kv_cache_192_gb300._lib import PA_BF16, check
         w, x = self.w, (src or self.inputs)
         kc, vc = self.pools[i % len(self.pools)]
+        if self.contig:
+            if ev:
+                ev["decode"][0].record()
+            check(L.pa_decode_contiguous((dst or self.outputs)["out"].data_ptr(),
+                                         x["q"].data_ptr(), kc.data_ptr(), vc.data_ptr(),
+                                         x["lens"].data_ptr(), w.B, w.Hq, w.Hkv, w.d,
+                                         self.max_len, 1.0 / math.sqrt(w.d), self.PT,
+                                         self.ws.data_ptr(), self.ws_bytes, PA_BF16, sp))
+            if ev:
+                ev["decode"][1].record()
+            return
         check(L.pa_reshape_and_cache(x["k_new"].data_ptr(), x["v_new"].data_ptr(), kc.data_ptr(),
                                      vc.data_ptr(), x["slots"].data_ptr(), w.B, w.num_blocks,
                                      w.Hkv, w.bs, w.d, PA_BF16, sp))
@@ -823,6 +862,9 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0,
                     help="override the decode workload's batch size (small profiling cases "
                          "of the same shape)")
+    ap.add_argument("--layout", choices=["paged", "contiguous"], default="paged",
+                    help="decode workloads: paged pools, or the contiguous-reservation control "
+                         "(pa_decode_contiguous, no block table)")
     ap.add_argument("--prefix-path", choices=["shared", "plain"], default="shared",
                     help="prefix workload: decode with the shared-prefix groups (pa_decode_shared) "
                          "or every sequence whole (pa_decode)")

@@ -223,6 +223,31 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               int dtype, pa_stream_t stream);
 
 /*
+ * pa_decode_contiguous -- the decode of pa_decode over a plain contiguous
+ * cache, for measuring what paging costs: each sequence reserves max_len
+ * slots up front, the reservation that paging replaces ("Apa itu
+ * PagedAttention?", section "Masalah fragmentasi memori KV Cache
+ * konvensional"), so no block table is read and no address depends on a
+ * table entry.  Following the block table is the cost paging adds
+ * ("PagedAttention: memetakan blok KV logis ke memori fisik tidak kontigu",
+ * section "Kernel attention harus mengikuti block table").  The kernel is
+ * pa_decode's persistent kernel with the same tiles and split; only the
+ * address of a tile differs.
+ *   k, v   [B][Hkv][max_len][head_dim] device arrays (dtype); token j of
+ *          sequence b, KV head h at row (b * Hkv + h) * max_len + j
+ *   max_len  a positive multiple of 32; context_lens[b] in [1, max_len]
+ *   workspace  at least pa_decode_contiguous_workspace_size bytes
+ * Other arguments and the result as for pa_decode.  At most 1024 sequences
+ * (PA_ERR_UNSUPPORTED beyond).
+ */
+int pa_decode_contiguous_workspace_size(int B, int Hq, int head_dim, int max_len,
+                                        int partition_tokens, size_t *bytes);
+int pa_decode_contiguous(void *out, const void *q, const void *k, const void *v,
+                         const int32_t *context_lens, int B, int Hq, int Hkv, int head_dim,
+                         int max_len, float scale, int partition_tokens, void *workspace,
+                         size_t workspace_bytes, int dtype, pa_stream_t stream);
+
+/*
  * pa_decode_shared -- pa_decode for a batch in which groups of sequences share
  * the physical blocks of a common prefix: a system prompt, or the history of
  * parallel-sampling branches forked from one parent.  A shared block is one

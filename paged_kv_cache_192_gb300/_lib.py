@@ -43,6 +43,10 @@ SIGNATURES = {
     "pa_decode": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_int,
                            _c_int, _c_int, _c_int, _c_i64, _c_f, _c_int, _c_vp, _c_sz, _c_int,
                            _c_vp]),
+    "pa_decode_contiguous_workspace_size": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int,
+                                                     ctypes.POINTER(_c_sz)]),
+    "pa_decode_contiguous": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int,
+                                      _c_int, _c_int, _c_f, _c_int, _c_vp, _c_sz, _c_int, _c_vp]),
     "pa_decode_shared_workspace_size": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                  _c_int, ctypes.POINTER(_c_sz)]),
     "pa_decode_shared": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int,

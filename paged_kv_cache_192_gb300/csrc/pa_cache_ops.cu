@@ -7,6 +7,10 @@
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
+#ifndef PA_STORE_PDL
+#define PA_STORE_PDL 1  // 0: ordinary stream-ordered launch (A/B of the dependent launch)
+#endif
+
 namespace {
 
 // One thread per 16-byte chunk of one (token, KV head) row.  Source rows are
@@ -165,7 +169,7 @@ int pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cache, vo
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = PA_STORE_PDL ? 1 : 0;
     const cudaError_t e = cudaLaunchKernelEx(
         &cfg, reshape_and_cache_kernel, static_cast<const uint4 *>(k_new),
         static_cast<const uint4 *>(v_new), static_cast<uint4 *>(k_cache),

@@ -139,6 +139,7 @@ struct DecodeParams {
     int B, Hq, Hkv, bs, bs_log2, MB, PT, max_parts, maxseg;
     int rowslots;                // partial slots per (sequence, query head)
     int pslot0, npfx;            // shared-prefix partials: slots pslot0 .. pslot0+npfx-1
+    int contig_len;              // > 0: contiguous caches [B][Hkv][contig_len][D], no table
     float qscale;                // scale * log2(e)
 };
 
@@ -739,8 +740,14 @@ __device__ __forceinline__ Cursor next_unit(Cursor c, const BatchTables &bt, int
 
 template <int TT>
 __device__ __forceinline__ int block_entry(const DecodeParams &p, const Cursor &c, int j) {
+    if (p.contig_len) return 0;  // contiguous caches: no block table
     return __ldg(p.block_table + static_cast<size_t>(c.b) * p.MB +
                  (first_token(c, TT) >> p.bs_log2) + j);
+}
+
+// Contiguous caches: first row of tile c, as a row index of [B][Hkv][len][D].
+__device__ __forceinline__ int64_t contig_row(const DecodeParams &p, const Cursor &c, int tok) {
+    return (static_cast<int64_t>(c.b) * p.Hkv + c.hk) * p.contig_len + tok;
 }
 
 __device__ __forceinline__ int checked_block(const DecodeParams &p, int v) {
@@ -759,7 +766,12 @@ __device__ __forceinline__ void produce_tile(const DecodeParams &p, const Cursor
     uint8_t *dk = stage;
     uint8_t *dv = stage + C::TILE;
     const int tok = first_token(c, C::TT);
-    if (C::TT <= p.bs) {
+    if (p.contig_len) {  // one copy of TT whole rows per cache (contig_len % 32 == 0)
+        const size_t off = static_cast<size_t>(contig_row(p, c, tok)) * C::ROW;
+        pa::mbar_arrive_expect_tx(bar, 2 * C::TILE);
+        pa::bulk_g2s(dk, p.k_cache + off, C::TILE, bar);
+        pa::bulk_g2s(dv, p.v_cache + off, C::TILE, bar);
+    } else if (C::TT <= p.bs) {
         const int r0 = tok & (p.bs - 1);
         const size_t off = ((static_cast<size_t>(blk) * p.Hkv + c.hk) * p.bs + r0) * C::ROW;
         pa::mbar_arrive_expect_tx(bar, 2 * C::TILE);
@@ -793,8 +805,9 @@ __device__ __forceinline__ void produce_tile_tma(const DecodeParams &p, const Cu
     using C = MmaCfg<D, GQ>;
     const uint32_t sk = pa::smem_u32(stage), sv = sk + C::TILE;
     const int tok = first_token(c, C::TT);
-    if (C::TT <= p.bs) {
-        const int y = (blk * p.Hkv + c.hk) * p.bs + (tok & (p.bs - 1));
+    if (p.contig_len || C::TT <= p.bs) {
+        const int y = p.contig_len ? static_cast<int>(contig_row(p, c, tok))
+                                   : (blk * p.Hkv + c.hk) * p.bs + (tok & (p.bs - 1));
         pa::mbar_arrive_expect_tx(bar, 2 * C::TILE);
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h) {
@@ -834,11 +847,13 @@ __device__ __forceinline__ void produce_tile_lanes(const DecodeParams &p, const 
         const int t = tok + row;
         if (t >= c.L) continue;  // rows past the end stay stale and are masked
         int id = blk;
-        if (C::TT > p.bs && (t >> p.bs_log2) != (tok >> p.bs_log2))
+        if (!p.contig_len && C::TT > p.bs && (t >> p.bs_log2) != (tok >> p.bs_log2))
             id = checked_block(p, __ldg(p.block_table + static_cast<size_t>(c.b) * p.MB +
                                         (t >> p.bs_log2)));
         const size_t off =
-            ((static_cast<size_t>(id) * p.Hkv + c.hk) * p.bs + (t & (p.bs - 1))) * C::ROW +
+            (p.contig_len ? static_cast<size_t>(contig_row(p, c, t))
+                          : (static_cast<size_t>(id) * p.Hkv + c.hk) * p.bs + (t & (p.bs - 1))) *
+                C::ROW +
             within * 16;
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sk + ch * 16),
                      "l"(p.k_cache + off)
@@ -1525,6 +1540,9 @@ bool partition_ok(int pt, int bs) {
 // Launch `kern` as a programmatic dependent of the previous kernel in the
 // stream: its CTAs may start while that kernel drains and wait for it with
 // griddepcontrol.wait.
+#ifndef PA_DECODE_PDL
+#define PA_DECODE_PDL 1  // 0: ordinary stream-ordered launches (A/B of the dependent launch)
+#endif
 template <typename... KArgs, typename... Args>
 cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                              cudaStream_t stream, Args &&...args) {
@@ -1537,7 +1555,7 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = PA_DECODE_PDL ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
@@ -1718,7 +1736,8 @@ int launch(const DecodeParams &p, const SharedPlan *sp, cudaStream_t stream) {
     }
     const int sms = sm_count();
     if (sms <= 0) return pa::fail(PA_ERR_CUDA, "decode: no SM count");
-    if (kernel_for(p.B, p.Hkv, p.MB, p.bs_log2, p.max_parts - 1, sms) != PA_DECODE_PERSISTENT)
+    if (!p.contig_len &&
+        kernel_for(p.B, p.Hkv, p.MB, p.bs_log2, p.max_parts - 1, sms) != PA_DECODE_PERSISTENT)
         return launch_grid<T, D, GQ>(p, stream);
     if constexpr (std::is_same<T, __nv_bfloat16>::value && GQ % 2 == 0 &&
                   GQ >= PA_DECODE_MMA_MIN_GQ)
@@ -1885,7 +1904,7 @@ int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cac
                 const int32_t *block_table, int max_blocks_per_seq, const int32_t *context_lens,
                 int B, int Hq, int Hkv, int head_dim, int block_size, int64_t num_blocks,
                 float scale, int partition_tokens, const SharedArgs *sh, void *workspace,
-                size_t workspace_bytes, int dtype, cudaStream_t stream) {
+                size_t workspace_bytes, int dtype, cudaStream_t stream, int contig_len = 0) {
     if (dtype != PA_BF16 && dtype != PA_F32) return pa::fail(PA_ERR_INVALID, "decode: bad dtype");
     if (B < 0 || B > 65535 || Hq <= 0 || Hkv <= 0 || Hkv > 65535 || Hq % Hkv || num_blocks <= 0 ||
         max_blocks_per_seq <= 0)
@@ -1907,7 +1926,7 @@ int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cac
     if (!(scale > 0.f) || !std::isfinite(scale))
         return pa::fail(PA_ERR_INVALID, "decode: scale must be positive and finite");
     if (B == 0) return PA_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens)
+    if (!out || !q || !k_cache || !v_cache || (!block_table && !contig_len) || !context_lens)
         return pa::fail(PA_ERR_INVALID, "decode: NULL pointer");
     if (!pa::aligned16(q) || !pa::aligned16(out) || !pa::aligned16(k_cache) ||
         !pa::aligned16(v_cache))
@@ -1925,15 +1944,17 @@ int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cac
     if (!pa::aligned16(workspace))
         return pa::fail(PA_ERR_INVALID, "decode: workspace must be 16-byte aligned");
     if (pa::validate_on()) {
-        std::vector<int32_t> lens(B), table(size_t(B) * max_blocks_per_seq);
+        std::vector<int32_t> lens(B), table(contig_len ? 0 : size_t(B) * max_blocks_per_seq);
         if (int rc = pa::fetch(lens.data(), context_lens, B * sizeof(int32_t), stream)) return rc;
-        if (int rc = pa::fetch(table.data(), block_table, table.size() * sizeof(int32_t), stream))
-            return rc;
+        if (!contig_len)
+            if (int rc = pa::fetch(table.data(), block_table, table.size() * sizeof(int32_t),
+                                   stream))
+                return rc;
         for (int b = 0; b < B; ++b) {
             if (lens[b] < 1 || lens[b] > cap)
                 return pa::fail(PA_ERR_INVALID, "validate: context_lens[%d]=%d outside [1,%lld]", b,
                                 lens[b], (long long)cap);
-            const int nb = (lens[b] + block_size - 1) / block_size;
+            const int nb = contig_len ? 0 : (lens[b] + block_size - 1) / block_size;
             for (int i = 0; i < nb; ++i) {
                 const int32_t v = table[size_t(b) * max_blocks_per_seq + i];
                 if (v < 0 || v >= num_blocks)
@@ -1972,6 +1993,7 @@ int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cac
     p.shared_len = nullptr;
     p.pslot0 = max_parts + 1;
     p.npfx = 0;
+    p.contig_len = contig_len;
     p.qscale = scale * kLog2e;
     const int gq = Hq / Hkv;
     // Shared-prefix path: bf16 batches that run on the persistent kernel and
@@ -2031,6 +2053,35 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     return decode_impl(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, B,
                        Hq, Hkv, head_dim, block_size, num_blocks, scale, partition_tokens, nullptr,
                        workspace, workspace_bytes, dtype, stream);
+}
+
+int pa_decode_contiguous_workspace_size(int B, int Hq, int head_dim, int max_len,
+                                        int partition_tokens, size_t *bytes) {
+    pa::clear_error();
+    if (max_len <= 0 || max_len % 32)
+        return pa::fail(PA_ERR_INVALID, "contiguous_workspace_size: max_len must be a positive "
+                                        "multiple of 32");
+    return pa_decode_workspace_size(B, Hq, head_dim, max_len / 16, 16, partition_tokens, bytes);
+}
+
+int pa_decode_contiguous(void *out, const void *q, const void *k, const void *v,
+                         const int32_t *context_lens, int B, int Hq, int Hkv, int head_dim,
+                         int max_len, float scale, int partition_tokens, void *workspace,
+                         size_t workspace_bytes, int dtype, pa_stream_t stream) {
+    pa::clear_error();
+    if (max_len <= 0 || max_len % 32 || max_len > (1 << 30))
+        return pa::fail(PA_ERR_INVALID, "decode_contiguous: max_len must be a positive "
+                                        "multiple of 32");
+    if (B > kPersistentMaxB)
+        return pa::fail(PA_ERR_UNSUPPORTED, "decode_contiguous: at most %d sequences",
+                        kPersistentMaxB);
+    if (B > 0 && int64_t(B) * max_len / 8 >= (int64_t(1) << 31))
+        return pa::fail(PA_ERR_UNSUPPORTED, "decode_contiguous: B * max_len too large");
+    // the caches viewed as B * max_len / 16 blocks of 16 rows (no table is read)
+    return decode_impl(out, q, k, v, nullptr, max_len / 16, context_lens, B, Hq, Hkv, head_dim,
+                       16, std::max<int64_t>(int64_t(B) * max_len / 16, 1), scale,
+                       partition_tokens, nullptr, workspace, workspace_bytes, dtype, stream,
+                       max_len);
 }
 
 int pa_decode_shared_workspace_size(int B, int Hq, int head_dim, int max_blocks_per_seq,

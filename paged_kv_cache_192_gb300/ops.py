@@ -201,6 +201,40 @@ def decode(q, k_cache, v_cache, block_table, context_lens, scale=None, partition
     return out
 
 
+def decode_contiguous_workspace_size(B, Hq, head_dim, max_len, partition_tokens=0):
+    out = ctypes.c_size_t(0)
+    check(lib().pa_decode_contiguous_workspace_size(B, Hq, head_dim, max_len, partition_tokens,
+                                                    ctypes.byref(out)))
+    return out.value
+
+
+def decode_contiguous(q, k, v, context_lens, scale=None, partition_tokens=0, workspace=None,
+                      out=None, stream=None):
+    """Decode over plain contiguous caches (pa_decode_contiguous): k, v
+    [B][Hkv][max_len][d], max_len a multiple of 32; no block table.  The
+    paging-overhead control of decode."""
+    _require(q.dim() == 3 and k.dim() == 4 and v.shape == k.shape,
+             "q must be [B][Hq][d], k and v [B][Hkv][max_len][d]")
+    B, Hq, d = q.shape
+    _require(k.shape[0] == B and k.shape[3] == d, f"k must be [{B}][Hkv][max_len][{d}]")
+    _require(context_lens.shape == (B,), f"context_lens must be [{B}]")
+    _require(out is None or out.shape == q.shape, "out must have the shape of q")
+    Hkv, max_len = k.shape[1], k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    nbytes = decode_contiguous_workspace_size(B, Hq, d, max_len, partition_tokens)
+    if workspace is None and nbytes:
+        workspace = torch.empty(nbytes // 4, dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(lib().pa_decode_contiguous(
+        _cuda(out, "out", q.dtype), _cuda(q, "q", k.dtype), _cuda(k, "k"), _cuda(v, "v", k.dtype),
+        _cuda(context_lens, "context_lens", torch.int32), B, Hq, Hkv, d, max_len, scale,
+        partition_tokens, ws_ptr, ws_len, _dt(q), _stream(stream)))
+    return out
+
+
 def decode_shared_workspace_size(B, Hq, head_dim, max_blocks_per_seq, block_size,
                                  partition_tokens=0, max_shared_len=0):
     out = ctypes.c_size_t(0)

@@ -164,3 +164,16 @@ def test_decode_tile_for_host_only(lib):
     out = ctypes.c_int(0)
     assert lib.pa_decode_tile_for(12, 8, 128, 16, 100, 0, ctypes.byref(out)) == 1
     assert lib.pa_decode_tile_for(32, 8, 96, 16, 100, 0, ctypes.byref(out)) == 1
+
+
+def test_contiguous_and_shared_workspace_sizes_host_only(lib):
+    """Workspace sizes of the contiguous control and of the shared-prefix
+    decode: the paged size for the same capacity, plus one prefix slot per
+    256 shared tokens for the latter; bad reservations are refused."""
+    from paged_kv_cache_192_gb300 import ops
+    assert ops.decode_contiguous_workspace_size(64, 32, 128, 4096, 512) == \
+        ops.decode_workspace_size(64, 32, 128, 256, 16, 512)
+    assert ops.decode_shared_workspace_size(320, 32, 128, 96, 16, 512, 1024) == (
+        _count_bytes(320 * 32) + 320 * 32 * (3 + 1 + 4) * 130 * 4)
+    out = ctypes.c_size_t(0)
+    assert lib.pa_decode_contiguous_workspace_size(4, 4, 128, 40, 0, ctypes.byref(out)) == 1

@@ -1468,52 +1468,94 @@ __global__ void __launch_bounds__(D) merge_kernel(const DecodeParams p) {
 template <typename T, int D, int GQ>
 __global__ void __launch_bounds__(GQ * 32) partial_merge_kernel(const DecodeParams p) {
     constexpr int EL = D / 32;
+    constexpr int kSpec = 8;  // segment slots loaded before the item's count is known
     const int item = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
     wait_prior_grids();
-    const unsigned meta = __ldcg(p.meta + item);
-    const int nseg = static_cast<int>(meta & 0xffffu), ns = nseg + static_cast<int>(meta >> 16);
-    if (ns == 0) return;  // written out by the decode
     const size_t row = static_cast<size_t>(item / p.Hkv) * p.Hq + (item % p.Hkv) * GQ + h;
     const size_t sb = row * p.rowslots;
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + sb;
     const float *src = p.ws_acc + sb * D + EL * lane;
+    // One round trip for the common case (no shared prefix, at most kSpec
+    // segments): the count, the (max, sum) of slots 0..kSpec-1 and this
+    // lane's values of them are all requested at once.
+    const int spec = min(kSpec, p.rowslots);
+    const unsigned meta = __ldcg(p.meta + item);
+    float2 v = make_float2(-INFINITY, 0.f);
+    if (lane < spec) v = __ldcg(&ml[lane]);
+    float pre[kSpec][EL];
+#pragma unroll
+    for (int i = 0; i < kSpec; ++i) {
+        if (i < spec) {
+            if constexpr (EL == 4) {
+                const float4 a = __ldcg(reinterpret_cast<const float4 *>(src + i * D));
+                pre[i][0] = a.x;
+                pre[i][1] = a.y;
+                pre[i][2] = a.z;
+                pre[i][3] = a.w;
+            } else {
+                const float2 a = __ldcg(reinterpret_cast<const float2 *>(src + i * D));
+                pre[i][0] = a.x;
+                pre[i][1] = a.y;
+            }
+        }
+    }
+    const int nseg = static_cast<int>(meta & 0xffffu), ns = nseg + static_cast<int>(meta >> 16);
+    if (ns == 0) return;  // written out by the decode
     float acc[EL];
 #pragma unroll
     for (int e = 0; e < EL; ++e) acc[e] = 0.f;
     float den = 0.f, M = -INFINITY;
-    // 32 partials at a time: lane s holds partial s's (max, sum); the weights
-    // travel by shuffle and every acc load is issued independently
-    for (int base = 0; base < ns; base += 32) {
-        const int k = min(32, ns - base);
-        float2 v = make_float2(-INFINITY, 0.f);
-        if (lane < k) v = __ldcg(&ml[slot_of(p, base + lane, nseg)]);
-        float Mc = v.x;
+    if (ns == nseg && ns <= spec) {
+        if (lane >= ns) v = make_float2(-INFINITY, 0.f);
+        M = v.x;
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(pa::kFull, Mc, o));
-        const float Mn = fmaxf(M, Mc);
-        const float rescale = M == -INFINITY ? 0.f : exp2f(M - Mn);
-        M = Mn;
-        const float wl = lane < k ? exp2f(v.x - M) : 0.f;
-        float d = wl * v.y;
+        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(pa::kFull, M, o));
+        const float wl = lane < ns ? exp2f(v.x - M) : 0.f;
+        den = wl * v.y;
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(pa::kFull, d, o);
-        den = den * rescale + d;
+        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(pa::kFull, den, o);
 #pragma unroll
-        for (int e = 0; e < EL; ++e) acc[e] *= rescale;
-#pragma unroll 8
-        for (int i = 0; i < k; ++i) {
+        for (int i = 0; i < kSpec; ++i) {
             const float f = __shfl_sync(pa::kFull, wl, i);
-            const float *sp = src + static_cast<size_t>(slot_of(p, base + i, nseg)) * D;
-            if constexpr (EL == 4) {
-                const float4 a = __ldcg(reinterpret_cast<const float4 *>(sp));
-                acc[0] += f * a.x;
-                acc[1] += f * a.y;
-                acc[2] += f * a.z;
-                acc[3] += f * a.w;
-            } else {
-                const float2 a = __ldcg(reinterpret_cast<const float2 *>(sp));
-                acc[0] += f * a.x;
-                acc[1] += f * a.y;
+            if (i < ns)
+#pragma unroll
+                for (int e = 0; e < EL; ++e) acc[e] += f * pre[i][e];
+        }
+    } else {
+        // 32 partials at a time: lane s holds partial s's (max, sum); the
+        // weights travel by shuffle and every value load is independent
+        for (int base = 0; base < ns; base += 32) {
+            const int k = min(32, ns - base);
+            float2 w2 = make_float2(-INFINITY, 0.f);
+            if (lane < k) w2 = __ldcg(&ml[slot_of(p, base + lane, nseg)]);
+            float Mc = w2.x;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(pa::kFull, Mc, o));
+            const float Mn = fmaxf(M, Mc);
+            const float rescale = M == -INFINITY ? 0.f : exp2f(M - Mn);
+            M = Mn;
+            const float wl = lane < k ? exp2f(w2.x - M) : 0.f;
+            float d = wl * w2.y;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(pa::kFull, d, o);
+            den = den * rescale + d;
+#pragma unroll
+            for (int e = 0; e < EL; ++e) acc[e] *= rescale;
+#pragma unroll 8
+            for (int i = 0; i < k; ++i) {
+                const float f = __shfl_sync(pa::kFull, wl, i);
+                const float *sp = src + static_cast<size_t>(slot_of(p, base + i, nseg)) * D;
+                if constexpr (EL == 4) {
+                    const float4 a = __ldcg(reinterpret_cast<const float4 *>(sp));
+                    acc[0] += f * a.x;
+                    acc[1] += f * a.y;
+                    acc[2] += f * a.z;
+                    acc[3] += f * a.w;
+                } else {
+                    const float2 a = __ldcg(reinterpret_cast<const float2 *>(sp));
+                    acc[0] += f * a.x;
+                    acc[1] += f * a.y;
+                }
             }
         }
     }

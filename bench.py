@@ -401,14 +401,25 @@ class PrefixPlan(Plan):
         new_slots = st["new_slots"]
         k_new, v_new = st["k_new"], st["v_new"]
         q_children = pf.q_child
+        # decode order: each child right after its parent, so that the child's
+        # reads of the parent's private blocks find them in L2
+        child_of = {int(par): B + i for i, par in enumerate(pf.parents)}
+        dec_order = []
+        for s_ in range(B):
+            dec_order.append(s_)
+            if s_ in child_of:
+                dec_order.append(child_of[s_])
+        dec_order = np.asarray(dec_order)
+        table, lens = table[dec_order], lens[dec_order]
+        q_all = torch.cat([w.q, q_children])[torch.from_numpy(dec_order)]
         self.NB, self.MB, self.Bd = NB, MB, len(order)
         self.Hq, self.Hkv, self.d, self.bs, self.dtype = Hq, Hkv, d, bs, w.dtype
         self.npairs = len(pairs)
         self.inputs = {
-            "q": torch.cat([w.q, q_children]).to(dev), "k_new": k_new.to(dev),
+            "q": q_all.to(dev), "k_new": k_new.to(dev),
             "v_new": v_new.to(dev),
             "slots": torch.tensor(new_slots, dtype=torch.int64, device=dev),
-            "table": torch.from_numpy(table).to(dev),
+            "table": torch.from_numpy(np.ascontiguousarray(table)).to(dev),
             "lens": torch.from_numpy(lens.astype(np.int32)).to(dev),
             "pairs": torch.tensor(pairs if pairs else [[0, 0]], dtype=torch.int64, device=dev)}
         self.outputs = {"out": torch.empty_like(self.inputs["q"])}
@@ -446,7 +457,8 @@ class PrefixPlan(Plan):
         self.launches = (2 if self.npairs else 1) + n_dec
         self.extra = {"unique_kv_bytes": unique, "logical_kv_bytes": self.decode_bytes,
                       "cow_pairs": self.npairs}
-        self.config = {"B": self.Bd, "sequences": f"{B} sharing a {P}-token prompt + {nf} forks",
+        self.config = {"B": self.Bd, "sequences": f"{B} sharing a {P}-token prompt + {nf} forks "
+                                                  "(each child decoded right after its parent)",
                        "suffix_len": "U[1,512]", "Hq": Hq, "Hkv": Hkv, "head_dim": d,
                        "block_size": bs, "pool_blocks": NB, "partition_tokens": self.PT,
                        "cow_pairs": self.npairs,

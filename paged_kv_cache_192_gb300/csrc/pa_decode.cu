@@ -471,7 +471,9 @@ struct MmaCfg {
     static constexpr int HALVES = D / 64;       // 128-byte column blocks of a row (64 bf16)
     static constexpr int HALF = TT * 128;       // bytes of one column block of one cache's tile
     static constexpr int TILE = HALVES * HALF;  // one cache's tile
-    static constexpr int STAGE = 2 * TILE;      // K then V
+    static constexpr int QB = GQ * D * 2;       // the group's q rows (first tile of an item)
+    // K, V, then q; stages stay 1024-byte aligned for the swizzle
+    static constexpr int STAGE = (2 * TILE + QB + 1023) / 1024 * 1024;
     static constexpr int NST = kRingBytes / STAGE >= 2 ? kRingBytes / STAGE : 2;
     static constexpr int WARP_SMEM = NST * STAGE;
     static constexpr int MINB = PA_DECODE_MMA_CTAS;
@@ -531,6 +533,24 @@ struct MmaAttn {
                 const uint32_t *row = reinterpret_cast<const uint32_t *>(qb + g * D + 16 * k);
                 b0 = __ldg(row + t);
                 b1 = __ldg(row + t + 4);
+            }
+            qf[k][0] = b0;
+            qf[k][1] = b1;
+        }
+    }
+
+    // q of the item from the stage (the producer copied the group's GQ rows
+    // there with the item's first tile): lane (g, t) takes head g's dims
+    // 16k + 2t (+1) and 16k + 2t + 8 (+9) as its B fragments.
+    __device__ __forceinline__ void load_q_smem(uint32_t qaddr, float qscale_) {
+        qscale = qscale_;
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+            uint32_t b0 = 0u, b1 = 0u;
+            if (g < GQ) {
+                const uint32_t a = qaddr + g * D * 2 + (16 * k + 2 * t) * 2;
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b0) : "r"(a));
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b1) : "r"(a + 16));
             }
             qf[k][0] = b0;
             qf[k][1] = b1;
@@ -801,14 +821,20 @@ template <int D, int GQ>
 __device__ __forceinline__ void produce_tile_tma(const DecodeParams &p, const Cursor &c, int blk,
                                                  uint8_t *stage, uint64_t *bar,
                                                  const CUtensorMap *kmap,
-                                                 const CUtensorMap *vmap) {
+                                                 const CUtensorMap *vmap, bool with_q = false) {
     using C = MmaCfg<D, GQ>;
     const uint32_t sk = pa::smem_u32(stage), sv = sk + C::TILE;
     const int tok = first_token(c, C::TT);
+    const uint32_t qbytes = with_q ? C::QB : 0u;
+    if (with_q)  // the group's q rows, contiguous in q [B][Hq][D]
+        pa::bulk_g2s(stage + 2 * C::TILE,
+                     static_cast<const __nv_bfloat16 *>(p.q) +
+                         (static_cast<size_t>(c.b) * p.Hq + c.hk * GQ) * D,
+                     C::QB, bar);
     if (p.contig_len || C::TT <= p.bs) {
         const int y = p.contig_len ? static_cast<int>(contig_row(p, c, tok))
                                    : (blk * p.Hkv + c.hk) * p.bs + (tok & (p.bs - 1));
-        pa::mbar_arrive_expect_tx(bar, 2 * C::TILE);
+        pa::mbar_arrive_expect_tx(bar, 2 * C::TILE + qbytes);
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h) {
             pa::tma_2d_g2s(sk + h * C::HALF, kmap, 64 * h, y, bar);
@@ -818,7 +844,7 @@ __device__ __forceinline__ void produce_tile_tma(const DecodeParams &p, const Cu
         const int nb = C::TT >> p.bs_log2;  // blocks per tile
         int avail = 0;
         for (int j = 0; j < nb; ++j) avail += (tok + j * p.bs < c.L) ? 1 : 0;
-        pa::mbar_arrive_expect_tx(bar, 2u * avail * C::HALVES * p.bs * 128);
+        pa::mbar_arrive_expect_tx(bar, 2u * avail * C::HALVES * p.bs * 128 + qbytes);
         for (int j = 0; j < avail; ++j) {
             const int id = j == 0 ? blk : checked_block(p, block_entry<C::TT>(p, c, j));
             const int y = (id * p.Hkv + c.hk) * p.bs;
@@ -1185,14 +1211,14 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
         if constexpr (MMA) {
             if (lane == 0)
                 produce_tile_tma<D, GQ>(p, pc, checked_block(p, pend), ring + i * C::STAGE,
-                                        &bars[i], &kmap, &vmap);
+                                        &bars[i], &kmap, &vmap, i == 0 || pc.t == 0);
         } else if (kLanes) {
             produce_tile_lanes<T, D, GQ>(p, pc, checked_block(p, pend), ring + i * C::STAGE,
                                          &bars[i], lane);
         } else if (lane == 0) {
             produce_tile<T, D, GQ>(p, pc, checked_block(p, pend), ring + i * C::STAGE, &bars[i]);
         }
-        if (i > 0 && pc.t == 0) prefetch_q<T, D, GQ>(p, pc, lane);
+        if (!MMA && i > 0 && pc.t == 0) prefetch_q<T, D, GQ>(p, pc, lane);
         pc = next_unit(pc, bt, p.B, p.Hkv);
         if ((kLanes || lane == 0) && i + 1 < my_n) pend = block_entry<C::TT>(p, pc, 0);
     }
@@ -1205,11 +1231,14 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
             failed_at = i;
             break;
         }
+        const uint32_t kaddr = pa::smem_u32(ring + s * C::STAGE);
         if (i == 0 || cc.t == 0) {
             st.reset();
-            st.load_q(qbase + (static_cast<size_t>(cc.b) * p.Hq + cc.hk * GQ) * D, p.qscale);
+            if constexpr (MMA)  // q came with this tile
+                st.load_q_smem(kaddr + 2 * C::TILE, p.qscale);
+            else
+                st.load_q(qbase + (static_cast<size_t>(cc.b) * p.Hq + cc.hk * GQ) * D, p.qscale);
         }
-        const uint32_t kaddr = pa::smem_u32(ring + s * C::STAGE);
         st.tile(kaddr, kaddr + C::TILE, min(C::TT, cc.L - first_token(cc, C::TT)), pbuf, sbuf);
         __syncwarp();
         if (i + C::NST < my_n) {
@@ -1217,7 +1246,7 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
                 if (lane == 0) {
                     pa::fence_proxy_async();
                     produce_tile_tma<D, GQ>(p, pc, checked_block(p, pend), ring + s * C::STAGE,
-                                            &bars[s], &kmap, &vmap);
+                                            &bars[s], &kmap, &vmap, pc.t == 0);
                 }
             } else if (kLanes) {
                 produce_tile_lanes<T, D, GQ>(p, pc, checked_block(p, pend), ring + s * C::STAGE,
@@ -1227,7 +1256,7 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
                 produce_tile<T, D, GQ>(p, pc, checked_block(p, pend), ring + s * C::STAGE,
                                        &bars[s]);
             }
-            if (pc.t == 0) prefetch_q<T, D, GQ>(p, pc, lane);
+            if (!MMA && pc.t == 0) prefetch_q<T, D, GQ>(p, pc, lane);
             pc = next_unit(pc, bt, p.B, p.Hkv);
             if ((kLanes || lane == 0) && i + C::NST + 1 < my_n)
                 pend = block_entry<C::TT>(p, pc, 0);
@@ -1469,31 +1498,37 @@ template <typename T, int D, int GQ>
 __global__ void __launch_bounds__(GQ * 32) partial_merge_kernel(const DecodeParams p) {
     constexpr int EL = D / 32;
     constexpr int kSpec = 8;  // segment slots loaded before the item's count is known
+    constexpr int kSpecP = 4; // shared-prefix slots loaded likewise (p.npfx of them)
     const int item = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
     wait_prior_grids();
     const size_t row = static_cast<size_t>(item / p.Hkv) * p.Hq + (item % p.Hkv) * GQ + h;
     const size_t sb = row * p.rowslots;
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + sb;
     const float *src = p.ws_acc + sb * D + EL * lane;
-    // One round trip for the common case (no shared prefix, at most kSpec
-    // segments): the count, the (max, sum) of slots 0..kSpec-1 and this
-    // lane's values of them are all requested at once.
-    const int spec = min(kSpec, p.rowslots);
+    // One round trip for the common case (at most kSpec segments and at most
+    // kSpecP shared-prefix partials): the count, the (max, sum) of segment
+    // slots 0..kSpec-1 and of the prefix slots, and this lane's values of
+    // them are all requested at once.  Lane / index i < kSpec stands for
+    // segment slot i, kSpec + k for prefix slot pslot0 + k.
+    const int spec = min(kSpec, p.pslot0);
+    const int specp = p.npfx <= kSpecP ? p.npfx : 0;
+    auto spec_slot = [&](int i) { return i < kSpec ? i : p.pslot0 + (i - kSpec); };
+    auto spec_on = [&](int i) { return i < kSpec ? i < spec : i - kSpec < specp; };
     const unsigned meta = __ldcg(p.meta + item);
     float2 v = make_float2(-INFINITY, 0.f);
-    if (lane < spec) v = __ldcg(&ml[lane]);
-    float pre[kSpec][EL];
+    if (lane < kSpec + kSpecP && spec_on(lane)) v = __ldcg(&ml[spec_slot(lane)]);
+    float pre[kSpec + kSpecP][EL];
 #pragma unroll
-    for (int i = 0; i < kSpec; ++i) {
-        if (i < spec) {
+    for (int i = 0; i < kSpec + kSpecP; ++i) {
+        if (spec_on(i)) {
             if constexpr (EL == 4) {
-                const float4 a = __ldcg(reinterpret_cast<const float4 *>(src + i * D));
+                const float4 a = __ldcg(reinterpret_cast<const float4 *>(src + spec_slot(i) * D));
                 pre[i][0] = a.x;
                 pre[i][1] = a.y;
                 pre[i][2] = a.z;
                 pre[i][3] = a.w;
             } else {
-                const float2 a = __ldcg(reinterpret_cast<const float2 *>(src + i * D));
+                const float2 a = __ldcg(reinterpret_cast<const float2 *>(src + spec_slot(i) * D));
                 pre[i][0] = a.x;
                 pre[i][1] = a.y;
             }
@@ -1505,19 +1540,22 @@ __global__ void __launch_bounds__(GQ * 32) partial_merge_kernel(const DecodePara
 #pragma unroll
     for (int e = 0; e < EL; ++e) acc[e] = 0.f;
     float den = 0.f, M = -INFINITY;
-    if (ns == nseg && ns <= spec) {
-        if (lane >= ns) v = make_float2(-INFINITY, 0.f);
+    const int npre = ns - nseg;
+    if (nseg <= spec && (npre == 0 || npre == specp)) {
+        // lanes in use: segments 0..nseg-1 and the npre prefix slots
+        const bool used = lane < kSpec ? lane < nseg : (lane < kSpec + kSpecP && lane - kSpec < npre);
+        if (!used) v = make_float2(-INFINITY, 0.f);
         M = v.x;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(pa::kFull, M, o));
-        const float wl = lane < ns ? exp2f(v.x - M) : 0.f;
+        const float wl = used && v.x != -INFINITY ? exp2f(v.x - M) : 0.f;
         den = wl * v.y;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(pa::kFull, den, o);
 #pragma unroll
-        for (int i = 0; i < kSpec; ++i) {
+        for (int i = 0; i < kSpec + kSpecP; ++i) {
             const float f = __shfl_sync(pa::kFull, wl, i);
-            if (i < ns)
+            if (i < kSpec ? i < nseg : i - kSpec < npre)
 #pragma unroll
                 for (int e = 0; e < EL; ++e) acc[e] += f * pre[i][e];
         }

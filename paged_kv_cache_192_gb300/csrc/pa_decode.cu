@@ -2100,6 +2100,9 @@ int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cac
             int64_t want = plan.tc ? int64_t(sms) / std::max<int64_t>(ctas, 1)
                                    : (2 * int64_t(sms) + ctas - 1) / std::max<int64_t>(ctas, 1);
             if (plan.tc) want = std::max<int64_t>(want, nc_min);
+#ifdef PA_PFX_NC
+            want = std::max(PA_PFX_NC, nc_min);
+#endif
             plan.pp.group_start = sh->group_start;
             plan.pp.group_seqs = sh->group_seqs;
             plan.pp.G = sh->G;

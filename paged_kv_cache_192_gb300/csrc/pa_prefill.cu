@@ -343,7 +343,10 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
 constexpr int kTcKT = 64;        // KV tokens per tile
 constexpr int kTcCols = 256;     // TMEM columns per CTA
 constexpr int kTcS = 128, kTcPH = 192, kTcPL = 224;
-constexpr float kTcTau = 8.0f;   // lazy-rescale headroom (log2 units)
+#ifndef PA_PREFILL_TAU
+#define PA_PREFILL_TAU 8.0f
+#endif
+constexpr float kTcTau = PA_PREFILL_TAU;  // lazy-rescale headroom (log2 units)
 
 template <int D>
 struct TcLayout {
@@ -619,23 +622,32 @@ __global__ void __launch_bounds__(128, 2) prefill_tc_kernel(const PrefillParams 
 // O_A [0,128), O_B [128,256), S_A[0..1] [256,384), S_B[0..1] [384,512).
 // All hand-offs are mbarriers; every wait is bounded.
 // ---------------------------------------------------------------------------
+#ifndef PA_PREFILL_NST
+#define PA_PREFILL_NST 4  // K/V ring stages of the two-query-tile kernel (3: 105.7 us, 4: 102.2 us on the mixed batch)
+#endif
 constexpr int kT2KT = 64;      // KV tokens per tile
-constexpr int kT2NST = 3;      // K/V ring stages
-constexpr int kT2Threads = 320;
 constexpr int kT2RankMax = 256;  // (request, query tile) pairs ranked in-kernel
 
-template <int D>
+// NQ query tiles of 128 rows per CTA: NQ = 2 (320 threads, 512 TMEM columns,
+// 3-stage K/V ring, one CTA per SM) or NQ = 1 (192 threads, 256 columns,
+// 2-stage ring, two CTAs per SM).
+template <int D, int NQ = 2>
 struct Tc2Layout {
-    static constexpr int Q_BYTES = 2 * 128 * D * 2;  // two query tiles
+    static constexpr int ROWS = 128 * NQ;
+    static constexpr int NST = NQ == 2 ? PA_PREFILL_NST : 2;  // K/V ring stages
+    static constexpr int THREADS = (4 * NQ + 2) * 32;  // softmax groups, MMA warp, loader warp
+    static constexpr int MMA_WARP = 4 * NQ, LOAD_WARP = 4 * NQ + 1;
+    static constexpr int TMEM_COLS = 256 * NQ;       // O per group, then S (2 x 64) per group
+    static constexpr int Q_BYTES = NQ * 128 * D * 2;  // the query tiles
     static constexpr int T_BYTES = kT2KT * D * 2;    // one K or V tile
     static constexpr int OFF_KV = Q_BYTES;           // [stage][K|V]
-    static constexpr int OFF_BAR = OFF_KV + kT2NST * 2 * T_BYTES;
-    static constexpr int N_BAR = 2 * kT2NST + 8;     // kv_full, kv_empty, s x 4, (p, o) x 2
+    static constexpr int OFF_BAR = OFF_KV + NST * 2 * T_BYTES;
+    static constexpr int N_BAR = 2 * NST + 4 * NQ;   // kv_full, kv_empty, s x 2NQ, (p, o) x NQ
     static constexpr int OFF_SLOT = OFF_BAR + 8 * N_BAR;
     static constexpr int OFF_BT = OFF_SLOT + 16;
     static constexpr int BT_MAX = 1024;
-    static constexpr int OFF_ROWS = OFF_BT + 4 * BT_MAX;  // prefix mode: row of each of 256
-    static constexpr int SMEM = OFF_ROWS + 8 * 256 + 1024;
+    static constexpr int OFF_ROWS = OFF_BT + 4 * BT_MAX;  // prefix mode: row of each row
+    static constexpr int SMEM = OFF_ROWS + 8 * ROWS + 1024;
 };
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
@@ -651,13 +663,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(pa::smem_u32(bar)) : "memory");
 }
 
-template <int D, int GQ, bool PFX>
-__global__ void __launch_bounds__(kT2Threads, 1)
+template <int D, int GQ, bool PFX, int NQ>
+__global__ void __launch_bounds__(Tc2Layout<D, NQ>::THREADS, 3 - NQ)
     prefill_tc2_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap) {
-    using Lay = Tc2Layout<D>;
+    using Lay = Tc2Layout<D, NQ>;
+    constexpr int kT2NST = Lay::NST;
+    constexpr int kT2Threads = Lay::THREADS;
+    constexpr int ROWS = Lay::ROWS;
     constexpr int CH = D * 2 / 16;
-    constexpr int QTOK = 256 / GQ;  // query tokens per CTA
+    constexpr int QTOK = ROWS / GQ;  // query tokens per CTA
     constexpr int TILE_TX = 2 * kT2KT * D * 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -667,7 +682,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::OFF_BAR);
     uint64_t *kv_full = bars, *kv_empty = bars + kT2NST;
     // s_full[2 * group + buffer]; p_full / o_done per query-tile group
-    uint64_t *s_full = bars + 2 * kT2NST, *p_full = s_full + 4, *o_done = p_full + 2;
+    uint64_t *s_full = bars + 2 * kT2NST, *p_full = s_full + 2 * NQ, *o_done = p_full + NQ;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + Lay::OFF_SLOT);
     volatile int *fail = reinterpret_cast<volatile int *>(smem + Lay::OFF_SLOT + 4);
     int32_t *bt_s = reinterpret_cast<int32_t *>(smem + Lay::OFF_BT);
@@ -780,7 +795,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     if constexpr (PFX) {
         if (ntiles == 0) {
             // a chunk past this group's prefix: neutral partials (weight 0)
-            for (int m = tid; m < 256; m += kT2Threads) {
+            for (int m = tid; m < ROWS; m += kT2Threads) {
                 const int64_t row = pfx_row(m);
                 if (row < 0) continue;
                 const size_t slot = static_cast<size_t>(row) * p.pfx_rowslots + p.pfx_pslot0 + pchunk;
@@ -805,31 +820,31 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     }
     int64_t *rows_s = reinterpret_cast<int64_t *>(smem + Lay::OFF_ROWS);
     if constexpr (PFX) {
-        for (int m = tid; m < 256; m += kT2Threads) rows_s[m] = pfx_row(m);
+        for (int m = tid; m < ROWS; m += kT2Threads) rows_s[m] = pfx_row(m);
     }
     if (tid == 0) {
         for (int i = 0; i < kT2NST; ++i) {
             pa::mbar_init(&kv_full[i], 1);
             pa::mbar_init(&kv_empty[i], 1);
         }
-        for (int i = 0; i < 4; ++i) pa::mbar_init(&s_full[i], 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 2 * NQ; ++i) pa::mbar_init(&s_full[i], 1);
+        for (int i = 0; i < NQ; ++i) {
             pa::mbar_init(&p_full[i], 4);  // one arrival per softmax warp
             pa::mbar_init(&o_done[i], 1);
         }
         *fail = 0;
         pa::fence_barrier_init();
     }
-    if (warp == 8) pa::tc::alloc(tslot, 512);
+    if (warp == Lay::MMA_WARP) pa::tc::alloc(tslot, Lay::TMEM_COLS);
     pa::tc::fence_before();
     __syncthreads();
     pa::tc::fence_after();
     const uint32_t tmem = *tslot;
-    if (warp != 9) {
-        // Q tiles: only the MMA warp's QK^T reads them; warps 0-8 load them
-        // and meet on named barrier 1 before it
+    if (warp != Lay::LOAD_WARP) {
+        // Q tiles: only the MMA warp's QK^T reads them; every warp but the
+        // loader loads them and they meet on named barrier 1 before it
         constexpr int kQThreads = kT2Threads - 32;
-        for (int idx = tid; idx < 256 * CH; idx += kQThreads) {
+        for (int idx = tid; idx < ROWS * CH; idx += kQThreads) {
             const int m = idx / CH, c = idx % CH;  // row m of the CTA's 256
             bool valid;
             const __nv_bfloat16 *src;
@@ -852,7 +867,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         asm volatile("bar.sync 1, %0;" ::"n"(kQThreads) : "memory");
     }
 
-    if (warp == 9) {
+    if (warp == Lay::LOAD_WARP) {
         // ---------------- loader ----------------
         if (lane == 0) {
             const int rows_total = static_cast<int>(p.num_blocks * p.Hkv) << p.bs_log2;
@@ -878,7 +893,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
                 }
             }
         }
-    } else if (warp == 8) {
+    } else if (warp == Lay::MMA_WARP) {
         // ---------------- MMA issuer ----------------
         // The whole warp follows the schedule (barrier waits, descriptor
         // arithmetic on warp-uniform values); one elected lane issues each
@@ -895,7 +910,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         auto issue_s = [&](int wg, int j) {
             const uint64_t a0 = dq + static_cast<uint32_t>(wg * ((128 * D * 2) >> 4));
             const uint64_t b0 = dk + static_cast<uint32_t>((j % kT2NST) * kStage);
-            const uint32_t sc = tmem + 256 + wg * 128 + (j & 1) * 64;
+            const uint32_t sc = tmem + 128 * NQ + wg * 128 + (j & 1) * 64;
             if (pa::tc::elect_one()) {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
@@ -909,7 +924,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         // O_wg += P_hi V + P_lo V; P of tile j sits in the S buffer it came from
         auto issue_pv = [&](int wg, int j) {
             const uint64_t b0 = dv + static_cast<uint32_t>((j % kT2NST) * kStage);
-            const uint32_t ph = tmem + 256 + wg * 128 + (j & 1) * 64, pl = ph + 32;
+            const uint32_t ph = tmem + 128 * NQ + wg * 128 + (j & 1) * 64, pl = ph + 32;
             const uint32_t od = tmem + wg * 128;
             const int acc0 = j > 0;
             if (pa::tc::elect_one()) {
@@ -934,18 +949,16 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         bool ok = wait_all(&kv_full[0], 0);
         if (ok) {
             pa::tc::fence_after();
-            issue_s(0, 0);
-            issue_s(1, 0);
+            for (int wg = 0; wg < NQ; ++wg) issue_s(wg, 0);
         }
         for (int j = 0; j < ntiles && ok; ++j) {
             if (j + 1 < ntiles) {
                 ok = wait_all(&kv_full[(j + 1) % kT2NST], ((j + 1) / kT2NST) & 1);
                 if (!ok) break;
                 pa::tc::fence_after();
-                issue_s(0, j + 1);
-                issue_s(1, j + 1);
+                for (int wg = 0; wg < NQ; ++wg) issue_s(wg, j + 1);
             }
-            for (int wg = 0; wg < 2 && ok; ++wg) {
+            for (int wg = 0; wg < NQ && ok; ++wg) {
                 ok = wait_all(&p_full[wg], j & 1);
                 if (!ok) break;
                 pa::tc::fence_after();
@@ -968,7 +981,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         float m_used = -INFINITY, lsum = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            const uint32_t s_col = 256 + wg * 128 + (j & 1) * 64;
+            const uint32_t s_col = 128 * NQ + wg * 128 + (j & 1) * 64;
             ok = pa::mbar_wait(&s_full[2 * wg + (j & 1)], (j >> 1) & 1);
             if (!ok) break;
             pa::tc::fence_after();
@@ -1117,12 +1130,12 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         // bounded chance to land before the TMEM and shared memory go away
         if (tid == 0) {
             pa::record_error(p.err, PA_DEVERR_TIMEOUT);
-            for (int i = 0; i < 2; ++i) (void)pa::mbar_wait(&o_done[i], 0);
+            for (int i = 0; i < NQ; ++i) (void)pa::mbar_wait(&o_done[i], 0);
             for (int i = 0; i < kT2NST; ++i) (void)pa::mbar_wait(&kv_full[i], 0);
         }
         __syncthreads();
     }
-    if (warp == 8) pa::tc::dealloc(tmem, 512);
+    if (warp == Lay::MMA_WARP) pa::tc::dealloc(tmem, Lay::TMEM_COLS);
 }
 
 int log2_int(int x) {
@@ -1133,6 +1146,9 @@ int log2_int(int x) {
 
 #ifndef PA_PREFILL_TCGEN05
 #define PA_PREFILL_TCGEN05 1  // 1: tcgen05 kernel; 0: warp-level mma.sync kernel
+#endif
+#ifndef PA_PREFILL_NQ
+#define PA_PREFILL_NQ 2  // query tiles of 128 rows per CTA of the warp-specialised kernel
 #endif
 
 template <int D, int GQ>
@@ -1170,7 +1186,7 @@ int set_smem_once(K kern, size_t smem, std::atomic<uint64_t> *done) {
 template <int D>
 bool tc2_ok(const PrefillParams &p) {
     const int64_t rows = (p.num_blocks * p.Hkv) << p.bs_log2;
-    return p.bs >= 8 && p.bs <= 64 && p.MB <= Tc2Layout<D>::BT_MAX && rows < (int64_t(1) << 31);
+    return p.bs >= 8 && p.bs <= 64 && p.MB <= Tc2Layout<D, 2>::BT_MAX && rows < (int64_t(1) << 31);
 }
 
 template <int D, int GQ>
@@ -1179,15 +1195,16 @@ int launch_tc2(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
     CUtensorMap kmap, vmap;
     if (int rc = pa::pool_tensor_map(&kmap, p.k_cache, rows, D, p.bs)) return rc;
     if (int rc = pa::pool_tensor_map(&vmap, p.v_cache, rows, D, p.bs)) return rc;
-    const size_t smem = Tc2Layout<D>::SMEM;
-    auto kern = prefill_tc2_kernel<D, GQ, false>;
+    using Lay = Tc2Layout<D, PA_PREFILL_NQ>;
+    const size_t smem = Lay::SMEM;
+    auto kern = prefill_tc2_kernel<D, GQ, false, PA_PREFILL_NQ>;
     static std::atomic<uint64_t> attr_done{0};
     if (int rc = set_smem_once(kern, smem, &attr_done)) return rc;
     (void)cudaGetLastError();
-    constexpr int qtok = 256 / GQ;
+    constexpr int qtok = Lay::ROWS / GQ;
     const int64_t ctas = int64_t((max_query_len + qtok - 1) / qtok) * p.R * p.Hkv;
     if (ctas > 0x7fffffff) return pa::fail(PA_ERR_INVALID, "prefill: grid too large");
-    kern<<<static_cast<unsigned>(ctas), kT2Threads, smem, stream>>>(p, kmap, vmap);
+    kern<<<static_cast<unsigned>(ctas), Lay::THREADS, smem, stream>>>(p, kmap, vmap);
     return pa::check_launch("prefill launch");
 }
 
@@ -1256,8 +1273,9 @@ int launch_prefix_tc_t(const pa::PrefixTcArgs &a, cudaStream_t stream) {
     CUtensorMap kmap, vmap;
     if (int rc = pa::pool_tensor_map(&kmap, a.k_cache, rows, D, a.bs)) return rc;
     if (int rc = pa::pool_tensor_map(&vmap, a.v_cache, rows, D, a.bs)) return rc;
-    const size_t smem = Tc2Layout<D>::SMEM;
-    auto kern = prefill_tc2_kernel<D, GQ, true>;
+    using Lay = Tc2Layout<D, 2>;
+    const size_t smem = Lay::SMEM;
+    auto kern = prefill_tc2_kernel<D, GQ, true, 2>;
     static std::atomic<uint64_t> attr_done{0};
     if (int rc = set_smem_once(kern, smem, &attr_done)) return rc;
     const int64_t ctas = int64_t(p.pfx_nmt) * a.G * a.nc * a.Hkv;
@@ -1266,7 +1284,7 @@ int launch_prefix_tc_t(const pa::PrefixTcArgs &a, cudaStream_t stream) {
     (void)cudaGetLastError();
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ctas));
-    cfg.blockDim = dim3(kT2Threads);
+    cfg.blockDim = dim3(Lay::THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -1510,7 +1510,9 @@ __global__ void __launch_bounds__(GQ * 32) partial_merge_kernel(const DecodePara
     // slots 0..kSpec-1 and of the prefix slots, and this lane's values of
     // them are all requested at once.  Lane / index i < kSpec stands for
     // segment slot i, kSpec + k for prefix slot pslot0 + k.
-    const int spec = min(kSpec, p.pslot0);
+    // batches with shared-prefix partials have short private parts (one or
+    // two segments per item): fewer speculative segment slots there
+    const int spec = min(p.npfx > 0 ? 2 : kSpec, p.pslot0);
     const int specp = p.npfx <= kSpecP ? p.npfx : 0;
     auto spec_slot = [&](int i) { return i < kSpec ? i : p.pslot0 + (i - kSpec); };
     auto spec_on = [&](int i) { return i < kSpec ? i < spec : i - kSpec < specp; };

@@ -353,6 +353,32 @@ int pa_prefill_chunk(void *out, const void *q, const void *k_cache, const void *
                      int max_query_len, int Hq, int Hkv, int head_dim, int block_size,
                      int64_t num_blocks, float scale, int dtype, pa_stream_t stream);
 
+/* kernels pa_prefill_chunk can launch (pa_prefill_kernel_for) */
+enum { PA_PREFILL_PERSISTENT_GRID = 1, PA_PREFILL_ITEM_GRID = 2, PA_PREFILL_SIMPLE = 3 };
+
+/*
+ * pa_prefill_kernel_for -- which kernel pa_prefill_chunk launches for these
+ * sizes (sizes only, never device data; no device needed).  A work item is
+ * (request, 256 query rows, KV head).
+ *   PA_PREFILL_PERSISTENT_GRID  one CTA per SM (at most one per item), each
+ *                               running a list of items dealt longest first
+ *                               to the least-loaded CTA; batches of at most
+ *                               256 (request, 256-row) pairs and 512 items;
+ *   PA_PREFILL_ITEM_GRID        one CTA per item, longest first (larger
+ *                               batches);
+ *                               both: blocks of 8..64 tokens, tables of at
+ *                               most 1024 blocks, fewer than 2^31 pool rows
+ *                               of (block, KV head, slot);
+ *   PA_PREFILL_SIMPLE           one CTA of 128 threads per 128 rows (every
+ *                               other supported size, e.g. 128-token blocks).
+ * All three meet the same error bound.  Arguments as for pa_prefill_chunk;
+ * *kernel receives the choice.  PA_ERR_INVALID / PA_ERR_UNSUPPORTED as
+ * pa_prefill_chunk would return for the sizes.
+ */
+int pa_prefill_kernel_for(int R, int max_query_len, int Hq, int Hkv, int head_dim,
+                          int block_size, int64_t num_blocks, int max_blocks_per_seq,
+                          int *kernel);
+
 /* ------------------------------------------------------------------------
  * Host block manager (opaque handle; C++ behind the C ABI).
  *

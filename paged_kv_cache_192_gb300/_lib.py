@@ -15,6 +15,7 @@ PA_BF16, PA_F32 = 0, 1
 PA_DEVERR_BAD_BLOCK, PA_DEVERR_TIMEOUT = 1, 2
 PA_DECODE_PERSISTENT, PA_DECODE_GRID = 1, 2
 PA_DECODE_TILE_CUDA_CORE, PA_DECODE_TILE_TENSOR_CORE = 1, 2
+PA_PREFILL_PERSISTENT_GRID, PA_PREFILL_ITEM_GRID, PA_PREFILL_SIMPLE = 1, 2, 3
 
 _c_int, _c_i64, _c_sz, _c_vp, _c_f = (ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
                                       ctypes.c_void_p, ctypes.c_float)
@@ -59,6 +60,8 @@ SIGNATURES = {
     "pa_prefill_chunk": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_vp, _c_int,
                                   _c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_f, _c_int,
                                   _c_vp]),
+    "pa_prefill_kernel_for": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_i64,
+                                       _c_int, ctypes.POINTER(_c_int)]),
     "pa_bm_create": (_c_int, [_c_i64, _c_int, ctypes.c_uint64, ctypes.POINTER(_c_vp)]),
     "pa_bm_destroy": (None, [_c_vp]),
     "pa_bm_add_seq": (_c_int, [_c_vp, _c_i64, _c_i64, _p_i64]),

@@ -1501,6 +1501,10 @@ __global__ void __launch_bounds__(GQ * 32) partial_merge_kernel(const DecodePara
     constexpr int kSpecP = 4; // shared-prefix slots loaded likewise (p.npfx of them)
     const int item = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
     wait_prior_grids();
+    // a kernel launched behind this one as a programmatic dependent (the
+    // persistent prefill) may start its set-up while the merge drains; it
+    // waits for this grid before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const size_t row = static_cast<size_t>(item / p.Hkv) * p.Hq + (item % p.Hkv) * GQ + h;
     const size_t sb = row * p.rowslots;
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + sb;

@@ -34,6 +34,11 @@ inline int check_launch(const char *what) {
 // 2D tensor map (128-byte swizzle, boxes of 64 columns x box_rows rows) over
 // a bf16 pool of `rows` rows of D elements; cached by value (pa_tma.cpp).
 int pool_tensor_map(CUtensorMap *map, const void *pool, int64_t rows, int D, int box_rows);
+// 3D tensor map over query rows [tokens][Hq][D] (bf16): boxes of 64 columns x
+// gq heads x box_tokens tokens, 128-byte swizzle; gq * box_tokens rows of
+// 128 bytes per box (a multiple of 8, at most 256 tokens).
+int q_tensor_map(CUtensorMap *map, const void *q, int64_t tokens, int Hq, int D, int gq,
+                 int box_tokens);
 
 inline size_t dtype_size(int dtype) { return dtype == PA_BF16 ? 2 : (dtype == PA_F32 ? 4 : 0); }
 

@@ -27,37 +27,15 @@
 #include <cmath>
 #include <vector>
 
-#include "pa_device.cuh"
-#include "pa_internal.h"
-#include "pa_tcgen05.cuh"
+#include "pa_prefill.cuh"
 
 namespace {
+
+using namespace pa::pf;
 
 constexpr int kRows = 64;   // query rows (token, head) per CTA
 constexpr int kKT = 64;     // KV tokens per tile
 constexpr int kThreads = 128;
-constexpr float kLog2e = 1.4426950408889634f;
-
-struct PrefillParams {
-    __nv_bfloat16 *out;
-    const __nv_bfloat16 *q;
-    const uint8_t *k_cache;
-    const uint8_t *v_cache;
-    const int32_t *block_table;
-    const int32_t *query_start;
-    const int32_t *context_lens;
-    int *err;
-    int64_t num_blocks;
-    int R, Hq, Hkv, bs, bs_log2, MB, max_query_len;
-    float qscale;
-    // shared-prefix mode of prefill_tc2_kernel (pa::launch_prefix_tc): rows are
-    // (group member, query head) pairs of a decode batch, all attending to
-    // the group's shared tokens [t_lo, t_hi) of one token chunk; the result is
-    // a log-sum-exp partial in the decode workspace
-    const int32_t *pfx_group_start, *pfx_group_seqs, *pfx_shared_len;
-    float *pfx_acc, *pfx_ml;
-    int pfx_G, pfx_nc, pfx_nmt, pfx_members, pfx_rowslots, pfx_pslot0, pfx_B;
-};
 
 // Swizzled address of 16-byte chunk `c` of row `r` in a tile of rows of
 // `CH` chunks: chunk positions are XORed with the row's low 3 bits so that
@@ -67,18 +45,6 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c) {
     return base + r * (CH * 16) + ((c ^ (r & 7)) * 16);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-    const int n = valid ? 16 : 0;  // 0: zero-fill without reading
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                         uint32_t &r3) {
@@ -103,23 +69,6 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&v);
-}
-
-// max(a, b, c) in one instruction
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-    float r;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 template <int D, int GQ>
 __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParams p) {
@@ -343,10 +292,6 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
 constexpr int kTcKT = 64;        // KV tokens per tile
 constexpr int kTcCols = 256;     // TMEM columns per CTA
 constexpr int kTcS = 128, kTcPH = 192, kTcPL = 224;
-#ifndef PA_PREFILL_TAU
-#define PA_PREFILL_TAU 8.0f
-#endif
-constexpr float kTcTau = PA_PREFILL_TAU;  // lazy-rescale headroom (log2 units)
 
 template <int D>
 struct TcLayout {
@@ -625,7 +570,6 @@ __global__ void __launch_bounds__(128, 2) prefill_tc_kernel(const PrefillParams 
 #ifndef PA_PREFILL_NST
 #define PA_PREFILL_NST 4  // K/V ring stages of the two-query-tile kernel (3: 105.7 us, 4: 102.2 us on the mixed batch)
 #endif
-constexpr int kT2KT = 64;      // KV tokens per tile
 constexpr int kT2RankMax = 256;  // (request, query tile) pairs ranked in-kernel
 
 // NQ query tiles of 128 rows per CTA: NQ = 2 (320 threads, 512 TMEM columns,
@@ -650,18 +594,6 @@ struct Tc2Layout {
     static constexpr int SMEM = OFF_ROWS + 8 * ROWS + 1024;
 };
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(pa::smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(pa::smem_u32(bar)) : "memory");
-}
 
 template <int D, int GQ, bool PFX, int NQ>
 __global__ void __launch_bounds__(Tc2Layout<D, NQ>::THREADS, 3 - NQ)
@@ -1138,11 +1070,6 @@ __global__ void __launch_bounds__(Tc2Layout<D, NQ>::THREADS, 3 - NQ)
     if (warp == Lay::MMA_WARP) pa::tc::dealloc(tmem, Lay::TMEM_COLS);
 }
 
-int log2_int(int x) {
-    int l = 0;
-    while ((1 << l) < x) ++l;
-    return l;
-}
 
 #ifndef PA_PREFILL_TCGEN05
 #define PA_PREFILL_TCGEN05 1  // 1: tcgen05 kernel; 0: warp-level mma.sync kernel
@@ -1165,21 +1092,6 @@ int launch_tc(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
     return pa::check_launch("prefill launch");
 }
 
-// cudaFuncSetAttribute for the dynamic shared memory of `kern`, once per
-// device (bit d of *done).
-template <typename K>
-int set_smem_once(K kern, size_t smem, std::atomic<uint64_t> *done) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return pa::cuda_fail(cudaGetLastError(), "prefill: device");
-    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
-    if (bit && (done->load(std::memory_order_acquire) & bit)) return PA_OK;
-    (void)cudaGetLastError();
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return pa::cuda_fail(e, "prefill: shared memory attribute");
-    if (bit) done->fetch_or(bit, std::memory_order_acq_rel);
-    return PA_OK;
-}
 
 // The warp-specialised kernel needs blocks of 8..64 tokens, a block-table
 // slice of at most BT_MAX entries and 32-bit pool row coordinates.
@@ -1212,10 +1124,17 @@ int launch_tc2(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
 #define PA_PREFILL_WARP_SPECIALIZED 1
 #endif
 
+#ifndef PA_PREFILL_PERSISTENT
+#define PA_PREFILL_PERSISTENT 1  // 1: persistent kernel for batches of at most 512 items
+#endif
+
 template <int D, int GQ>
 int launch(const PrefillParams &p, int max_query_len, cudaStream_t stream) {
-    if (PA_PREFILL_TCGEN05 && PA_PREFILL_WARP_SPECIALIZED && tc2_ok<D>(p))
+    if (PA_PREFILL_TCGEN05 && PA_PREFILL_WARP_SPECIALIZED && tc2_ok<D>(p)) {
+        if (PA_PREFILL_PERSISTENT && persist_ok(p.R, max_query_len, p.Hq, p.Hkv))
+            return launch_persist(p, D, GQ, stream);
         return launch_tc2<D, GQ>(p, max_query_len, stream);
+    }
     if (PA_PREFILL_TCGEN05) return launch_tc<D, GQ>(p, max_query_len, stream);
     const size_t smem = kRows * D * 2 + 4 * kKT * D * 2;
     auto kern = prefill_kernel<D, GQ>;
@@ -1325,14 +1244,10 @@ int launch_prefix_tc(const PrefixTcArgs &a, cudaStream_t stream) {
 
 }  // namespace pa
 
-extern "C" int pa_prefill_chunk(void *out, const void *q, const void *k_cache, const void *v_cache,
-                                const int32_t *block_table, int max_blocks_per_seq,
-                                const int32_t *query_start, const int32_t *context_lens, int R,
-                                int max_query_len, int Hq, int Hkv, int head_dim, int block_size,
-                                int64_t num_blocks, float scale, int dtype, pa_stream_t stream) {
-    pa::clear_error();
-    if (dtype != PA_BF16)
-        return pa::fail(PA_ERR_UNSUPPORTED, "prefill: only bf16 is supported (dtype %d)", dtype);
+namespace {
+
+int check_sizes(int R, int max_query_len, int Hq, int Hkv, int head_dim, int block_size,
+                int64_t num_blocks, int max_blocks_per_seq) {
     if (R < 0 || R > 65535 || Hq <= 0 || Hkv <= 0 || Hkv > 65535 || Hq % Hkv ||
         max_query_len < 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
         return pa::fail(PA_ERR_INVALID, "prefill: bad sizes");
@@ -1344,6 +1259,45 @@ extern "C" int pa_prefill_chunk(void *out, const void *q, const void *k_cache, c
         return pa::fail(PA_ERR_UNSUPPORTED, "prefill: block_size %d unsupported", block_size);
     if (int64_t(max_blocks_per_seq) * block_size > (int64_t(1) << 30))
         return pa::fail(PA_ERR_INVALID, "prefill: table capacity too large");
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_prefill_kernel_for(int R, int max_query_len, int Hq, int Hkv, int head_dim,
+                                     int block_size, int64_t num_blocks, int max_blocks_per_seq,
+                                     int *kernel) {
+    pa::clear_error();
+    if (!kernel) return pa::fail(PA_ERR_INVALID, "prefill_kernel_for: NULL kernel");
+    if (int rc = check_sizes(R, max_query_len, Hq, Hkv, head_dim, block_size, num_blocks,
+                             max_blocks_per_seq))
+        return rc;
+    PrefillParams p{};
+    p.num_blocks = num_blocks;
+    p.Hkv = Hkv;
+    p.bs = block_size;
+    p.bs_log2 = log2_int(block_size);
+    p.MB = max_blocks_per_seq;
+    if (!(PA_PREFILL_TCGEN05 && PA_PREFILL_WARP_SPECIALIZED && tc2_ok<128>(p)))
+        *kernel = PA_PREFILL_SIMPLE;
+    else if (PA_PREFILL_PERSISTENT && persist_ok(R, max_query_len, Hq, Hkv))
+        *kernel = PA_PREFILL_PERSISTENT_GRID;
+    else
+        *kernel = PA_PREFILL_ITEM_GRID;
+    return PA_OK;
+}
+
+extern "C" int pa_prefill_chunk(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *block_table, int max_blocks_per_seq,
+                                const int32_t *query_start, const int32_t *context_lens, int R,
+                                int max_query_len, int Hq, int Hkv, int head_dim, int block_size,
+                                int64_t num_blocks, float scale, int dtype, pa_stream_t stream) {
+    pa::clear_error();
+    if (dtype != PA_BF16)
+        return pa::fail(PA_ERR_UNSUPPORTED, "prefill: only bf16 is supported (dtype %d)", dtype);
+    if (int rc = check_sizes(R, max_query_len, Hq, Hkv, head_dim, block_size, num_blocks,
+                             max_blocks_per_seq))
+        return rc;
     if (!(scale > 0.f) || !std::isfinite(scale))
         return pa::fail(PA_ERR_INVALID, "prefill: scale must be positive and finite");
     if (R == 0 || max_query_len == 0) return PA_OK;

@@ -148,6 +148,18 @@ def decode_kernel_for(B, Hkv, max_blocks_per_seq, block_size, partition_tokens=0
     return {_lib.PA_DECODE_PERSISTENT: "persistent", _lib.PA_DECODE_GRID: "grid"}[out.value]
 
 
+def prefill_kernel_for(R, max_query_len, Hq, Hkv, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq) -> str:
+    """Kernel pa_prefill_chunk runs for these sizes: "persistent" (one CTA per
+    SM running a list of work items), "item_grid" (one CTA per item) or
+    "simple" (128-thread CTAs; other block sizes and longer tables)."""
+    out = ctypes.c_int(0)
+    check(lib().pa_prefill_kernel_for(R, max_query_len, Hq, Hkv, head_dim, block_size,
+                                      num_blocks, max_blocks_per_seq, ctypes.byref(out)))
+    return {_lib.PA_PREFILL_PERSISTENT_GRID: "persistent", _lib.PA_PREFILL_ITEM_GRID: "item_grid",
+            _lib.PA_PREFILL_SIMPLE: "simple"}[out.value]
+
+
 def decode_tile_for(Hq, Hkv, head_dim, block_size, num_blocks, dtype=torch.bfloat16) -> str:
     """Tile the persistent decode kernel uses for these shapes: "tensor_core"
     (bf16, groups of 4 or 8 heads) or "cuda_core"."""

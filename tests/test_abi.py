@@ -166,6 +166,30 @@ def test_decode_tile_for_host_only(lib):
     assert lib.pa_decode_tile_for(32, 8, 96, 16, 100, 0, ctypes.byref(out)) == 1
 
 
+def test_prefill_kernel_for_host_only(lib):
+    """Prefill kernel choice from sizes alone (no device): the persistent grid
+    for batches of at most 256 (request, 256-row) pairs and 512 work items,
+    one CTA per item past that, the 128-thread kernel for 128-token blocks
+    and block tables longer than 1024 entries."""
+    from paged_kv_cache_192_gb300 import ops
+    # mixed batch: 4 chunks of 512 tokens, 32/8 heads -> 32 pairs, 256 items
+    assert ops.prefill_kernel_for(4, 512, 32, 8, 128, 16, 100000, 512) == "persistent"
+    # 64 items per KV head at 8 KV heads: exactly 512 items
+    assert ops.prefill_kernel_for(64, 64, 32, 8, 128, 16, 100000, 512) == "persistent"
+    assert ops.prefill_kernel_for(65, 64, 32, 8, 128, 16, 100000, 512) == "item_grid"
+    # 280 pairs of 2 KV heads (560 items): past both limits
+    assert ops.prefill_kernel_for(70, 200, 8, 2, 128, 16, 100000, 64) == "item_grid"
+    # groups of 8 heads: 32-token query tiles
+    assert ops.prefill_kernel_for(2, 1024, 64, 8, 128, 16, 100000, 512) == "persistent"
+    assert ops.prefill_kernel_for(4, 512, 32, 8, 128, 128, 100000, 64) == "simple"
+    assert ops.prefill_kernel_for(2, 64, 8, 2, 128, 8, 100000, 1038) == "simple"
+    out = ctypes.c_int(0)
+    assert lib.pa_prefill_kernel_for(4, 512, 32, 8, 96, 16, 100000, 512, ctypes.byref(out)) == 4
+    assert lib.pa_prefill_kernel_for(4, 512, 32, 8, 128, 24, 100000, 512, ctypes.byref(out)) == 4
+    assert lib.pa_prefill_kernel_for(-1, 512, 32, 8, 128, 16, 100000, 512, ctypes.byref(out)) == 1
+    assert lib.pa_prefill_kernel_for(4, 512, 32, 8, 128, 16, 100000, 512, None) == 1
+
+
 def test_contiguous_and_shared_workspace_sizes_host_only(lib):
     """Workspace sizes of the contiguous control and of the shared-prefix
     decode: the paged size for the same capacity, plus one prefix slot per

@@ -31,6 +31,11 @@ def _prefill_workload(priors, n_new, Hq=32, Hkv=8, d=128, bs=16, seed=0):
     return w, q
 
 
+def _kernel(w, n_new):
+    return ops().prefill_kernel_for(len(n_new), max(n_new), w.Hq, w.Hkv, w.d, w.bs,
+                                    w.num_blocks, w.table.shape[1])
+
+
 def _run(w, q, priors, n_new):
     k_cache, v_cache, table, lens = device_inputs(w, DEV)
     qs = torch.tensor(np.concatenate([[0], np.cumsum(n_new)]), dtype=torch.int32, device=DEV)
@@ -60,8 +65,40 @@ def test_prefill_many_requests_natural_order():
     n_new[3] = 200
     priors = [int(x) for x in rng.integers(0, 300, size=70)]
     w, q = _prefill_workload(priors, n_new, Hq=8, Hkv=2, seed=5)
+    assert _kernel(w, n_new) == "item_grid"
     got, ref = _run(w, q, priors, n_new)
     compare(got, ref, torch.bfloat16, "prefill 70 requests")
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,bs,R,nmax", [
+    (32, 8, 128, 8, 30, 128),    # groups of 4: 2 query tiles of 64 tokens, 480 items
+    (16, 8, 64, 16, 60, 128),    # groups of 2, head_dim 64: 480 items
+    (64, 8, 128, 32, 12, 160),   # groups of 8: 32-token tiles, 5 per request, 480 items
+    (8, 8, 128, 64, 60, 256),    # groups of 1: 256-token tiles, 480 items
+])
+def test_prefill_persistent_item_lists(Hq, Hkv, d, bs, R, nmax):
+    """More work items than SMs on the persistent grid: each CTA runs a list
+    of about three items (longest first to the least-loaded CTA), so the
+    query-tile, K/V-ring and TMEM pipelines cross item boundaries.  Ragged
+    chunks over ragged priors; every row against the oracle."""
+    rng = np.random.default_rng(11 + R)
+    n_new = [int(x) for x in rng.integers(1, nmax + 1, size=R)]
+    n_new[0] = nmax
+    priors = [int(x) for x in rng.integers(0, 700, size=R)]
+    w, q = _prefill_workload(priors, n_new, Hq, Hkv, d, bs, seed=R)
+    assert _kernel(w, n_new) == "persistent"
+    got, ref = _run(w, q, priors, n_new)
+    compare(got, ref, torch.bfloat16, f"persistent prefill {Hq}/{Hkv} d{d} bs{bs} R{R}")
+
+
+def test_prefill_persistent_one_item_per_kv_head():
+    """Fewer items than SMs: one request of 3 new tokens over 61 prior ones
+    gives 8 CTAs of one item each."""
+    priors, n_new = [61], [3]
+    w, q = _prefill_workload(priors, n_new, seed=12)
+    assert _kernel(w, n_new) == "persistent"
+    got, ref = _run(w, q, priors, n_new)
+    compare(got, ref, torch.bfloat16, "persistent prefill, one item per KV head")
 
 
 @pytest.mark.parametrize("bs", [128])
@@ -70,6 +107,7 @@ def test_prefill_large_block_fallback_kernel(bs):
     priors = [0, 200, 77, 1000]
     n_new = [100, 129, 3, 64]
     w, q = _prefill_workload(priors, n_new, Hq=8, Hkv=2, bs=bs, seed=6)
+    assert _kernel(w, n_new) == "simple"
     got, ref = _run(w, q, priors, n_new)
     compare(got, ref, torch.bfloat16, f"prefill bs{bs}")
 
@@ -120,6 +158,8 @@ def test_mixed_config_full_size():
     n = pre.extra["chunk"]
     R = pre.B
     qs = torch.arange(0, (R + 1) * n, n, dtype=torch.int32, device=DEV)
+    assert ops().prefill_kernel_for(R, n, pre.Hq, pre.Hkv, pre.d, pre.bs, dec.num_blocks,
+                                    pre.table.shape[1]) == "persistent"
     out_p = ops().prefill_chunk(pre.q.to(DEV), k_cache, v_cache, torch.from_numpy(pre.table).to(DEV),
                                 qs, torch.from_numpy(pre.lens.astype(np.int32)).to(DEV), n)
     torch.cuda.synchronize()

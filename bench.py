@@ -145,6 +145,17 @@ def source_sha1(*names):
     return h.hexdigest()
 
 
+# kernel sources each traffic record is keyed to (the decode call of a
+# workload; the prefill chunk of the mixed batch)
+DECODE_SOURCES = ("pa_decode.cu", "pa_device.cuh")
+PREFIX_SOURCES = DECODE_SOURCES + ("pa_prefill.cu", "pa_prefill.cuh", "pa_tcgen05.cuh")
+PREFILL_SOURCES = ("pa_prefill_persist.cu", "pa_prefill.cuh", "pa_tcgen05.cuh", "pa_device.cuh")
+
+
+def traffic_sources(workload):
+    return PREFIX_SOURCES if workload == "prefix" else DECODE_SOURCES
+
+
 def kernel_traffic(record, *sources):
     """ncu DRAM bytes per launch of a kernel, if recorded for its current
     source (else None)."""
@@ -560,6 +571,12 @@ class MixedPlan(Plan):
         self.step_bytes = (self.decode_bytes + prefill_kv +
                            store_bytes(self.T, dec.Hkv, dec.d, dec.dtype))
         self.prefill_flops = prefill_flops(priors, [n] * R, pre.Hq, pre.d)
+        self.prefill_kernel = {
+            "persistent": f"prefill_persist_kernel<{pre.d},{pre.Hq // pre.Hkv}>",
+            "item_grid": f"prefill_tc2_kernel<{pre.d},{pre.Hq // pre.Hkv}>",
+            "simple": f"prefill_tc_kernel<{pre.d},{pre.Hq // pre.Hkv}>"}[
+            ops.prefill_kernel_for(R, n, pre.Hq, pre.Hkv, pre.d, pre.bs, dec.num_blocks,
+                                   pre.max_blocks)]
         self.tokens = dec.B + R * n
         self.launches = 2 + n_dec
         self.extra = {"prefill_flops": self.prefill_flops, "priors": [int(x) for x in priors]}
@@ -749,7 +766,7 @@ def run_gpu(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "traffic": kernel_traffic(f"decode_traffic_{args.workload}.json",
-                                               "pa_decode.cu", "pa_device.cuh"),
+                                               *traffic_sources(args.workload)),
                      "kernel": plan.decode_kernel,
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "avg_launch_us": round(dec_ms * 1e3, 2),
@@ -767,7 +784,9 @@ def run_gpu(args, world, rank, local):
         tf = plan.prefill_flops / (pre_ms / 1e3) / 1e12
         result["roofline_prefill"] = {
             "bound": "tensor", "achieved": round(tf, 2), "peak": bf16_sus, "unit": "TFLOP/s",
-            "frac": round(tf / bf16_sus, 4), "traffic": None, "kernel": "pa_prefill_chunk",
+            "frac": round(tf / bf16_sus, 4),
+            "traffic": kernel_traffic("prefill_traffic_mixed.json", *PREFILL_SOURCES),
+            "kernel": plan.prefill_kernel,
             "peak_source": f"{peak_kind} bf16_tflops_sustained",
             "avg_launch_us": round(pre_ms * 1e3, 2), "algorithmic_flops": plan.prefill_flops}
     if plan.extra:

@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::OFF_BAR);
     uint64_t *kv_full = bars, *kv_empty = bars + NST;
     uint64_t *s_full = bars + 2 * NST;  // [2 * group + buffer]
-    uint64_t *p_full = s_full + 4, *o_done = p_full + 2, *o_free = o_done + 2;
+    uint64_t *p_full = s_full + 4, *o_done = p_full + 2, *o_free = o_done + 2;  // o_done[1] unused
     uint64_t *q_full = o_free + 2, *q_empty = q_full + 1, *sched = q_empty + 1, *drain = sched + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + Lay::OFF_MISC);
     volatile int *fail = reinterpret_cast<volatile int *>(smem + Lay::OFF_MISC + 4);
@@ -418,7 +418,9 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
             }
             __syncwarp();
         };
-        // O_wg (+)= P_hi V + P_lo V; P of tile g sits in the S buffer it came from
+        // O_wg (+)= P_hi V + P_lo V; P of tile g sits in the S buffer it came
+        // from.  Group 1's PV is the tile's last MMA, so its commit also
+        // releases the K/V stage: kv_empty doubles as group 1's PV barrier.
         auto issue_pv = [&](int wg, int g, int acc0) {
             const uint64_t b0 = dv + static_cast<uint32_t>((g % NST) * kStage);
             const uint32_t ph = tmem + 256 + wg * 128 + (g & 1) * 64, pl = ph + 32;
@@ -430,7 +432,7 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
                     pa::tc::mma_ts(od, ph + ks * 8, b, kIdO, ks == 0 ? acc0 : 1);
                     pa::tc::mma_ts(od, pl + ks * 8, b, kIdO, 1);
                 }
-                pa::tc::commit(&o_done[wg]);
+                pa::tc::commit(wg == 0 ? &o_done[0] : &kv_empty[g % NST]);
             }
             __syncwarp();
         };
@@ -438,8 +440,8 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
             return __all_sync(pa::kFull, pa::mbar_wait(bar, parity));
         };
         // Per item: S(0) of both groups once its query tiles are in; then per
-        // tile: S(g+1) of both groups, PV(g) of group 0, PV(g) of group 1,
-        // release of the K/V stage.  After the item's last S the query tiles
+        // tile: S(g+1) of both groups, PV(g) of group 0, PV(g) of group 1
+        // (whose commit releases the K/V stage).  After the item's last S the query tiles
         // are released; its first PV per group waits until that group has
         // read the previous item's O out of TMEM.
         bool ok = true;
@@ -469,8 +471,6 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
                     pa::tc::fence_after();
                     issue_pv(wg, g, j > 0);
                 }
-                if (ok && pa::tc::elect_one()) pa::tc::commit(&kv_empty[g % NST]);
-                __syncwarp();
             }
         }
         if (!ok) *fail = 1;
@@ -482,6 +482,16 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
         const uint32_t o_col = wg * 128;
         const int m = wg * 128 + row;
         const float qs2 = p.qscale;  // softmax scale in log2 units
+        // PV of CTA tile gg of this group done: group 0 on o_done[0] (one
+        // phase per tile), group 1 on the K/V stage's release (one phase per
+        // NST tiles).  Either barrier is at most one phase from the one waited
+        // for: the phase before it belongs to a PV that ran before the S tile
+        // this warp read last, and the phase after it needs this group's P of
+        // a later tile.
+        auto pv_done = [&](int gg) {
+            return wg == 0 ? pa::mbar_wait(&o_done[0], gg & 1)
+                           : pa::mbar_wait(&kv_empty[gg % NST], (gg / NST) & 1);
+        };
         bool ok = true;
         int g = 0, k;
         for (int it = 0; ok && next_item(it, &k); ++it) {
@@ -540,7 +550,7 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
                                  ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
                 lsum = lsum * alpha + rs;
                 if (j > 0) {  // PV of the previous tile must be done before O is rescaled
-                    ok = pa::mbar_wait(&o_done[wg], (g - 1) & 1);
+                    ok = pv_done(g - 1);
                     if (!ok) break;
                     pa::tc::fence_after();
                     if (__any_sync(pa::kFull, alpha != 1.f)) {
@@ -579,7 +589,7 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
                 if (lane == 0) mbar_arrive(&p_full[wg]);
             }
             if (!ok) break;
-            ok = pa::mbar_wait(&o_done[wg], (g - 1) & 1);  // PV of the item's last tile
+            ok = pv_done(g - 1);  // PV of the item's last tile
             if (!ok) break;
             pa::tc::fence_after();
             const int t = I.t0 + m / GQ;

@@ -91,6 +91,53 @@ def test_prefill_persistent_item_lists(Hq, Hkv, d, bs, R, nmax):
     compare(got, ref, torch.bfloat16, f"persistent prefill {Hq}/{Hkv} d{d} bs{bs} R{R}")
 
 
+@pytest.mark.parametrize("R,want", [(64, "persistent"), (65, "item_grid")])
+def test_prefill_item_count_boundary(R, want):
+    """64-token chunks of 32/8 heads: R requests give R x 8 work items; 512
+    items still run on the persistent grid, 513+ on one CTA per item.  Both
+    sides of the boundary against the oracle."""
+    rng = np.random.default_rng(20 + R)
+    n_new = [64] * R
+    priors = [int(x) for x in rng.integers(0, 200, size=R)]
+    w, q = _prefill_workload(priors, n_new, seed=R)
+    assert _kernel(w, n_new) == want
+    got, ref = _run(w, q, priors, n_new)
+    compare(got, ref, torch.bfloat16, f"prefill {R} requests ({want})")
+
+
+def test_prefill_persistent_many_one_tile_items():
+    """504 one-tile items (63 requests of 1..64 new tokens, no prior context):
+    each CTA runs three or four short items back to back, so every item
+    boundary (query tiles reloaded, O handed over, barrier phases carried on)
+    is exercised many times."""
+    rng = np.random.default_rng(31)
+    n_new = [int(x) for x in rng.integers(1, 65, size=63)]
+    n_new[0] = 64
+    priors = [0] * 63
+    w, q = _prefill_workload(priors, n_new, seed=31)
+    assert _kernel(w, n_new) == "persistent"
+    got, ref = _run(w, q, priors, n_new)
+    compare(got, ref, torch.bfloat16, "persistent prefill, 504 one-tile items")
+
+
+def test_prefill_max_query_len_above_longest_chunk():
+    """max_query_len larger than every request's new tokens: the extra query
+    tiles have no work and the query rows' bound (R x max_query_len) exceeds
+    the tokens present."""
+    priors, n_new = [40, 0, 300], [17, 90, 5]
+    w, q = _prefill_workload(priors, n_new, seed=13)
+    k_cache, v_cache, table, lens = device_inputs(w, DEV)
+    qs = torch.tensor(np.concatenate([[0], np.cumsum(n_new)]), dtype=torch.int32, device=DEV)
+    assert ops().prefill_kernel_for(3, 400, w.Hq, w.Hkv, w.d, w.bs, w.num_blocks,
+                                    w.table.shape[1]) == "persistent"
+    out = ops().prefill_chunk(q.to(DEV), k_cache, v_cache, table, qs, lens, 400)
+    torch.cuda.synchronize()
+    assert ops().device_error() == 0
+    ref = oracle.prefill_chunk(q.double().numpy(), w.k.double().numpy(), w.v.double().numpy(),
+                               n_new, priors, 1.0 / np.sqrt(w.d))
+    compare(out.double().cpu().numpy(), ref, torch.bfloat16, "prefill, max_query_len 400")
+
+
 def test_prefill_persistent_one_item_per_kv_head():
     """Fewer items than SMs: one request of 3 new tokens over 61 prior ones
     gives 8 CTAs of one item each."""

@@ -12,9 +12,13 @@
 // A row is one (query token, query head) pair, so the GQ heads that share a
 // KV head share every K/V tile (GQA packed into the M dimension); K/V tiles
 // of 64 tokens; online softmax in the log2 domain with a lazy rescale.
-// Three kernels:
-//   prefill_tc2_kernel  (default) warp-specialised tcgen05: TMA loader warp,
-//                       MMA warp, two softmax warp groups over 2 x 128 rows;
+// Kernels (pa_prefill_kernel_for picks one from the sizes):
+//   prefill_persist_kernel (pa_prefill_persist.cu; batches of at most 512
+//                       work items) one CTA per SM running a list of work
+//                       items with the warp specialisation below;
+//   prefill_tc2_kernel  (larger batches) warp-specialised tcgen05, one CTA per
+//                       work item: TMA loader warp, MMA warp, two softmax
+//                       warp groups over 2 x 128 rows;
 //   prefill_tc_kernel   (block sizes outside 8..64, block tables longer than
 //                       1024 entries) 128 threads per 128 rows, tcgen05,
 //                       cp.async K/V;

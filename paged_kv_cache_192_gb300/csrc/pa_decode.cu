@@ -1653,8 +1653,13 @@ int sm_count() {
     return sms;
 }
 
+struct SharedPlan;
+int launch_prefix_any(const DecodeParams &p, const SharedPlan &sp, int D, bool after_decode,
+                      cudaStream_t stream);
+
 template <typename T, int D, int GQ, bool MMA>
-int launch_persistent(const DecodeParams &p, cudaStream_t stream) {
+int launch_persistent(const DecodeParams &p, cudaStream_t stream,
+                      const SharedPlan *prefix_after = nullptr) {
     using C = typename AttnOf<T, D, GQ, MMA>::type::C;
     const size_t smem = C::OFF_BT + sizeof(int32_t) * (3 * p.B + 1) + (MMA ? 1024 : 0);
     auto kern = decode_persistent_kernel<T, D, GQ, MMA>;
@@ -1684,6 +1689,11 @@ int launch_persistent(const DecodeParams &p, cudaStream_t stream) {
     e = launch_dependent(kern, dim3(grid), dim3(kWarps * 32), smem, stream, p, kmap, vmap);
     if (e != cudaSuccess) return pa::cuda_fail(e, "decode launch");
     if (int rc = pa::check_launch("decode launch")) return rc;
+    // shared-prefix partials on the tcgen05 kernel go behind the decode grid:
+    // they read none of its results, so their CTAs take the SMs its CTAs
+    // leave; the merge behind them then finds both complete
+    if (prefix_after)
+        if (int rc = launch_prefix_any(p, *prefix_after, D, true, stream)) return rc;
     const int64_t items = int64_t(p.B) * p.Hkv;
     e = launch_dependent(partial_merge_kernel<T, D, GQ>, dim3(static_cast<unsigned>(items)),
                          dim3(GQ * 32), 0, stream, p);
@@ -1778,8 +1788,10 @@ struct SharedPlan {
     bool tc;  // tcgen05 prefill kernel in prefix mode, else prefix_kernel
 };
 
-int launch_prefix_any(const DecodeParams &p, const SharedPlan &sp, int D, cudaStream_t stream) {
+int launch_prefix_any(const DecodeParams &p, const SharedPlan &sp, int D, bool after_decode,
+                      cudaStream_t stream) {
     pa::PrefixTcArgs a{};
+    a.after_decode = after_decode;
     a.q = p.q;
     a.k_cache = p.k_cache;
     a.v_cache = p.v_cache;
@@ -1812,12 +1824,14 @@ template <typename T, int D, int GQ>
 int launch(const DecodeParams &p, const SharedPlan *sp, cudaStream_t stream) {
     if constexpr (std::is_same<T, __nv_bfloat16>::value) {
         if (sp) {  // the host checked: bf16, persistent kernel, 32-bit pool rows
-            if (int rc = sp->tc ? launch_prefix_any(p, *sp, D, stream)
-                                : launch_prefix<D, GQ>(p, sp->pp, sp->max_group_size, stream))
-                return rc;
+            // the tcgen05 prefix kernel runs behind the decode grid, the
+            // warp-level one before it
+            const SharedPlan *after = sp->tc ? sp : nullptr;
+            if (!sp->tc)
+                if (int rc = launch_prefix<D, GQ>(p, sp->pp, sp->max_group_size, stream)) return rc;
             if constexpr (GQ % 2 == 0 && GQ >= PA_DECODE_MMA_MIN_GQ)
-                if (use_mma<T, GQ>(p)) return launch_persistent<T, D, GQ, true>(p, stream);
-            return launch_persistent<T, D, GQ, false>(p, stream);
+                if (use_mma<T, GQ>(p)) return launch_persistent<T, D, GQ, true>(p, stream, after);
+            return launch_persistent<T, D, GQ, false>(p, stream, after);
         }
     }
     const int sms = sm_count();

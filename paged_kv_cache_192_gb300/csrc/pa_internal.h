@@ -60,6 +60,10 @@ struct PrefixTcArgs {
     int64_t num_blocks;
     int B, Hq, Hkv, D, bs, MB, G, nc, max_group_size, num_members, rowslots, pslot0;
     float qscale;  // softmax scale * log2(e)
+    // launched behind the decode grid (whose trigger follows its own wait for
+    // the inputs) instead of before it: the kernel waits for that grid only
+    // before exiting, so its CTAs fill the SMs the decode grid leaves
+    bool after_decode;
 };
 inline int prefix_tc_members(int gq) { return 256 / gq; }
 // Block sizes 8..64, 32-bit pool rows and chunks of at most 1024 blocks.

@@ -625,8 +625,14 @@ __global__ void __launch_bounds__(Tc2Layout<D, NQ>::THREADS, 3 - NQ)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // launched as a programmatic dependent in prefix mode: inputs are ready
-    // past this point (a no-op otherwise)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // past this point (a no-op otherwise).  Behind the decode grid
+    // (pfx_wait_end) the inputs were complete before that grid started this
+    // one, and the wait moves to every exit instead.
+    const bool wait_end = PFX && p.pfx_wait_end;
+    if (!wait_end) asm volatile("griddepcontrol.wait;" ::: "memory");
+    auto exit_wait = [&]() {
+        if (wait_end) asm volatile("griddepcontrol.wait;" ::: "memory");
+    };
     int hk, kv_end, ntiles, nblk;
     const int32_t *bt_g;
     int qs = 0, n = 0, t0 = 0, P = 0;            // chunked-prefill work item
@@ -642,11 +648,15 @@ __global__ void __launch_bounds__(Tc2Layout<D, NQ>::THREADS, 3 - NQ)
         const int mbeg = p.pfx_group_start[g], mend = p.pfx_group_start[g + 1];
         if (mbeg < 0 || mend > p.pfx_members || mbeg > mend) {
             if (tid == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+            exit_wait();
             return;
         }
         pm0 = mbeg + mt * QTOK;
         pmend = mend;
-        if (pm0 >= mend) return;
+        if (pm0 >= mend) {
+            exit_wait();
+            return;
+        }
         const int b0 = p.pfx_group_seqs[mbeg];  // its table row holds the shared blocks
         if (b0 >= 0 && b0 < p.pfx_B) {
             pS = p.pfx_shared_len[b0];
@@ -655,6 +665,7 @@ __global__ void __launch_bounds__(Tc2Layout<D, NQ>::THREADS, 3 - NQ)
         }
         if (pS == 0) {
             if (tid == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+            exit_wait();
             return;
         }
         const int ch = ((pS + kT2KT - 1) / kT2KT + p.pfx_nc - 1) / p.pfx_nc * kT2KT;
@@ -718,6 +729,7 @@ __global__ void __launch_bounds__(Tc2Layout<D, NQ>::THREADS, 3 - NQ)
     }
     if (nblk > Lay::BT_MAX) {  // the host routes such requests elsewhere
         if (tid == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+        exit_wait();
         return;
     }
     // prefix mode: the decode-workspace row of CTA row m (-1: no member)
@@ -740,6 +752,7 @@ __global__ void __launch_bounds__(Tc2Layout<D, NQ>::THREADS, 3 - NQ)
                     *reinterpret_cast<float4 *>(p.pfx_acc + slot * D + c) =
                         make_float4(0.f, 0.f, 0.f, 0.f);
             }
+            exit_wait();
             return;
         }
     }
@@ -1072,6 +1085,7 @@ __global__ void __launch_bounds__(Tc2Layout<D, NQ>::THREADS, 3 - NQ)
         __syncthreads();
     }
     if (warp == Lay::MMA_WARP) pa::tc::dealloc(tmem, Lay::TMEM_COLS);
+    exit_wait();
 }
 
 
@@ -1192,6 +1206,7 @@ int launch_prefix_tc_t(const pa::PrefixTcArgs &a, cudaStream_t stream) {
     p.pfx_rowslots = a.rowslots;
     p.pfx_pslot0 = a.pslot0;
     p.pfx_B = a.B;
+    p.pfx_wait_end = a.after_decode ? 1 : 0;
     const int64_t rows = (a.num_blocks * a.Hkv) << p.bs_log2;
     CUtensorMap kmap, vmap;
     if (int rc = pa::pool_tensor_map(&kmap, a.k_cache, rows, D, a.bs)) return rc;

@@ -41,6 +41,10 @@ struct PrefillParams {
     const int32_t *pfx_group_start, *pfx_group_seqs, *pfx_shared_len;
     float *pfx_acc, *pfx_ml;
     int pfx_G, pfx_nc, pfx_nmt, pfx_members, pfx_rowslots, pfx_pslot0, pfx_B;
+    // prefix mode launched behind the decode grid, whose outputs it does not
+    // read: no wait before the work, a wait for that grid before exiting (so
+    // that a kernel waiting for this one also finds the decode complete)
+    int pfx_wait_end;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {

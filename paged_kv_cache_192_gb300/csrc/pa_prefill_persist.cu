@@ -20,7 +20,7 @@
 // Warps: 0-3 and 4-7 softmax of the item's two 128-row query tiles, 8 issues
 // every tcgen05.mma (one lane), 9 loads K/V tiles with TMA through a 4-stage
 // ring, 10 schedules and then loads each item's query tiles (3D tensor
-// copies of 8-row boxes).
+// copies: one 16 KB box per full tile and 64 columns).
 // TMEM (512 columns): O_A [0,128), O_B [128,256), S_A[0..1] [256,384),
 // S_B[0..1] [384,512).  Every barrier phase follows a CTA-wide tile or item
 // counter, so the pipelines run across item boundaries; every wait is bounded.

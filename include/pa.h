@@ -280,7 +280,10 @@ int pa_decode_contiguous(void *out, const void *q, const void *k, const void *v,
  * Validate mode checks every rule above.  Calls that cannot take the shared
  * path (fp32, batches that pa_decode_kernel_for sends to the grid kernel,
  * pools of 2^31 rows or more) decode every sequence whole, which gives the
- * same result.  Launches: the prefix kernel, then pa_decode's two.
+ * same result.  Launches (each a programmatic dependent of the one before):
+ * block sizes 8..64: the decode grid, the tcgen05 prefix kernel (it reads none
+ * of the decode's results and waits for it only before exiting), the merge;
+ * other block sizes: the warp-level prefix kernel, the decode grid, the merge.
  * Outside validate mode, a member whose own shared_len is not a positive
  * multiple of block_size below its context length is decoded whole and
  * PA_DEVERR_BAD_BLOCK is recorded; members that disagree with their group's

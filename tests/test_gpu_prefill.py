@@ -138,6 +138,32 @@ def test_prefill_max_query_len_above_longest_chunk():
     compare(out.double().cpu().numpy(), ref, torch.bfloat16, "prefill, max_query_len 400")
 
 
+@pytest.mark.parametrize("bs,R,want", [(16, 3, "persistent"), (16, 70, "item_grid"),
+                                       (128, 3, "simple")])
+def test_prefill_bad_block_id_is_recorded_not_faulted(bs, R, want):
+    """An out-of-pool block-table entry of request 0 is replaced by block 0 in
+    every prefill kernel and reported in the device error word (no
+    out-of-bounds access); the other requests' rows still match the oracle."""
+    from paged_kv_cache_192_gb300._lib import PA_DEVERR_BAD_BLOCK
+    rng = np.random.default_rng(40 + R)
+    n_new = [64] + [int(x) for x in rng.integers(1, 65, size=R - 1)]
+    priors = [200] + [int(x) for x in rng.integers(0, 200, size=R - 1)]
+    w, q = _prefill_workload(priors, n_new, Hq=8, Hkv=8, bs=bs, seed=40 + R)
+    assert _kernel(w, n_new) == want
+    k_cache, v_cache, table, lens = device_inputs(w, DEV)
+    table[0, 1] = w.num_blocks + 5
+    qs = torch.tensor(np.concatenate([[0], np.cumsum(n_new)]), dtype=torch.int32, device=DEV)
+    ops().device_error(clear=True)
+    out = ops().prefill_chunk(q.to(DEV), k_cache, v_cache, table, qs, lens, max(n_new))
+    torch.cuda.synchronize()
+    assert ops().device_error(clear=True) & PA_DEVERR_BAD_BLOCK
+    ref = oracle.prefill_chunk(q.double().numpy(), w.k.double().numpy(), w.v.double().numpy(),
+                               n_new, priors, 1.0 / np.sqrt(w.d))
+    keep = slice(n_new[0], None)  # rows of requests 1..R-1
+    compare(out.double().cpu().numpy()[keep], ref[keep], torch.bfloat16,
+            f"prefill ({want}) rows beside a bad block id")
+
+
 def test_prefill_persistent_one_item_per_kv_head():
     """Fewer items than SMs: one request of 3 new tokens over 61 prior ones
     gives 8 CTAs of one item each."""

@@ -436,19 +436,39 @@ class PrefixPlan(Plan):
         self.outputs = {"out": torch.empty_like(self.inputs["q"])}
         self.PT = args.partition
         # every sequence takes the 1024-token system prompt from one group's
-        # shared blocks (the children's parent suffix blocks stay private reads)
-        self.shared = args.prefix_path == "shared"
+        # shared blocks (default); with forks each child also takes the blocks
+        # before its fork point from its parent's reads (measured slower here:
+        # the fork kernel's wider slot rows and extra per-tile work cost more
+        # than the 38 MB of reads it saves)
+        self.path = args.prefix_path
+        self.shared = self.path in ("shared", "forks")
         Bd = B + nf
+        pos = {int(o): k for k, o in enumerate(dec_order)}
+        fork_parent = np.full(Bd, -1, dtype=np.int32)
+        fork_len = np.zeros(Bd, dtype=np.int32)
+        for i, par in enumerate(pf.parents):
+            # the parent's blocks at the fork, but its last, partly filled one
+            # (copied on write by whichever writes first)
+            fork_parent[pos[B + i]] = pos[int(par)]
+            fork_len[pos[B + i]] = (int(w.lens[par]) - 1) // bs * bs
         self.inputs.update({
             "shared_len": torch.full((Bd,), P, dtype=torch.int32, device=dev),
             "group_start": torch.tensor([0, Bd], dtype=torch.int32, device=dev),
-            "group_seqs": torch.arange(Bd, dtype=torch.int32, device=dev)})
+            "group_seqs": torch.arange(Bd, dtype=torch.int32, device=dev),
+            "fork_parent": torch.from_numpy(fork_parent).to(dev),
+            "fork_len": torch.from_numpy(fork_len).to(dev)})
         self.P = P
         if self.shared:
-            self.ws_bytes = ops.decode_shared_workspace_size(Bd, Hq, d, MB, bs, self.PT, P)
+            wsf = (ops.decode_shared_forks_workspace_size if self.path == "forks"
+                   else ops.decode_shared_workspace_size)
+            self.ws_bytes = wsf(Bd, Hq, d, MB, bs, self.PT, P)
             name, n_dec = decode_kernel_info(Bd, Hq, Hkv, d, MB, bs, NB, self.PT)
-            self.decode_kernel = ("pa_decode_shared (prefix_kernel: the shared prompt once per "
-                                  "KV head for all members on tensor cores; then " + name + ")")
+            self.decode_kernel = (
+                ("pa_decode_shared_forks" if self.path == "forks" else "pa_decode_shared") +
+                " (" + name + "; then the shared prompt once per KV head for all members on "
+                "tensor cores" + ("; each child's query heads ride with its parent's reads "
+                                  "over the blocks before its fork" if self.path == "forks"
+                                  else "") + ")")
             n_dec += 1
         else:
             self.ws_bytes = ops.decode_workspace_size(Bd, Hq, d, MB, bs, self.PT)
@@ -473,8 +493,12 @@ class PrefixPlan(Plan):
                        "suffix_len": "U[1,512]", "Hq": Hq, "Hkv": Hkv, "head_dim": d,
                        "block_size": bs, "pool_blocks": NB, "partition_tokens": self.PT,
                        "cow_pairs": self.npairs,
-                       "decode": ("pa_decode_shared, one group of all sequences over the "
-                                  f"{P}-token prompt" if self.shared else "pa_decode")}
+                       "decode": {"forks": "pa_decode_shared_forks, one group of all "
+                                           f"sequences over the {P}-token prompt and the "
+                                           f"{nf} forks",
+                                  "shared": "pa_decode_shared, one group of all sequences "
+                                            f"over the {P}-token prompt",
+                                  "plain": "pa_decode"}[self.path]}
         self.oracle_sample = lambda n, seed, threads=None: time_oracle_decode(w, n, seed, threads)
 
     def run(self, i, L, sp, ev=None, src=None, dst=None):
@@ -489,7 +513,16 @@ class PrefixPlan(Plan):
                                      self.Hkv, self.bs, self.d, PA_BF16, sp))
         if ev:
             ev["decode"][0].record()
-        if self.shared:
+        if self.path == "forks":
+            check(L.pa_decode_shared_forks(
+                (dst or self.outputs)["out"].data_ptr(), x["q"].data_ptr(), kc.data_ptr(),
+                vc.data_ptr(), x["table"].data_ptr(), self.MB, x["lens"].data_ptr(), self.Bd,
+                self.Hq, self.Hkv, self.d, self.bs, self.NB, 1.0 / math.sqrt(self.d), self.PT,
+                x["shared_len"].data_ptr(), x["group_start"].data_ptr(),
+                x["group_seqs"].data_ptr(), 1, self.Bd, self.Bd, self.P,
+                x["fork_parent"].data_ptr(), x["fork_len"].data_ptr(), self.ws.data_ptr(),
+                self.ws_bytes, PA_BF16, sp))
+        elif self.shared:
             check(L.pa_decode_shared(
                 (dst or self.outputs)["out"].data_ptr(), x["q"].data_ptr(), kc.data_ptr(),
                 vc.data_ptr(), x["table"].data_ptr(), self.MB, x["lens"].data_ptr(), self.Bd,
@@ -765,8 +798,10 @@ def run_gpu(args, world, rank, local):
         "pct_of_hbm_peak": round(100 * value / hbm, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "traffic": kernel_traffic(f"decode_traffic_{args.workload}.json",
-                                               *traffic_sources(args.workload)),
+                     # the prefix record was taken on the default (shared) path
+                     "traffic": (kernel_traffic(f"decode_traffic_{args.workload}.json",
+                                                *traffic_sources(args.workload))
+                                 if getattr(plan, "path", "shared") == "shared" else None),
                      "kernel": plan.decode_kernel,
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "avg_launch_us": round(dec_ms * 1e3, 2),
@@ -896,9 +931,10 @@ def main(argv=None):
     ap.add_argument("--layout", choices=["paged", "contiguous"], default="paged",
                     help="decode workloads: paged pools, or the contiguous-reservation control "
                          "(pa_decode_contiguous, no block table)")
-    ap.add_argument("--prefix-path", choices=["shared", "plain"], default="shared",
-                    help="prefix workload: decode with the shared-prefix groups (pa_decode_shared) "
-                         "or every sequence whole (pa_decode)")
+    ap.add_argument("--prefix-path", choices=["shared", "forks", "plain"], default="shared",
+                    help="prefix workload: decode with the prompt group (pa_decode_shared), "
+                         "the prompt group and the forks (pa_decode_shared_forks) or every "
+                         "sequence whole (pa_decode)")
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pools", type=int, default=N_POOLS, help="pools rotated between steps")

@@ -54,6 +54,12 @@ SIGNATURES = {
                                   _c_int, _c_int, _c_int, _c_int, _c_i64, _c_f, _c_int, _c_vp,
                                   _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_int, _c_vp, _c_sz,
                                   _c_int, _c_vp]),
+    "pa_decode_shared_forks_workspace_size": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int,
+                                                       _c_int, _c_int, ctypes.POINTER(_c_sz)]),
+    "pa_decode_shared_forks": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp,
+                                        _c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_f,
+                                        _c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int,
+                                        _c_int, _c_vp, _c_vp, _c_vp, _c_sz, _c_int, _c_vp]),
     "pa_decode_noalloc_capacity": (_c_sz, []),
     "pa_decode_noalloc": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_int,
                                    _c_int, _c_int, _c_int, _c_i64, _c_f, _c_int, _c_int, _c_vp]),

@@ -139,7 +139,12 @@ struct DecodeParams {
     int B, Hq, Hkv, bs, bs_log2, MB, PT, max_parts, maxseg;
     int rowslots;                // partial slots per (sequence, query head)
     int pslot0, npfx;            // shared-prefix partials: slots pslot0 .. pslot0+npfx-1
+    // forked children (pa_decode_shared_forks): fork_parent[b] >= 0 names the
+    // row whose blocks [0, fork_len[b]) row b shares; the parent's items then
+    // serve b's heads over [shared_len, fork_len) too (NULL: none)
+    const int32_t *fork_parent, *fork_len;
     int contig_len;              // > 0: contiguous caches [B][Hkv][contig_len][D], no table
+    int early_dependents;        // persistent kernel: release the next kernel at the start
     float qscale;                // scale * log2(e)
 };
 
@@ -465,13 +470,15 @@ __device__ __forceinline__ void WarpAttn<T, D, GQ>::store_out(T *outh, const flo
 // context get score -inf and their V rows are zeroed in shared memory (a
 // stale row may hold NaN; 0 * NaN = NaN).
 // ---------------------------------------------------------------------------
-template <int D, int GQ>
+// QH: query rows carried in a stage with an item's first tile (GQ, or 2 GQ
+// when an item also serves a forked child's heads in the spare columns).
+template <int D, int GQ, int QH = GQ>
 struct MmaCfg {
     static constexpr int TT = 16;               // tokens per tile (the M of the first product)
     static constexpr int HALVES = D / 64;       // 128-byte column blocks of a row (64 bf16)
     static constexpr int HALF = TT * 128;       // bytes of one column block of one cache's tile
     static constexpr int TILE = HALVES * HALF;  // one cache's tile
-    static constexpr int QB = GQ * D * 2;       // the group's q rows (first tile of an item)
+    static constexpr int QB = QH * D * 2;       // the q rows (first tile of an item)
     // K, V, then q; stages stay 1024-byte aligned for the swizzle
     static constexpr int STAGE = (2 * TILE + QB + 1023) / 1024 * 1024;
     static constexpr int NST = kRingBytes / STAGE >= 2 ? kRingBytes / STAGE : 2;
@@ -484,13 +491,13 @@ struct MmaCfg {
     static constexpr int OFF_FLAG = OFF_BAR + kWarps * NST * 8;
     static constexpr int OFF_BT = OFF_FLAG + 16;
     static constexpr int KS = D / 16;           // k-steps of QK^T = m-tiles of PV
-    static_assert(D % 64 == 0 && GQ <= 8 && 8 % GQ == 0, "tensor-core tile shape");
+    static_assert(D % 64 == 0 && GQ <= 8 && 8 % GQ == 0 && QH <= 8, "tensor-core tile shape");
     static_assert(HALF % 1024 == 0 && STAGE % 1024 == 0, "swizzle atoms must stay aligned");
 };
 
-template <int D, int GQ>
+template <int D, int GQ, int QH = GQ>
 struct MmaAttn {
-    using C = MmaCfg<D, GQ>;
+    using C = MmaCfg<D, GQ, QH>;
     static constexpr int KS = C::KS;
     int lane, g, t, grp;
     float *qs;  // unused (interface of WarpAttn)
@@ -542,12 +549,12 @@ struct MmaAttn {
     // q of the item from the stage (the producer copied the group's GQ rows
     // there with the item's first tile): lane (g, t) takes head g's dims
     // 16k + 2t (+1) and 16k + 2t + 8 (+9) as its B fragments.
-    __device__ __forceinline__ void load_q_smem(uint32_t qaddr, float qscale_) {
+    __device__ __forceinline__ void load_q_smem(uint32_t qaddr, float qscale_, int ncols = GQ) {
         qscale = qscale_;
 #pragma unroll
         for (int k = 0; k < KS; ++k) {
             uint32_t b0 = 0u, b1 = 0u;
-            if (g < GQ) {
+            if (g < ncols) {
                 const uint32_t a = qaddr + g * D * 2 + (16 * k + 2 * t) * 2;
                 asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b0) : "r"(a));
                 asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b1) : "r"(a + 16));
@@ -573,8 +580,11 @@ struct MmaAttn {
         }
     }
 
+    // nvalid: tokens of the tile inside the context; with QH > GQ, the
+    // columns from GQ on (a forked child's heads) see only the first
+    // nvalid_hi of them.
     __device__ __forceinline__ void tile(uint32_t kaddr, uint32_t vaddr, int nvalid, float *,
-                                         float *) {
+                                         float *, int nvalid_hi = 0) {
         // ---- S^T = K q^T (two accumulators: shorter dependency chains) ----
         float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -596,7 +606,8 @@ struct MmaAttn {
             }
             __syncwarp();
         }
-        const bool v0 = g < nvalid, v1 = g + 8 < nvalid;
+        const int nv = (QH > GQ && 2 * t >= GQ) ? nvalid_hi : nvalid;
+        const bool v0 = g < nv, v1 = g + 8 < nv;
         const float x0 = v0 ? (s[0] + s2[0]) * qscale : -INFINITY;  // token g, head 2t
         const float x1 = v0 ? (s[1] + s2[1]) * qscale : -INFINITY;  // token g, head 2t+1
         const float x2 = v1 ? (s[2] + s2[2]) * qscale : -INFINITY;  // token g+8, head 2t
@@ -626,8 +637,12 @@ struct MmaAttn {
             m_run[0] = m0;
             m_run[1] = m1;
         }
-        const float p0 = fast_exp2(x0 - m_run[0]), p1 = fast_exp2(x1 - m_run[1]);
-        const float p2 = fast_exp2(x2 - m_run[0]), p3 = fast_exp2(x3 - m_run[1]);
+        // a column that has seen no token yet (m = -inf) takes p = 0, not
+        // exp2(-inf + inf): the forked child's columns past its fork point
+        const float mr0 = (QH > GQ && m_run[0] == -INFINITY) ? 0.f : m_run[0];
+        const float mr1 = (QH > GQ && m_run[1] == -INFINITY) ? 0.f : m_run[1];
+        const float p0 = fast_exp2(x0 - mr0), p1 = fast_exp2(x1 - mr1);
+        const float p2 = fast_exp2(x2 - mr0), p3 = fast_exp2(x3 - mr1);
         lsum[0] += p0 + p2;
         lsum[1] += p1 + p3;
         // ---- P^T as bf16 hi + lo B fragments --------------------------------
@@ -698,6 +713,29 @@ struct MmaAttn {
             *reinterpret_cast<float2 *>(ml_dst + (2 * t) * ml_stride) = make_float2(m_run[0], l.x);
             *reinterpret_cast<float2 *>(ml_dst + (2 * t + 1) * ml_stride) =
                 make_float2(m_run[1], l.y);
+        }
+    }
+
+    // The partial of columns GQ .. 2 GQ - 1 (a forked child's heads) into the
+    // child's rows: acc_dst / ml_dst address its head 0.
+    __device__ __forceinline__ void store_partial_hi(float *acc_dst, size_t head_stride,
+                                                     float *ml_dst, size_t ml_stride,
+                                                     const float (&lh)[GQ]) {
+        static_assert(QH == 2 * GQ && GQ % 2 == 0, "the child's heads fill columns GQ ..");
+        const float2 l = make_float2(lh[0], lh[1]);
+        const int c0 = 2 * t - GQ;
+        if (c0 < 0 || c0 >= GQ) return;
+        float *a0 = acc_dst + c0 * head_stride + g, *a1 = a0 + head_stride;
+#pragma unroll
+        for (int m = 0; m < KS; ++m) {
+            a0[16 * m] = acc[m][0];
+            a1[16 * m] = acc[m][1];
+            a0[16 * m + 8] = acc[m][2];
+            a1[16 * m + 8] = acc[m][3];
+        }
+        if (g == 0) {
+            *reinterpret_cast<float2 *>(ml_dst + c0 * ml_stride) = make_float2(m_run[0], l.x);
+            *reinterpret_cast<float2 *>(ml_dst + (c0 + 1) * ml_stride) = make_float2(m_run[1], l.y);
         }
     }
 };
@@ -817,20 +855,28 @@ __device__ __forceinline__ void produce_tile(const DecodeParams &p, const Cursor
 // into the stage: [K block 0 | K block 1 | V block 0 | V block 1] by 64-column
 // block.  Tiles longer than a block take one box per block; blocks past the
 // context are not copied (their rows are masked).
-template <int D, int GQ>
+template <int D, int GQ, int QH = GQ>
 __device__ __forceinline__ void produce_tile_tma(const DecodeParams &p, const Cursor &c, int blk,
                                                  uint8_t *stage, uint64_t *bar,
                                                  const CUtensorMap *kmap,
-                                                 const CUtensorMap *vmap, bool with_q = false) {
-    using C = MmaCfg<D, GQ>;
+                                                 const CUtensorMap *vmap, bool with_q = false,
+                                                 int child_row = -1) {
+    using C = MmaCfg<D, GQ, QH>;
+    constexpr uint32_t QG = GQ * D * 2;  // one sequence's group of q rows
     const uint32_t sk = pa::smem_u32(stage), sv = sk + C::TILE;
     const int tok = first_token(c, C::TT);
-    const uint32_t qbytes = with_q ? C::QB : 0u;
+    const bool with_child = QH > GQ && with_q && child_row >= 0;
+    const uint32_t qbytes = with_q ? QG * (with_child ? 2u : 1u) : 0u;
     if (with_q)  // the group's q rows, contiguous in q [B][Hq][D]
         pa::bulk_g2s(stage + 2 * C::TILE,
                      static_cast<const __nv_bfloat16 *>(p.q) +
                          (static_cast<size_t>(c.b) * p.Hq + c.hk * GQ) * D,
-                     C::QB, bar);
+                     QG, bar);
+    if (with_child)  // then the forked child's, for the spare columns
+        pa::bulk_g2s(stage + 2 * C::TILE + QG,
+                     static_cast<const __nv_bfloat16 *>(p.q) +
+                         (static_cast<size_t>(child_row) * p.Hq + c.hk * GQ) * D,
+                     QG, bar);
     if (p.contig_len || C::TT <= p.bs) {
         const int y = p.contig_len ? static_cast<int>(contig_row(p, c, tok))
                                    : (blk * p.Hkv + c.hk) * p.bs + (tok & (p.bs - 1));
@@ -916,10 +962,18 @@ __device__ __forceinline__ int slot_of(const DecodeParams &p, int i, int nseg) {
 // values) to its slot and partial_merge_kernel, launched behind this grid,
 // merges the item's partials.  The item's first segment records how many
 // there are.  No segment waits for, or signals, any other.
-template <typename T, int D, int GQ, typename St>
+// Fork tables of the persistent kernel (pa_decode_shared_forks), in shared
+// memory: each row's validated shared_len, the child its items also serve
+// (-1: none) and the parent whose items serve its fork range (-1: none).
+struct ForkTables {
+    const int32_t *slen, *child, *parent;
+};
+
+template <typename T, int D, int GQ, bool FORK = false, typename St>
 __device__ __forceinline__ void finish_segment(St &st, const DecodeParams &p,
                                                const BatchTables &bt, const Cursor &c,
-                                               int64_t per, int64_t w, int lane) {
+                                               int64_t per, int64_t w, int lane,
+                                               const ForkTables &ft = ForkTables{}) {
     float lh[GQ];
     st.reduce(lh);
     const int64_t ia = int64_t(p.Hkv) * bt.pre[c.b] + int64_t(c.hk) * c.nt;
@@ -927,11 +981,29 @@ __device__ __forceinline__ void finish_segment(St &st, const DecodeParams &p,
     const int nseg = static_cast<int>(wb - wa + 1), seg = static_cast<int>(w - wa);
     const size_t hq0 = static_cast<size_t>(c.b) * p.Hq + c.hk * GQ;
     // an item that starts after a shared prefix also merges the prefix partials
-    const int npre = c.s0 > 0 ? p.npfx : 0;
-    const bool whole = nseg == 1 && npre == 0;
+    int npre = c.s0 > 0 ? p.npfx : 0;
+    int npair = 0;  // a forked child's partials from its parent's item segments
+    if constexpr (FORK) {
+        npre = ft.slen[c.b] > 0 ? p.npfx : 0;
+        const int par = ft.parent[c.b];
+        if (par >= 0) {
+            const int ntp = bt.pre[par + 1] - bt.pre[par];
+            const int64_t iap = int64_t(p.Hkv) * bt.pre[par] + int64_t(c.hk) * ntp;
+            npair = static_cast<int>((iap + ntp - 1) / per - iap / per + 1);
+        }
+        const int cr = ft.child[c.b];
+        if (cr >= 0) {  // this segment's partial for the child's heads, after its prefix slots
+            const size_t hqc = static_cast<size_t>(cr) * p.Hq + c.hk * GQ;
+            const size_t slot =
+                hqc * p.rowslots + p.pslot0 + (ft.slen[cr] > 0 ? p.npfx : 0) + seg;
+            st.store_partial_hi(p.ws_acc + slot * D, size_t(p.rowslots) * D, p.ws_ml + 2 * slot,
+                                size_t(p.rowslots) * 2, lh);
+        }
+    }
+    const bool whole = nseg == 1 && npre == 0 && npair == 0;
     if (seg == 0 && lane == 0)
         p.meta[static_cast<size_t>(c.b) * p.Hkv + c.hk] =
-            whole ? 0u : static_cast<unsigned>(nseg) | (static_cast<unsigned>(npre) << 16);
+            whole ? 0u : static_cast<unsigned>(nseg) | (static_cast<unsigned>(npre + npair) << 16);
     if (whole) {
         st.store_out(static_cast<T *>(p.out) + hq0 * D, lh);
         return;
@@ -1112,14 +1184,27 @@ template <int D, int GQ>
 struct AttnOf<__nv_bfloat16, D, GQ, true> {
     using type = MmaAttn<D, GQ>;
 };
+// with forked children: the tile's spare columns carry a child's heads
+template <typename T, int D, int GQ, bool MMA, bool FORK>
+struct KernelAttn {
+    using type = typename AttnOf<T, D, GQ, MMA>::type;
+};
+template <int D, int GQ>
+struct KernelAttn<__nv_bfloat16, D, GQ, true, true> {
+    using type = MmaAttn<D, GQ, 2 * GQ>;
+};
 
 // MMA: the tensor-core tile (K/V by 2D tensor copies through kmap / vmap);
 // otherwise the CUDA-core tile (bulk copies; the maps are not read).
-template <typename T, int D, int GQ, bool MMA>
+// FORK (tensor-core tile, groups of at most 4 heads): a forked child's heads
+// ride in the spare columns of its parent's items over the blocks they share
+// (pa_decode_shared_forks); the child's own items start at its fork point.
+template <typename T, int D, int GQ, bool MMA, bool FORK = false>
 __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::MINB))
     decode_persistent_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                              const __grid_constant__ CUtensorMap vmap) {
-    using St = typename AttnOf<T, D, GQ, MMA>::type;
+    static_assert(!FORK || (MMA && 2 * GQ <= 8), "forks ride in the tensor-core tile's columns");
+    using St = typename KernelAttn<T, D, GQ, MMA, FORK>::type;
     using C = typename St::C;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     // swizzled tensor copies need 1024-byte aligned stages
@@ -1135,16 +1220,80 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
     int32_t *pre = reinterpret_cast<int32_t *>(smem + C::OFF_BT);  // [B+1] tile prefix
     int32_t *lens = pre + p.B + 1;                                  // [B]
     int32_t *starts = lens + p.B;                                   // [B]
+    int32_t *slen = starts + p.B;     // FORK: [B] validated shared_len
+    int32_t *child = slen + p.B;      // FORK: [B] child served by the row's items
+    int32_t *parent = child + p.B;    // FORK: [B] parent serving the row's fork range
     wait_prior_grids();  // inputs are ready past this point
+    // With the shared-prefix kernel behind this grid: that kernel launches
+    // once every CTA of this grid has passed this point, so its CTAs take the
+    // SMs this grid leaves as it drains (it reads none of this grid's results
+    // and waits for it before it exits).  The merge otherwise launches at
+    // this grid's end (launched early, its waiting CTAs slowed the 8B step).
+    if (p.early_dependents) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr bool kLanes = PA_DECODE_LOADER != 0 && !MMA;
 
     // ---- tiles per sequence and their prefix sums (whole CTA) ---------------
     const int cap = p.MB << p.bs_log2;
     int carry = 0;
+    if constexpr (FORK) {
+        // context lengths and shared lengths, validated as below
+        for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+            int L = p.context_lens[b];
+            if (L < 1 || L > cap) {
+                if (blockIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+                L = L < 1 ? 0 : cap;
+            }
+            int S = p.shared_len ? p.shared_len[b] : 0;
+            if (S < 0 || S >= L || (S & (p.bs - 1))) {
+                if (S != 0 && blockIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+                S = 0;
+            }
+            lens[b] = L;
+            slen[b] = S;
+            starts[b] = S;
+            child[b] = 0x7fffffff;
+            parent[b] = -1;
+        }
+        __syncthreads();
+        // A child takes its parent when both have the same shared length, its
+        // fork length is a multiple of the block size in [S, both lengths),
+        // and the parent is no child itself; of several children of one
+        // parent the lowest row (same choice in every CTA).  Others decode
+        // their fork range themselves.
+        auto fork_ok = [&](int c) {
+            const int par = p.fork_parent[c];
+            if (par < 0) return false;
+            const int F = p.fork_len[c];
+            const bool ok = par < p.B && par != c && p.fork_parent[par] < 0 && F > 0 &&
+                            !(F & (p.bs - 1)) && F >= slen[c] && F < lens[c] && F < lens[par] &&
+                            slen[par] == slen[c];
+            if (!ok && blockIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+            return ok;
+        };
+        for (int c = threadIdx.x; c < p.B; c += blockDim.x)
+            if (fork_ok(c)) atomicMin(&child[p.fork_parent[c]], c);
+        __syncthreads();
+        for (int c = threadIdx.x; c < p.B; c += blockDim.x) {
+            const int par = p.fork_parent[c];
+            if (par < 0) continue;
+            if (par < p.B && par != c && child[par] == c) {
+                parent[c] = par;
+                starts[c] = p.fork_len[c];
+            } else if (blockIdx.x == 0) {  // an invalid fork, or a parent's second child
+                pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
+            }
+        }
+        __syncthreads();
+        for (int b = threadIdx.x; b < p.B; b += blockDim.x)
+            if (child[b] == 0x7fffffff) child[b] = -1;
+        __syncthreads();
+    }
     for (int base = 0; base < p.B; base += blockDim.x) {
         const int b = base + threadIdx.x;
         int nt = 0;
-        if (b < p.B) {
+        if (FORK && b < p.B) {
+            nt = (lens[b] - starts[b] + C::TT - 1) / C::TT;
+        } else if (b < p.B) {
             int L = p.context_lens[b];
             if (L < 1 || L > cap) {
                 if (blockIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
@@ -1184,6 +1333,9 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
     }
     __syncthreads();
     const BatchTables bt{pre, lens, starts};
+    const ForkTables ft{slen, child, parent};
+    constexpr int QH = FORK ? 2 * GQ : GQ;
+    auto child_of = [&](const Cursor &c) { return FORK ? child[c.b] : -1; };
 
     // ---- this warp's range of units ------------------------------------------
     const int64_t U = int64_t(p.Hkv) * pre[p.B];
@@ -1210,8 +1362,9 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
     for (int i = 0; i < npro; ++i) {
         if constexpr (MMA) {
             if (lane == 0)
-                produce_tile_tma<D, GQ>(p, pc, checked_block(p, pend), ring + i * C::STAGE,
-                                        &bars[i], &kmap, &vmap, i == 0 || pc.t == 0);
+                produce_tile_tma<D, GQ, QH>(p, pc, checked_block(p, pend), ring + i * C::STAGE,
+                                            &bars[i], &kmap, &vmap, i == 0 || pc.t == 0,
+                                            child_of(pc));
         } else if (kLanes) {
             produce_tile_lanes<T, D, GQ>(p, pc, checked_block(p, pend), ring + i * C::STAGE,
                                          &bars[i], lane);
@@ -1234,19 +1387,27 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
         const uint32_t kaddr = pa::smem_u32(ring + s * C::STAGE);
         if (i == 0 || cc.t == 0) {
             st.reset();
-            if constexpr (MMA)  // q came with this tile
-                st.load_q_smem(kaddr + 2 * C::TILE, p.qscale);
+            if constexpr (MMA)  // q came with this tile (and the child's, if any)
+                st.load_q_smem(kaddr + 2 * C::TILE, p.qscale, child_of(cc) >= 0 ? QH : GQ);
             else
                 st.load_q(qbase + (static_cast<size_t>(cc.b) * p.Hq + cc.hk * GQ) * D, p.qscale);
         }
-        st.tile(kaddr, kaddr + C::TILE, min(C::TT, cc.L - first_token(cc, C::TT)), pbuf, sbuf);
+        const int tok0 = first_token(cc, C::TT);
+        if constexpr (FORK) {
+            // the child's heads see the tile's tokens below its fork point
+            const int cr = child[cc.b];
+            const int nhi = cr >= 0 ? max(0, min(C::TT, starts[cr] - tok0)) : 0;
+            st.tile(kaddr, kaddr + C::TILE, min(C::TT, cc.L - tok0), pbuf, sbuf, nhi);
+        } else {
+            st.tile(kaddr, kaddr + C::TILE, min(C::TT, cc.L - tok0), pbuf, sbuf);
+        }
         __syncwarp();
         if (i + C::NST < my_n) {
             if constexpr (MMA) {
                 if (lane == 0) {
                     pa::fence_proxy_async();
-                    produce_tile_tma<D, GQ>(p, pc, checked_block(p, pend), ring + s * C::STAGE,
-                                            &bars[s], &kmap, &vmap, pc.t == 0);
+                    produce_tile_tma<D, GQ, QH>(p, pc, checked_block(p, pend), ring + s * C::STAGE,
+                                                &bars[s], &kmap, &vmap, pc.t == 0, child_of(pc));
                 }
             } else if (kLanes) {
                 produce_tile_lanes<T, D, GQ>(p, pc, checked_block(p, pend), ring + s * C::STAGE,
@@ -1261,7 +1422,8 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
             if ((kLanes || lane == 0) && i + C::NST + 1 < my_n)
                 pend = block_entry<C::TT>(p, pc, 0);
         }
-        if (cc.t == cc.nt - 1 || i == my_n - 1) finish_segment<T, D, GQ>(st, p, bt, cc, per, w, lane);
+        if (cc.t == cc.nt - 1 || i == my_n - 1)
+            finish_segment<T, D, GQ, FORK>(st, p, bt, cc, per, w, lane, ft);
         cc = next_unit(cc, bt, p.B, p.Hkv);
     }
     if (failed_at >= 0) {
@@ -1657,12 +1819,13 @@ struct SharedPlan;
 int launch_prefix_any(const DecodeParams &p, const SharedPlan &sp, int D, bool after_decode,
                       cudaStream_t stream);
 
-template <typename T, int D, int GQ, bool MMA>
+template <typename T, int D, int GQ, bool MMA, bool FORK = false>
 int launch_persistent(const DecodeParams &p, cudaStream_t stream,
                       const SharedPlan *prefix_after = nullptr) {
-    using C = typename AttnOf<T, D, GQ, MMA>::type::C;
-    const size_t smem = C::OFF_BT + sizeof(int32_t) * (3 * p.B + 1) + (MMA ? 1024 : 0);
-    auto kern = decode_persistent_kernel<T, D, GQ, MMA>;
+    using C = typename KernelAttn<T, D, GQ, MMA, FORK>::type::C;
+    const size_t smem =
+        C::OFF_BT + sizeof(int32_t) * ((FORK ? 6 : 3) * p.B + 1) + (MMA ? 1024 : 0);
+    auto kern = decode_persistent_kernel<T, D, GQ, MMA, FORK>;
     CUtensorMap kmap{}, vmap{};
     if constexpr (MMA) {
         const int64_t rows = p.num_blocks * p.Hkv * p.bs;
@@ -1686,7 +1849,9 @@ int launch_persistent(const DecodeParams &p, cudaStream_t stream,
     const int sms = sm_count();
     if (sms <= 0) return pa::fail(PA_ERR_CUDA, "decode: no SM count");
     const int grid = sms * std::max(per_sm, 1);
-    e = launch_dependent(kern, dim3(grid), dim3(kWarps * 32), smem, stream, p, kmap, vmap);
+    DecodeParams pk = p;
+    pk.early_dependents = prefix_after ? 1 : 0;
+    e = launch_dependent(kern, dim3(grid), dim3(kWarps * 32), smem, stream, pk, kmap, vmap);
     if (e != cudaSuccess) return pa::cuda_fail(e, "decode launch");
     if (int rc = pa::check_launch("decode launch")) return rc;
     // shared-prefix partials on the tcgen05 kernel go behind the decode grid:
@@ -1830,9 +1995,18 @@ int launch(const DecodeParams &p, const SharedPlan *sp, cudaStream_t stream) {
             if (!sp->tc)
                 if (int rc = launch_prefix<D, GQ>(p, sp->pp, sp->max_group_size, stream)) return rc;
             if constexpr (GQ % 2 == 0 && GQ >= PA_DECODE_MMA_MIN_GQ)
-                if (use_mma<T, GQ>(p)) return launch_persistent<T, D, GQ, true>(p, stream, after);
+                if (use_mma<T, GQ>(p)) {
+                    if constexpr (2 * GQ <= 8)
+                        if (p.fork_parent)
+                            return launch_persistent<T, D, GQ, true, true>(p, stream, after);
+                    return launch_persistent<T, D, GQ, true>(p, stream, after);
+                }
             return launch_persistent<T, D, GQ, false>(p, stream, after);
         }
+        // forked children without shared-prefix groups (the host checked:
+        // persistent kernel, tensor-core tile, groups of at most 4 heads)
+        if constexpr (GQ % 2 == 0 && GQ >= PA_DECODE_MMA_MIN_GQ && 2 * GQ <= 8)
+            if (p.fork_parent) return launch_persistent<T, D, GQ, true, true>(p, stream);
     }
     const int sms = sm_count();
     if (sms <= 0) return pa::fail(PA_ERR_CUDA, "decode: no SM count");
@@ -1947,6 +2121,7 @@ namespace {
 struct SharedArgs {
     const int32_t *shared_len, *group_start, *group_seqs;
     int G, num_members, max_group_size, max_shared_len;
+    const int32_t *fork_parent = nullptr, *fork_len = nullptr;  // pa_decode_shared_forks
 };
 
 constexpr int kPfxChunkMin = 256;  // tokens: the prefix slots bound is max_shared_len / this
@@ -2000,6 +2175,40 @@ int validate_groups(const SharedArgs &sh, const int32_t *context_lens, const int
     return PA_OK;
 }
 
+// Validate mode: a child names a parent row (no child itself) with the same
+// shared_len, its fork length is a multiple of the block size in
+// [shared_len, both lengths), the two table rows agree on the blocks before
+// it, and no parent is named twice.
+int validate_forks(const SharedArgs &sh, const int32_t *context_lens, const int32_t *block_table,
+                   int B, int MB, int bs, cudaStream_t stream) {
+    std::vector<int32_t> lens(B), S(B, 0), fp(B), fl(B), table(size_t(B) * MB);
+    if (int rc = pa::fetch(lens.data(), context_lens, B * sizeof(int32_t), stream)) return rc;
+    if (sh.shared_len)
+        if (int rc = pa::fetch(S.data(), sh.shared_len, B * sizeof(int32_t), stream)) return rc;
+    if (int rc = pa::fetch(fp.data(), sh.fork_parent, B * sizeof(int32_t), stream)) return rc;
+    if (int rc = pa::fetch(fl.data(), sh.fork_len, B * sizeof(int32_t), stream)) return rc;
+    if (int rc = pa::fetch(table.data(), block_table, table.size() * sizeof(int32_t), stream))
+        return rc;
+    std::vector<char> named(B, 0);
+    for (int c = 0; c < B; ++c) {
+        const int par = fp[c];
+        if (par < 0) continue;
+        if (par >= B || par == c || fp[par] >= 0)
+            return pa::fail(PA_ERR_INVALID, "validate: fork_parent[%d]=%d", c, par);
+        if (named[par]++)
+            return pa::fail(PA_ERR_INVALID, "validate: row %d is the fork parent of two rows", par);
+        const int F = fl[c];
+        if (S[par] != S[c] || F <= 0 || F % bs || F < S[c] || F >= lens[c] || F >= lens[par])
+            return pa::fail(PA_ERR_INVALID, "validate: fork_len[%d]=%d", c, F);
+        for (int i = 0; i < F / bs; ++i)
+            if (table[size_t(c) * MB + i] != table[size_t(par) * MB + i])
+                return pa::fail(PA_ERR_INVALID,
+                                "validate: rows %d and %d differ in block %d before the fork", c,
+                                par, i);
+    }
+    return PA_OK;
+}
+
 int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
                 const int32_t *block_table, int max_blocks_per_seq, const int32_t *context_lens,
                 int B, int Hq, int Hkv, int head_dim, int block_size, int64_t num_blocks,
@@ -2034,8 +2243,10 @@ int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cac
     const int64_t cap = int64_t(max_blocks_per_seq) * block_size;
     const int max_parts = static_cast<int>((cap + pt - 1) / pt);
     const int npslot = sh ? prefix_slots_for(sh->max_shared_len) : 0;
+    // with fork arrays: a child's partials from its parent's item segments
+    const int nfslot = (sh && sh->fork_parent) ? max_parts + 1 : 0;
     WsLayout wl;
-    if (!workspace_layout(B, Hq, head_dim, int64_t(max_parts) + 1 + npslot, &wl))
+    if (!workspace_layout(B, Hq, head_dim, int64_t(max_parts) + 1 + npslot + nfslot, &wl))
         return pa::fail(PA_ERR_INVALID, "decode: workspace size does not fit in size_t");
     const size_t need = wl.total;
     if (need > workspace_bytes || !workspace)
@@ -2066,6 +2277,10 @@ int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cac
             if (int rc = validate_groups(*sh, context_lens, block_table, B, max_blocks_per_seq,
                                          block_size, stream))
                 return rc;
+        if (sh && sh->fork_parent)
+            if (int rc = validate_forks(*sh, context_lens, block_table, B, max_blocks_per_seq,
+                                        block_size, stream))
+                return rc;
     }
     DecodeParams p{};
     p.out = out;
@@ -2089,7 +2304,7 @@ int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cac
     p.PT = pt;
     p.max_parts = max_parts + 1;  // slot stride of the grid kernel
     p.maxseg = max_parts + 1;
-    p.rowslots = max_parts + 1 + npslot;  // slot stride of the persistent kernel
+    p.rowslots = max_parts + 1 + npslot + nfslot;  // slot stride of the persistent kernel
     p.shared_len = nullptr;
     p.pslot0 = max_parts + 1;
     p.npfx = 0;
@@ -2134,6 +2349,21 @@ int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cac
             p.shared_len = sh->shared_len;
             p.npfx = plan.pp.nc;
             sp = &plan;
+        }
+    }
+    // Forked children: bf16 groups of 4 heads on the persistent kernel's
+    // tensor-core tile (the child's heads take the tile's 4 spare columns);
+    // elsewhere every sequence reads its whole range itself.
+    if (sh && sh->fork_parent && dtype == PA_BF16 && gq * 2 <= 8 && gq >= PA_DECODE_MMA_MIN_GQ &&
+        tile_is_mma(gq, dtype, num_blocks, Hkv, block_size) && !contig_len) {
+        const int sms = sm_count();
+        if (sms <= 0) return pa::fail(PA_ERR_CUDA, "decode_shared: no SM count");
+        if (kernel_for(B, Hkv, max_blocks_per_seq, p.bs_log2, max_parts, sms) ==
+            PA_DECODE_PERSISTENT) {
+            p.fork_parent = sh->fork_parent;
+            p.fork_len = sh->fork_len;
+            // without the prefix plan p.shared_len stays NULL: every row starts
+            // at token 0 (or its fork point)
         }
     }
     if (dtype == PA_BF16)
@@ -2224,6 +2454,55 @@ int pa_decode_shared(void *out, const void *q, const void *k_cache, const void *
         return pa::fail(PA_ERR_INVALID, "decode_shared: max_shared_len beyond the table");
     const SharedArgs sh{shared_len, group_start, group_seqs, G,
                         num_members, max_group_size, max_shared_len};
+    return decode_impl(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, B,
+                       Hq, Hkv, head_dim, block_size, num_blocks, scale, partition_tokens, &sh,
+                       workspace, workspace_bytes, dtype, stream);
+}
+
+int pa_decode_shared_forks_workspace_size(int B, int Hq, int head_dim, int max_blocks_per_seq,
+                                          int block_size, int partition_tokens,
+                                          int max_shared_len, size_t *bytes) {
+    pa::clear_error();
+    if (!bytes) return pa::fail(PA_ERR_INVALID, "shared_forks_workspace_size: bytes is NULL");
+    if (B < 0 || Hq <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 || max_shared_len < 0 ||
+        !pa::pow2_in(block_size, 8, 128))
+        return pa::fail(PA_ERR_INVALID, "shared_forks_workspace_size: bad sizes");
+    const int pt = resolve_partition(partition_tokens);
+    if (!partition_ok(pt, block_size))
+        return pa::fail(PA_ERR_INVALID, "shared_forks_workspace_size: bad partition_tokens %d",
+                        pt);
+    const int64_t cap = int64_t(max_blocks_per_seq) * block_size;
+    const int64_t parts = (cap + pt - 1) / pt + 1;
+    const int64_t slots = 2 * parts + prefix_slots_for(max_shared_len);
+    WsLayout l;
+    if (!workspace_layout(B, Hq, head_dim, slots, &l))
+        return pa::fail(PA_ERR_INVALID, "shared_forks_workspace_size: size does not fit in size_t");
+    *bytes = l.total;
+    return PA_OK;
+}
+
+int pa_decode_shared_forks(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_table, int max_blocks_per_seq,
+                           const int32_t *context_lens, int B, int Hq, int Hkv, int head_dim,
+                           int block_size, int64_t num_blocks, float scale, int partition_tokens,
+                           const int32_t *shared_len, const int32_t *group_start,
+                           const int32_t *group_seqs, int G, int num_members, int max_group_size,
+                           int max_shared_len, const int32_t *fork_parent,
+                           const int32_t *fork_len, void *workspace, size_t workspace_bytes,
+                           int dtype, pa_stream_t stream) {
+    pa::clear_error();
+    if (G < 0 || num_members < 0 || max_group_size < 0 || max_shared_len < 0)
+        return pa::fail(PA_ERR_INVALID, "decode_shared_forks: bad group sizes");
+    if (G > 0 && (!shared_len || !group_start || (num_members > 0 && !group_seqs)))
+        return pa::fail(PA_ERR_INVALID, "decode_shared_forks: NULL group array");
+    if (B > 0 && (!fork_parent || !fork_len))
+        return pa::fail(PA_ERR_INVALID, "decode_shared_forks: NULL fork array");
+    if (max_shared_len > (int64_t(max_blocks_per_seq) * block_size))
+        return pa::fail(PA_ERR_INVALID, "decode_shared_forks: max_shared_len beyond the table");
+    SharedArgs sh{shared_len, group_start, group_seqs, G,
+                  num_members, max_group_size, max_shared_len};
+    sh.fork_parent = fork_parent;
+    sh.fork_len = fork_len;
     return decode_impl(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, B,
                        Hq, Hkv, head_dim, block_size, num_blocks, scale, partition_tokens, &sh,
                        workspace, workspace_bytes, dtype, stream);

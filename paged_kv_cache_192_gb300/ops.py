@@ -294,6 +294,54 @@ def decode_shared(q, k_cache, v_cache, block_table, context_lens, shared_len, gr
     return out
 
 
+def decode_shared_forks_workspace_size(B, Hq, head_dim, max_blocks_per_seq, block_size,
+                                       partition_tokens=0, max_shared_len=0):
+    out = ctypes.c_size_t(0)
+    check(lib().pa_decode_shared_forks_workspace_size(B, Hq, head_dim, max_blocks_per_seq,
+                                                      block_size, partition_tokens,
+                                                      max_shared_len, ctypes.byref(out)))
+    return out.value
+
+
+def decode_shared_forks(q, k_cache, v_cache, block_table, context_lens, shared_len,
+                        group_start, group_seqs, max_group_size, max_shared_len, fork_parent,
+                        fork_len, scale=None, partition_tokens=0, workspace=None, out=None,
+                        stream=None):
+    """pa_decode_shared_forks: decode_shared for a batch that also holds forked
+    children.  fork_parent int32 [B] (a child's parent row, else -1) and
+    fork_len int32 [B] (tokens whose blocks a child shares with its parent):
+    the blocks a child shares with its parent are read once for both."""
+    _check_decode_shapes(q, k_cache, v_cache, block_table, context_lens, out)
+    B, Hq, d = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    MB = block_table.shape[1]
+    _require(shared_len.shape == (B,), f"shared_len must be [{B}]")
+    _require(fork_parent.shape == (B,) and fork_len.shape == (B,),
+             f"fork_parent and fork_len must be [{B}]")
+    _require(group_start.dim() == 1 and group_start.numel() >= 1, "group_start must be [G+1]")
+    G = group_start.numel() - 1
+    M = group_seqs.numel()
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    ws_bytes = decode_shared_forks_workspace_size(B, Hq, d, MB, bs, partition_tokens,
+                                                  max_shared_len)
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes // 4, dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(lib().pa_decode_shared_forks(
+        _cuda(out, "out", q.dtype), _cuda(q, "q", k_cache.dtype), _cuda(k_cache, "k_cache"),
+        _cuda(v_cache, "v_cache", k_cache.dtype), _cuda(block_table, "block_table", torch.int32),
+        MB, _cuda(context_lens, "context_lens", torch.int32), B, Hq, Hkv, d, bs, NB, scale,
+        partition_tokens, _cuda(shared_len, "shared_len", torch.int32),
+        _cuda(group_start, "group_start", torch.int32),
+        _cuda(group_seqs, "group_seqs", torch.int32) if M else None, G, M, int(max_group_size),
+        int(max_shared_len), _cuda(fork_parent, "fork_parent", torch.int32),
+        _cuda(fork_len, "fork_len", torch.int32), ws_ptr, ws_len, _dt(q), _stream(stream)))
+    return out
+
+
 def decode_noalloc_capacity() -> int:
     """Bytes of the library's fixed decode scratch (pa_decode_noalloc)."""
     return int(lib().pa_decode_noalloc_capacity())

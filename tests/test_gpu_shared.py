@@ -187,3 +187,190 @@ def test_shared_groups_large_blocks_warp_level_prefix(Hq, Hkv):
                                      Hq=Hq, Hkv=Hkv, bs=128)
     out, _ = run_shared(w, partition_tokens=128)
     compare(out.double().cpu().numpy(), oracle_decode_all(w), torch.bfloat16, f"bs128 {Hq}/{Hkv}")
+
+
+# ---------------------------------------------------------------------------
+# Forked children (pa_decode_shared_forks): the blocks a child shares with its
+# parent are read once for both ("Apa itu PagedAttention?", section "Cara kerja
+# PagedAttention", item 3).
+# ---------------------------------------------------------------------------
+
+def _fork(w, pairs_f):
+    """Make each (child, parent, F) of pairs_f a fork: the child's first F
+    tokens (logical K/V and table blocks) become the parent's."""
+    offs = w.kv_offsets
+    for c, par, F in pairs_f:
+        assert F % w.bs == 0 and F < w.lens[c] and F < w.lens[par]
+        w.k[offs[c]:offs[c] + F] = w.k[offs[par]:offs[par] + F]
+        w.v[offs[c]:offs[c] + F] = w.v[offs[par]:offs[par] + F]
+        w.table[c, :F // w.bs] = w.table[par, :F // w.bs]
+    fp = np.full(w.B, -1, dtype=np.int32)
+    fl = np.zeros(w.B, dtype=np.int32)
+    for c, par, F in pairs_f:
+        fp[c], fl[c] = par, F
+    return torch.from_numpy(fp).to(DEV), torch.from_numpy(fl).to(DEV)
+
+
+def run_forks(w, fp, fl, groups=None, partition_tokens=0, expect_error=0):
+    k_cache, v_cache, table, lens = device_inputs(w, DEV)
+    if groups is None:
+        sl = torch.zeros(w.B, dtype=torch.int32, device=DEV)
+        gs = torch.zeros(1, dtype=torch.int32, device=DEV)
+        gm = torch.zeros(0, dtype=torch.int32, device=DEV)
+        mg, ms = 0, 0
+    else:
+        sl, gs, gm, mg, ms = groups
+    ops().device_error(clear=True)
+    out = ops().decode_shared_forks(w.q.to(DEV), k_cache, v_cache, table, lens, sl, gs, gm, mg,
+                                    ms, fp, fl, partition_tokens=partition_tokens)
+    torch.cuda.synchronize()
+    assert ops().device_error(clear=True) == expect_error
+    return out
+
+
+def test_forks_without_groups_match_oracle():
+    """64 sequences of the 8B shape, 20 of them forks of others at fork points
+    from one block to nearly their whole length; no shared-prefix groups."""
+    rng = np.random.default_rng(3)
+    lens = [int(x) for x in rng.integers(200, 3000, size=64)]
+    parents = list(range(0, 40, 2))[:20]
+    children = list(range(40, 60))
+    pairs = []
+    for c, par in zip(children, parents):
+        m = min(lens[c], lens[par]) - 1
+        F = int(rng.integers(1, m // 16 + 1)) * 16
+        pairs.append((c, par, F))
+    w = synth.decode_workload("8b", seed=3, lens=lens)
+    fp, fl = _fork(w, pairs)
+    assert ops().decode_kernel_for(w.B, w.Hkv, w.table.shape[1], w.bs, 0) == "persistent"
+    out = run_forks(w, fp, fl)
+    compare(out.double().cpu().numpy(), oracle_decode_all(w), torch.bfloat16, "forks, no groups")
+
+
+def test_forks_inside_groups_match_oracle():
+    """Two prompt groups; inside each, members fork other members past the
+    prompt; ungrouped sequences fork each other too."""
+    w = synth.shared_groups_workload([(512, 12), (256, 10)], singles=40, seed=21,
+                                     suffix_range=(40, 900))
+    e = w.extra
+    gs, gm, S = e["group_start"], e["group_seqs"], e["shared_len"]
+    rng = np.random.default_rng(22)
+    pairs = []
+    for g in range(len(gs) - 1):
+        mem = [int(x) for x in gm[gs[g]:gs[g + 1]]]
+        for par, c in zip(mem[0::2], mem[1::2]):
+            lo, hi = S[c] // w.bs, (min(w.lens[c], w.lens[par]) - 1) // w.bs
+            pairs.append((c, par, int(rng.integers(lo, hi + 1)) * w.bs))
+    singles = [b for b in range(w.B) if S[b] == 0]
+    for par, c in zip(singles[0:20:2], singles[1:20:2]):
+        hi = (min(w.lens[c], w.lens[par]) - 1) // w.bs
+        pairs.append((c, par, int(rng.integers(1, hi + 1)) * w.bs))
+    fp, fl = _fork(w, pairs)
+    out = run_forks(w, fp, fl, groups=_groups(w), partition_tokens=64)
+    compare(out.double().cpu().numpy(), oracle_decode_all(w), torch.bfloat16, "forks in groups")
+
+
+def test_fork_parent_split_into_many_segments():
+    """A long parent (6,000 tokens) split over many warps and 64-token
+    partitions, its child forked near the end: the child gets one partial per
+    segment of its parent's item (more than the merge loads speculatively)."""
+    rng = np.random.default_rng(5)
+    lens = [6000, 6010] + [int(x) for x in rng.integers(100, 1500, size=60)]
+    w = synth.decode_workload("8b", seed=5, lens=lens)
+    fp, fl = _fork(w, [(1, 0, 5984)])
+    out = run_forks(w, fp, fl, partition_tokens=64)
+    compare(out.double().cpu().numpy(), oracle_decode_all(w), torch.bfloat16, "long fork")
+
+
+def test_two_children_of_one_parent():
+    """Rows 10 and 11 both name row 3: the lower row rides with the parent, the
+    other reads its fork range itself and is reported in the device error
+    word; both match the oracle."""
+    from paged_kv_cache_192_gb300._lib import PA_DEVERR_BAD_BLOCK
+    rng = np.random.default_rng(7)
+    lens = [int(x) for x in rng.integers(300, 2000, size=64)]
+    lens[3], lens[10], lens[11] = 1500, 1600, 1550
+    w = synth.decode_workload("8b", seed=7, lens=lens)
+    fp, fl = _fork(w, [(10, 3, 800), (11, 3, 1200)])
+    out = run_forks(w, fp, fl, expect_error=PA_DEVERR_BAD_BLOCK)
+    compare(out.double().cpu().numpy(), oracle_decode_all(w), torch.bfloat16, "two children")
+
+
+@pytest.mark.parametrize("bad", ["len", "beyond", "chain"])
+def test_invalid_fork_is_recorded_and_read_whole(bad):
+    """A fork length that is no multiple of the block size, one at the
+    child's length, or a parent that is itself a child: the child reads its
+    whole range, the error is recorded, every output still matches."""
+    from paged_kv_cache_192_gb300._lib import PA_DEVERR_BAD_BLOCK
+    rng = np.random.default_rng(9)
+    lens = [int(x) for x in rng.integers(300, 2000, size=64)]
+    lens[5], lens[6], lens[7] = 1000, 1000, 1000
+    w = synth.decode_workload("8b", seed=9, lens=lens)
+    fp, fl = _fork(w, [(6, 5, 480), (7, 6, 320)] if bad == "chain" else [(6, 5, 480)])
+    if bad == "len":
+        fl[6] = 479
+    elif bad == "beyond":
+        fl[6] = 1008
+    out = run_forks(w, fp, fl, expect_error=PA_DEVERR_BAD_BLOCK)
+    compare(out.double().cpu().numpy(), oracle_decode_all(w), torch.bfloat16, f"bad fork {bad}")
+
+
+def test_fork_validate_mode_rejects_bad_forks():
+    from paged_kv_cache_192_gb300._lib import PAError
+    rng = np.random.default_rng(11)
+    lens = [int(x) for x in rng.integers(300, 2000, size=48)]
+    w = synth.decode_workload("8b", seed=11, lens=lens)
+    fp, fl = _fork(w, [(6, 5, 160)])
+    k_cache, v_cache, table, lens_d = device_inputs(w, DEV)
+    sl = torch.zeros(w.B, dtype=torch.int32, device=DEV)
+    gs = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gm = torch.zeros(0, dtype=torch.int32, device=DEV)
+    table[6, 2] = table[6, 2] + 1  # the rows now differ before the fork
+    ops().set_validate(True)
+    try:
+        with pytest.raises(PAError):
+            ops().decode_shared_forks(w.q.to(DEV), k_cache, v_cache, table, lens_d, sl, gs, gm,
+                                      0, 0, fp, fl)
+    finally:
+        ops().set_validate(False)
+
+
+def test_prefix_fork_step_with_forks_full_size():
+    """The shared-prefix config's fork step (256 users sharing a 1024-token
+    prompt, 64 forks, copy-on-write, 320 new tokens) decoded with the prompt
+    group and the 64 forks: each child's blocks before its parent's last,
+    partly filled one are read once for both; every output against the
+    oracle."""
+    from paged_kv_cache_192_gb300 import layout
+    pf = synth.prefix_fork_workload(seed=0)
+    w = pf.base
+    st = layout.place_prefix_forks(pf, bm_seed=5)
+    NB, P, bs = st["num_blocks"], w.extra["prefix"], w.bs
+    k_cache, v_cache = layout.alloc_pools(NB, w.Hkv, w.bs, w.d, w.dtype, DEV)
+    ops().reshape_and_cache(w.k[:P].to(DEV), w.v[:P].to(DEV), k_cache, v_cache,
+                            torch.from_numpy(st["prompt_slots"]).to(DEV))
+    rows = torch.from_numpy(st["hist_rows"])
+    ops().reshape_and_cache(w.k[rows].to(DEV), w.v[rows].to(DEV), k_cache, v_cache,
+                            torch.from_numpy(st["hist_slots"]).to(DEV))
+    ops().copy_blocks(k_cache, v_cache, torch.tensor(st["pairs"], dtype=torch.int64, device=DEV))
+    ops().reshape_and_cache(st["k_new"].to(DEV), st["v_new"].to(DEV), k_cache, v_cache,
+                            torch.from_numpy(st["new_slots"]).to(DEV))
+    lw = pf.logical()
+    Bt = lw.B
+    fp = np.full(Bt, -1, dtype=np.int32)
+    fl = np.zeros(Bt, dtype=np.int32)
+    for i, par in enumerate(pf.parents):
+        c = w.B + i
+        fp[c], fl[c] = par, (int(w.lens[par]) - 1) // bs * bs
+        assert np.array_equal(st["table"][c, :fl[c] // bs], st["table"][par, :fl[c] // bs])
+    table = torch.from_numpy(st["table"]).to(DEV)
+    lens = torch.from_numpy(st["lens"].astype(np.int32)).to(DEV)
+    sl = torch.full((Bt,), P, dtype=torch.int32, device=DEV)
+    gs = torch.tensor([0, Bt], dtype=torch.int32, device=DEV)
+    gm = torch.arange(Bt, dtype=torch.int32, device=DEV)
+    ops().device_error(clear=True)
+    out = ops().decode_shared_forks(lw.q.to(DEV), k_cache, v_cache, table, lens, sl, gs, gm, Bt, P,
+                                    torch.from_numpy(fp).to(DEV), torch.from_numpy(fl).to(DEV))
+    torch.cuda.synchronize()
+    assert ops().device_error(clear=True) == 0
+    compare(out.double().cpu().numpy(), oracle_decode_all(lw), torch.bfloat16, "fork step, forks")

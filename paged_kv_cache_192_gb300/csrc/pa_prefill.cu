@@ -630,6 +630,9 @@ __global__ void __launch_bounds__(Tc2Layout<D, NQ>::THREADS, 3 - NQ)
     // one, and the wait moves to every exit instead.
     const bool wait_end = PFX && p.pfx_wait_end;
     if (!wait_end) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // behind the decode grid the merge comes next: it may launch now (its
+    // CTAs wait for this grid, which itself waits for the decode at exit)
+    if (wait_end) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     auto exit_wait = [&]() {
         if (wait_end) asm volatile("griddepcontrol.wait;" ::: "memory");
     };

@@ -17,13 +17,20 @@
 // while a spare warp computes the rest.  No global counter and no workspace,
 // so launches on different streams never interfere.
 //
-// Warps: 0-3 and 4-7 softmax of the item's two 128-row query tiles, 8 issues
-// every tcgen05.mma (one lane), 9 loads K/V tiles with TMA through a 4-stage
-// ring, 10 schedules and then loads each item's query tiles (3D tensor
+// Warps: 0-3 and 4-7 softmax of the item's two 128-row query tiles A and B;
+// 8 and 11 issue the tcgen05.mma of tile A and of tile B (one lane each, so
+// one tile's products never wait behind the other tile's P); 9 loads K/V
+// tiles with TMA through a 4-stage ring (a stage is free once both tiles' PV
+// are done); 10 schedules and then loads each item's query tiles (3D tensor
 // copies: one 16 KB box per full tile and 64 columns).
-// TMEM (512 columns): O_A [0,128), O_B [128,256), S_A[0..1] [256,384),
-// S_B[0..1] [384,512).  Every barrier phase follows a CTA-wide tile or item
-// counter, so the pipelines run across item boundaries; every wait is bounded.
+// TMEM (512 columns): O_A [0,128), O_B [128,256), then per query tile 64
+// columns of S and 64 of P (hi, lo): S_A [256,320), P_A [320,384), S_B
+// [384,448), P_B [448,512).  A softmax group frees S as soon as it has
+// loaded it, so S of the next tile is computed while it works on this one;
+// P of the next tile overwrites P only after this tile's PV is done (the
+// group waits for that PV before it may rescale O anyway).  Every barrier
+// phase follows a CTA-wide tile or item counter, so the pipelines run across
+// item boundaries; every wait is bounded.
 #include <cuda.h>
 
 #include <algorithm>
@@ -51,14 +58,14 @@ constexpr int kPCtasMax = 255;    // the CTA index sits in the low 8 bits of a l
 template <int D>
 struct PLayout {
     static constexpr int NST = PA_PERSIST_NST;
-    static constexpr int THREADS = 11 * 32;
-    static constexpr int MMA_WARP = 8, LOAD_WARP = 9, Q_WARP = 10;
+    static constexpr int THREADS = 12 * 32;
+    static constexpr int MMA_WARP = 8, LOAD_WARP = 9, Q_WARP = 10, MMA_WARP_B = 11;
     static constexpr int TMEM_COLS = 512;
     static constexpr int Q_BYTES = 2 * 128 * D * 2;  // two query tiles
     static constexpr int T_BYTES = kT2KT * D * 2;    // one K or V tile
     static constexpr int OFF_KV = Q_BYTES;           // [stage][K|V]
     static constexpr int OFF_BAR = OFF_KV + NST * 2 * T_BYTES;
-    // kv_full, kv_empty [NST]; s_full [4]; p_full, o_done, o_free [2];
+    // kv_full, kv_empty [NST]; s_full, s_free [2]; p_full, o_done, o_free [2];
     // q_full, q_empty, sched, drain
     static constexpr int N_BAR = 2 * NST + 4 + 6 + 4;
     static constexpr int OFF_MISC = OFF_BAR + 8 * N_BAR;  // TMEM slot, fail flag, list length
@@ -111,8 +118,8 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
     const uint32_t skv = sq + Lay::OFF_KV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::OFF_BAR);
     uint64_t *kv_full = bars, *kv_empty = bars + NST;
-    uint64_t *s_full = bars + 2 * NST;  // [2 * group + buffer]
-    uint64_t *p_full = s_full + 4, *o_done = p_full + 2, *o_free = o_done + 2;  // o_done[1] unused
+    uint64_t *s_full = bars + 2 * NST, *s_free = s_full + 2;  // [group]
+    uint64_t *p_full = s_full + 4, *o_done = p_full + 2, *o_free = o_done + 2;
     uint64_t *q_full = o_free + 2, *q_empty = q_full + 1, *sched = q_empty + 1, *drain = sched + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + Lay::OFF_MISC);
     volatile int *fail = reinterpret_cast<volatile int *>(smem + Lay::OFF_MISC + 4);
@@ -135,18 +142,19 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
     if (tid == 0) {
         for (int i = 0; i < NST; ++i) {
             pa::mbar_init(&kv_full[i], 1);
-            pa::mbar_init(&kv_empty[i], 1);
+            pa::mbar_init(&kv_empty[i], 2);  // both query tiles' PV
         }
-        for (int i = 0; i < 4; ++i) pa::mbar_init(&s_full[i], 1);
         for (int i = 0; i < 2; ++i) {
+            pa::mbar_init(&s_full[i], 1);
+            pa::mbar_init(&s_free[i], 4);  // one arrival per softmax warp
             pa::mbar_init(&p_full[i], 4);  // one arrival per softmax warp
             pa::mbar_init(&o_done[i], 1);
             pa::mbar_init(&o_free[i], 4);
         }
         pa::mbar_init(q_full, 1);
-        pa::mbar_init(q_empty, 1);
+        pa::mbar_init(q_empty, 2);  // both query tiles' last S
         pa::mbar_init(sched, 1);
-        pa::mbar_init(drain, 1);
+        pa::mbar_init(drain, 2);  // both MMA warps
         *fail = 0;
         *nmine = 1;
         mine[0] = static_cast<uint16_t>(blockIdx.x);
@@ -395,36 +403,42 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
             g = __shfl_sync(pa::kFull, g, 0);
             __syncwarp();
         }
-    } else if (warp == Lay::MMA_WARP) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp == Lay::MMA_WARP || warp == Lay::MMA_WARP_B) {
+        // ---------------- MMA issuers, one per query tile ----------------
+        const int wg = warp == Lay::MMA_WARP ? 0 : 1;
         constexpr uint32_t kIdS = pa::tc::idesc_bf16(128, kT2KT, 0, 0);
         constexpr uint32_t kIdO = pa::tc::idesc_bf16(128, D, 0, 1);
         constexpr uint32_t kStage = (2 * Lay::T_BYTES) >> 4;
-        const uint64_t dq = pa::tc::sdesc(sq, 16, 1024);
+        const uint64_t dq = pa::tc::sdesc(sq, 16, 1024) +
+                            static_cast<uint32_t>(wg * ((128 * D * 2) >> 4));
         const uint64_t dk = pa::tc::sdesc(skv, 16, 1024);
         const uint64_t dv = pa::tc::sdesc(skv + Lay::T_BYTES, kT2KT * 128, 1024);
-        // S of CTA tile g for group wg: TMEM columns 256 + 128 wg + 64 (g % 2)
-        auto issue_s = [&](int wg, int g) {
-            const uint64_t a0 = dq + static_cast<uint32_t>(wg * ((128 * D * 2) >> 4));
+        const uint32_t sc = tmem + 256 + wg * 128, ph = sc + 64, pl = ph + 32;
+        const uint32_t od = tmem + wg * 128;
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+            return __all_sync(pa::kFull, pa::mbar_wait(bar, parity));
+        };
+        // S of CTA tile g: TMEM columns 256 + 128 wg, once the group has
+        // loaded S of tile g - 1 from them
+        auto issue_s = [&](int g) {
+            if (g > 0 && !wait_all(&s_free[wg], (g - 1) & 1)) return false;
+            pa::tc::fence_after();
             const uint64_t b0 = dk + static_cast<uint32_t>((g % NST) * kStage);
-            const uint32_t sc = tmem + 256 + wg * 128 + (g & 1) * 64;
             if (pa::tc::elect_one()) {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    pa::tc::mma_ss(sc, a0 + (((ks >> 2) * 128 * 128 + (ks & 3) * 32) >> 4),
+                    pa::tc::mma_ss(sc, dq + (((ks >> 2) * 128 * 128 + (ks & 3) * 32) >> 4),
                                    b0 + (((ks >> 2) * kT2KT * 128 + (ks & 3) * 32) >> 4), kIdS,
                                    ks > 0);
-                pa::tc::commit(&s_full[2 * wg + (g & 1)]);
+                pa::tc::commit(&s_full[wg]);
             }
             __syncwarp();
+            return true;
         };
-        // O_wg (+)= P_hi V + P_lo V; P of tile g sits in the S buffer it came
-        // from.  Group 1's PV is the tile's last MMA, so its commit also
-        // releases the K/V stage: kv_empty doubles as group 1's PV barrier.
-        auto issue_pv = [&](int wg, int g, int acc0) {
+        // O (+)= P_hi V + P_lo V; P sits in the 64 columns after the group's
+        // S.  The K/V stage is free once both query tiles' PV are done.
+        auto issue_pv = [&](int g, int acc0) {
             const uint64_t b0 = dv + static_cast<uint32_t>((g % NST) * kStage);
-            const uint32_t ph = tmem + 256 + wg * 128 + (g & 1) * 64, pl = ph + 32;
-            const uint32_t od = tmem + wg * 128;
             if (pa::tc::elect_one()) {
 #pragma unroll
                 for (int ks = 0; ks < kT2KT / 16; ++ks) {
@@ -432,18 +446,15 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
                     pa::tc::mma_ts(od, ph + ks * 8, b, kIdO, ks == 0 ? acc0 : 1);
                     pa::tc::mma_ts(od, pl + ks * 8, b, kIdO, 1);
                 }
-                pa::tc::commit(wg == 0 ? &o_done[0] : &kv_empty[g % NST]);
+                pa::tc::commit(&o_done[wg]);
+                pa::tc::commit(&kv_empty[g % NST]);
             }
             __syncwarp();
         };
-        auto wait_all = [&](uint64_t *bar, uint32_t parity) {
-            return __all_sync(pa::kFull, pa::mbar_wait(bar, parity));
-        };
-        // Per item: S(0) of both groups once its query tiles are in; then per
-        // tile: S(g+1) of both groups, PV(g) of group 0, PV(g) of group 1
-        // (whose commit releases the K/V stage).  After the item's last S the query tiles
-        // are released; its first PV per group waits until that group has
-        // read the previous item's O out of TMEM.
+        // Per item: S(0) once its query tiles are in; then per tile S(g+1)
+        // and PV(g).  After the item's last S this query tile is released;
+        // the item's first PV waits until the group has read the previous
+        // item's O out of TMEM.
         bool ok = true;
         int g = 0, k;
         for (int it = 0; ok && next_item(it, &k); ++it) {
@@ -451,26 +462,23 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
             ok = wait_all(q_full, it & 1) && wait_all(&kv_full[g % NST], (g / NST) & 1);
             if (!ok) break;
             pa::tc::fence_after();
-            issue_s(0, g);
-            issue_s(1, g);
+            ok = issue_s(g);
             for (int j = 0; j < nt && ok; ++j, ++g) {
                 if (j + 1 < nt) {
                     ok = wait_all(&kv_full[(g + 1) % NST], ((g + 1) / NST) & 1);
                     if (!ok) break;
                     pa::tc::fence_after();
-                    issue_s(0, g + 1);
-                    issue_s(1, g + 1);
+                    ok = issue_s(g + 1);
+                    if (!ok) break;
                 } else {
                     if (pa::tc::elect_one()) pa::tc::commit(q_empty);
                     __syncwarp();
                 }
-                for (int wg = 0; wg < 2 && ok; ++wg) {
-                    if (j == 0 && it > 0) ok = wait_all(&o_free[wg], (it - 1) & 1);
-                    if (ok) ok = wait_all(&p_full[wg], g & 1);
-                    if (!ok) break;
-                    pa::tc::fence_after();
-                    issue_pv(wg, g, j > 0);
-                }
+                if (j == 0 && it > 0) ok = wait_all(&o_free[wg], (it - 1) & 1);
+                if (ok) ok = wait_all(&p_full[wg], g & 1);
+                if (!ok) break;
+                pa::tc::fence_after();
+                issue_pv(g, j > 0);
             }
         }
         if (!ok) *fail = 1;
@@ -482,16 +490,9 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
         const uint32_t o_col = wg * 128;
         const int m = wg * 128 + row;
         const float qs2 = p.qscale;  // softmax scale in log2 units
-        // PV of CTA tile gg of this group done: group 0 on o_done[0] (one
-        // phase per tile), group 1 on the K/V stage's release (one phase per
-        // NST tiles).  Either barrier is at most one phase from the one waited
-        // for: the phase before it belongs to a PV that ran before the S tile
-        // this warp read last, and the phase after it needs this group's P of
-        // a later tile.
-        auto pv_done = [&](int gg) {
-            return wg == 0 ? pa::mbar_wait(&o_done[0], gg & 1)
-                           : pa::mbar_wait(&kv_empty[gg % NST], (gg / NST) & 1);
-        };
+        // PV of CTA tile gg of this group done (one phase per tile; the next
+        // phase needs this group's P of a later tile)
+        auto pv_done = [&](int gg) { return pa::mbar_wait(&o_done[wg], gg & 1); };
         bool ok = true;
         int g = 0, k;
         for (int it = 0; ok && next_item(it, &k); ++it) {
@@ -499,14 +500,18 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
             const int pos = I.P + min(I.t0 + m / GQ, I.n - 1);  // last key this row sees
             float m_used = -INFINITY, lsum = 0.f;
             for (int j = 0; j < I.ntiles; ++j, ++g) {
-                const uint32_t s_col = 256 + wg * 128 + (g & 1) * 64;
-                ok = pa::mbar_wait(&s_full[2 * wg + (g & 1)], (g >> 1) & 1);
+                const uint32_t s_col = 256 + wg * 128, p_col = s_col + 64;
+                ok = pa::mbar_wait(&s_full[wg], g & 1);
                 if (!ok) break;
                 pa::tc::fence_after();
                 uint32_t sr[2][32];
                 pa::tc::ld32(lane_base + s_col, sr[0]);
                 pa::tc::ld32(lane_base + s_col + 32, sr[1]);
                 pa::tc::wait_ld();
+                // S may now be overwritten by the next tile's
+                pa::tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_free[wg]);
                 const int j0 = j * kT2KT;
                 float s[64];
 #pragma unroll
@@ -566,10 +571,11 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
                         }
                     }
                 }
-                if (j == I.ntiles - 1 && wg == 0) {
+                if (j == I.ntiles - 1) {
                     // rows past the context in the last tile may hold anything
                     // (unwritten slots); P is 0 there but 0 * NaN is NaN: zero
-                    // them.  Group 1's PV of this tile follows group 0's arrival.
+                    // them.  Each group does so before its own P arrival (its
+                    // PV may run before the other group's); both write zeros.
                     const int first = I.kv_end - j0;
                     const uint32_t vst = skv + (g % NST) * 2 * Lay::T_BYTES + Lay::T_BYTES;
                     for (int idx = row; idx < (kT2KT - first) * CH; idx += 128) {
@@ -581,8 +587,8 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
-                pa::tc::st32(lane_base + s_col, ph);
-                pa::tc::st32(lane_base + s_col + 32, pl);
+                pa::tc::st32(lane_base + p_col, ph);
+                pa::tc::st32(lane_base + p_col + 32, pl);
                 pa::tc::wait_st();
                 pa::tc::fence_before();
                 __syncwarp();
@@ -630,7 +636,7 @@ __global__ void __launch_bounds__(PLayout<D>::THREADS, 1)
         // a wait ran out: record it, then let the MMAs and the K/V copies in
         // flight land (bounded) before TMEM and shared memory go away
         if (tid == 0) pa::record_error(p.err, PA_DEVERR_TIMEOUT);
-        if (warp == Lay::MMA_WARP) {
+        if (warp == Lay::MMA_WARP || warp == Lay::MMA_WARP_B) {
             if (pa::tc::elect_one()) pa::tc::commit(drain);
             __syncwarp();
             (void)pa::mbar_wait(drain, 0);

@@ -374,3 +374,46 @@ def test_prefix_fork_step_with_forks_full_size():
     torch.cuda.synchronize()
     assert ops().device_error(clear=True) == 0
     compare(out.double().cpu().numpy(), oracle_decode_all(lw), torch.bfloat16, "fork step, forks")
+
+
+@pytest.mark.parametrize("forks", [False, True])
+def test_back_to_back_calls_are_identical(forks):
+    """24 calls issued back to back on one stream with one workspace and no
+    synchronisation between them: each call's decode grid releases the
+    shared-prefix kernel at its start and that kernel releases the merge, so
+    consecutive calls overlap their launches; every output must equal the
+    first bit for bit, and the first must match the oracle."""
+    w = synth.shared_groups_workload([(512, 12), (256, 10)], singles=40, seed=31,
+                                     suffix_range=(40, 900))
+    fp = fl = None
+    if forks:
+        S = w.extra["shared_len"]
+        singles = [b for b in range(w.B) if S[b] == 0]
+        pairs = []
+        for par, c in zip(singles[0:16:2], singles[1:16:2]):
+            hi = (min(w.lens[c], w.lens[par]) - 1) // w.bs
+            if hi > 0:  # a fork shares at least one whole block
+                pairs.append((c, par, hi * w.bs))
+        assert len(pairs) >= 6
+        fp, fl = _fork(w, pairs)
+    k_cache, v_cache, table, lens = device_inputs(w, DEV)
+    sl, gs, gm, mg, ms = _groups(w)
+    q = w.q.to(DEV)
+    MB = table.shape[1]
+    wsf = ops().decode_shared_forks_workspace_size if forks else ops().decode_shared_workspace_size
+    ws = torch.empty(wsf(w.B, w.Hq, w.d, MB, w.bs, 64, ms) // 4, dtype=torch.float32, device=DEV)
+    outs = [torch.empty_like(q) for _ in range(24)]
+    ops().device_error(clear=True)
+    for out in outs:
+        if forks:
+            ops().decode_shared_forks(q, k_cache, v_cache, table, lens, sl, gs, gm, mg, ms, fp, fl,
+                                      partition_tokens=64, workspace=ws, out=out)
+        else:
+            ops().decode_shared(q, k_cache, v_cache, table, lens, sl, gs, gm, mg, ms,
+                                partition_tokens=64, workspace=ws, out=out)
+    torch.cuda.synchronize()
+    assert ops().device_error(clear=True) == 0
+    for i, out in enumerate(outs[1:], 1):
+        assert torch.equal(out, outs[0]), f"call {i} differs from call 0"
+    compare(outs[0].double().cpu().numpy(), oracle_decode_all(w), torch.bfloat16,
+            "back to back" + (" with forks" if forks else ""))

@@ -242,3 +242,31 @@ def test_mixed_config_full_size():
     ref = oracle.prefill_chunk(pre.q.double().numpy(), pre.k.double().numpy(),
                                pre.v.double().numpy(), [n] * R, priors, 1.0 / np.sqrt(pre.d))
     compare(out_p.double().cpu().numpy(), ref, torch.bfloat16, "mixed prefill (all rows)")
+
+
+def test_prefill_back_to_back_calls_are_identical():
+    """16 persistent-grid prefill calls issued back to back on one stream
+    (each a programmatic dependent of the one before, so its set-up overlaps
+    the previous call's tail) with work lists of several items per CTA: every
+    output equals the first bit for bit, and the first matches the oracle."""
+    rng = np.random.default_rng(77)
+    R = 16  # 64 (request, query tile) pairs, at most 512 items
+    n_new = [int(x) for x in rng.integers(1, 257, size=R)]
+    n_new[0] = 256
+    priors = [int(x) for x in rng.integers(0, 900, size=R)]
+    w, q = _prefill_workload(priors, n_new, seed=77)
+    assert _kernel(w, n_new) == "persistent"
+    k_cache, v_cache, table, lens = device_inputs(w, DEV)
+    qs = torch.tensor(np.concatenate([[0], np.cumsum(n_new)]), dtype=torch.int32, device=DEV)
+    qd = q.to(DEV)
+    outs = [torch.empty_like(qd) for _ in range(16)]
+    ops().device_error(clear=True)
+    for out in outs:
+        ops().prefill_chunk(qd, k_cache, v_cache, table, qs, lens, max(n_new), out=out)
+    torch.cuda.synchronize()
+    assert ops().device_error(clear=True) == 0
+    for i, out in enumerate(outs[1:], 1):
+        assert torch.equal(out, outs[0]), f"call {i} differs from call 0"
+    ref = oracle.prefill_chunk(q.double().numpy(), w.k.double().numpy(), w.v.double().numpy(),
+                               n_new, priors, 1.0 / np.sqrt(w.d))
+    compare(outs[0].double().cpu().numpy(), ref, torch.bfloat16, "prefill back to back")

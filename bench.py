@@ -880,10 +880,28 @@ def cpu_baseline(plan, args, budget_s=10.0):
                            "sample": f"{r1} x {k1} seeded sequences, 1 thread, {dt1:.1f} s"}}
 
 
+def reference_workload(args):
+    """The host-side synthetic workload whose decode the oracle times: the
+    same seeded inputs as the GPU arm's workload (its cpu_baseline samples
+    the same decode).  Returns (workload, context-length description)."""
+    name = args.workload
+    if name in ("8b", "70b"):
+        w = synth.decode_workload(name, seed=args.seed, bs=args.block_size or None,
+                                  B=args.batch or None)
+        lo, hi = synth.CONFIGS[name]["len_range"]
+        return w, f"U[{lo},{hi}] seed {args.seed}"
+    if name == "prefix":
+        pf = synth.prefix_fork_workload(seed=args.seed)
+        return pf.base, (f"{pf.base.extra['prefix']}-token shared prompt + U[1,512] private "
+                         f"suffix, seed {args.seed} (the sequences before the forks)")
+    dec, _ = synth.mixed_workload(seed=args.seed)
+    return dec, f"the mixed batch's decodes, seed {args.seed} (its prefill chunks not timed)"
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    w = synth.decode_workload("8b", seed=args.seed)
+    w, ctx = reference_workload(args)
     threads = os.cpu_count() or 1
     n_seq = args.cpu_sample_seqs
     for _ in range(args.warmup):
@@ -899,9 +917,9 @@ def run_reference(args, world, rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * total_t / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOADS["8b"], "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
-                   "head_dim": w.d, "block_size": w.bs,
-                   "context_len": "U[128,4096] seed %d" % args.seed, "parallelism": "host cores"},
+        "config": {"workload": WORKLOADS[args.workload], "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "head_dim": w.d, "block_size": w.bs, "context_len": ctx,
+                   "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
                          "sample": f"{n_seq} of {w.B} sequences per step (seeded), fp64 C "

@@ -83,6 +83,17 @@ def test_reference_arm_prints_the_contract_line(bench, capsys):
     assert e2e["d2h_bytes_per_step"] == 0
 
 
+def test_reference_arm_follows_the_workload(bench, capsys):
+    """--impl reference --workload prefix times the oracle on that workload's
+    sequences (256 sharing a 1024-token prompt), not on the default batch."""
+    import json
+    bench.main(["--impl", "reference", "--workload", "prefix", "--steps", "1", "--warmup", "3",
+                "--cpu-sample-seqs", "2"])
+    j = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert j["config"]["workload"] == bench.WORKLOADS["prefix"]
+    assert j["config"]["B"] == 256 and j["value"] > 0
+
+
 def test_unique_kv_bytes_counts_shared_blocks_once(bench):
     """Two sequences sharing a 2-block prompt (blocks 7, 3) plus private
     blocks: 5 distinct blocks are read; padding entries past a sequence's

@@ -159,7 +159,7 @@ enum { PA_DECODE_PERSISTENT = 1, PA_DECODE_GRID = 2 };
  *                         merge kernel; chosen when B * Hkv * (partitions of
  *                         the table capacity) is at most 1.75 times the
  *                         persistent grid's warp count (little work), and for
- *                         B > 1024.
+ *                         B > 4096.
  * Both meet the same error bound; their results may differ in the last bits
  * (another order of the partial sums).  Arguments as for pa_decode;
  * *kernel receives PA_DECODE_PERSISTENT or PA_DECODE_GRID.  PA_ERR_INVALID
@@ -237,7 +237,7 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
  *          sequence b, KV head h at row (b * Hkv + h) * max_len + j
  *   max_len  a positive multiple of 32; context_lens[b] in [1, max_len]
  *   workspace  at least pa_decode_contiguous_workspace_size bytes
- * Other arguments and the result as for pa_decode.  At most 1024 sequences
+ * Other arguments and the result as for pa_decode.  At most 4096 sequences
  * (PA_ERR_UNSUPPORTED beyond).
  */
 int pa_decode_contiguous_workspace_size(int B, int Hq, int head_dim, int max_len,

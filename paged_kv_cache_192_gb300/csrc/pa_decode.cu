@@ -81,7 +81,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTau = 8.0f;           // lazy-rescale headroom (log2 units)
 constexpr int kDefaultPartition = 512;
 constexpr int kMaxPartition = 8192;
-constexpr int kPersistentMaxB = 1024;  // the persistent kernel keeps [B] tables in smem
+// the persistent kernel keeps [B] tables in shared memory: (3 B + 1) ints,
+// two CTAs per SM up to about 3,200 sequences, one beyond (the occupancy
+// query at launch decides)
+constexpr int kPersistentMaxB = 4096;
 
 template <typename T, int D, int GQ>
 struct Cfg {

@@ -144,19 +144,32 @@ def test_long_sequence_many_segments(lens, Hq, Hkv, kernel):
 
 @pytest.mark.parametrize("Hq,Hkv", [(8, 2), (16, 2)])
 def test_large_batch_grid_kernel(Hq, Hkv):
-    """More than 1024 sequences: the grid kernel (one CTA per sequence, KV
+    """More than 4096 sequences: the grid kernel (one CTA per sequence, KV
     head and 64-token partition) and its separate log-sum-exp merge kernel."""
     rng = np.random.default_rng(13)
-    lens = [int(x) for x in rng.integers(1, 301, size=1100)]
+    lens = [int(x) for x in rng.integers(1, 161, size=4200)]
     w = synth.decode_workload("8b", seed=13, lens=lens, Hq=Hq, Hkv=Hkv)
     got, ref, _ = run(w, partition_tokens=64, kernel="grid")
-    compare(got, ref, torch.bfloat16, f"B=1100 {Hq}/{Hkv}")
+    compare(got, ref, torch.bfloat16, f"B=4200 {Hq}/{Hkv}")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv", [(1500, 32, 8), (3000, 8, 2), (4096, 32, 8)])
+def test_large_batch_of_short_sequences_persistent(B, Hq, Hkv):
+    """Up to 4096 short sequences on the persistent kernel (its [B] tables
+    in shared memory: two CTAs per SM up to ~3,200 sequences, one beyond),
+    with 64-token partitions so that the longer ones split; every output
+    against the oracle."""
+    rng = np.random.default_rng(B)
+    lens = [int(x) for x in rng.integers(1, 201 if B < 4096 else 121, size=B)]
+    w = synth.decode_workload("8b", seed=B, lens=lens, Hq=Hq, Hkv=Hkv)
+    got, ref, _ = run(w, partition_tokens=64, kernel="persistent")
+    compare(got, ref, torch.bfloat16, f"B={B} {Hq}/{Hkv}")
 
 
 def test_kernel_choice_follows_the_work_bound():
     """The grid kernel runs a batch while B * Hkv * partitions of the table
     capacity is at most 1.75 x the persistent grid's warps (8 per SM), and for
-    B > 1024; the persistent kernel otherwise.  On a 152-SM GB300, 8B-shaped
+    B > 4096; the persistent kernel otherwise.  On a 152-SM GB300, 8B-shaped
     batches (4096-token tables, 512-token partitions) switch after 33
     sequences and 32k-token tables after 4."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
@@ -165,8 +178,8 @@ def test_kernel_choice_follows_the_work_bound():
             parts = -(-MB * bs // 512)
             want = "grid" if 4 * B * Hkv * parts <= 7 * 8 * sms else "persistent"
             assert ops().decode_kernel_for(B, Hkv, MB, bs, 512) == want, (B, Hkv, MB, bs)
-    assert ops().decode_kernel_for(1025, 8, 256, 16, 512) == "grid"
-    assert ops().decode_kernel_for(1024, 8, 256, 16, 512) == "persistent"
+    assert ops().decode_kernel_for(4097, 8, 256, 16, 512) == "grid"
+    assert ops().decode_kernel_for(4096, 8, 256, 16, 512) == "persistent"
     if sms == 152:
         assert ops().decode_kernel_for(33, 8, 256, 16, 512) == "grid"
         assert ops().decode_kernel_for(34, 8, 256, 16, 512) == "persistent"

@@ -1238,22 +1238,41 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
     // ---- tiles per sequence and their prefix sums (whole CTA) ---------------
     const int cap = p.MB << p.bs_log2;
     int carry = 0;
-    if constexpr (FORK) {
-        // context lengths and shared lengths, validated as below
-        for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-            int L = p.context_lens[b];
+    // Every sequence's context length and shared length into the tables first,
+    // eight independent loads per thread at a time: one memory latency per
+    // 8 x blockDim sequences (not one per blockDim behind two CTA barriers).
+    for (int b0 = threadIdx.x; b0 < p.B; b0 += 8 * blockDim.x) {
+        int Lv[8], Sv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int b = b0 + u * blockDim.x;
+            Lv[u] = b < p.B ? p.context_lens[b] : 1;
+            Sv[u] = b < p.B && p.shared_len ? p.shared_len[b] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int b = b0 + u * blockDim.x;
+            if (b >= p.B) break;
+            int L = Lv[u];
             if (L < 1 || L > cap) {
                 if (blockIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
                 L = L < 1 ? 0 : cap;
             }
-            int S = p.shared_len ? p.shared_len[b] : 0;
+            // tokens before S are covered by the sequence's shared-prefix
+            // partials (a multiple of the block size, below L; else none)
+            int S = Sv[u];
             if (S < 0 || S >= L || (S & (p.bs - 1))) {
                 if (S != 0 && blockIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
                 S = 0;
             }
             lens[b] = L;
-            slen[b] = S;
             starts[b] = S;
+        }
+    }
+    __syncthreads();
+    if constexpr (FORK) {
+        for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+            slen[b] = starts[b];
             child[b] = 0x7fffffff;
             parent[b] = -1;
         }
@@ -1293,26 +1312,7 @@ __global__ void __launch_bounds__(kWarps * 32, (AttnOf<T, D, GQ, MMA>::type::C::
     }
     for (int base = 0; base < p.B; base += blockDim.x) {
         const int b = base + threadIdx.x;
-        int nt = 0;
-        if (FORK && b < p.B) {
-            nt = (lens[b] - starts[b] + C::TT - 1) / C::TT;
-        } else if (b < p.B) {
-            int L = p.context_lens[b];
-            if (L < 1 || L > cap) {
-                if (blockIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
-                L = L < 1 ? 0 : cap;
-            }
-            // tokens before S are covered by the sequence's shared-prefix
-            // partials (a multiple of the block size, below L; else none)
-            int S = p.shared_len ? p.shared_len[b] : 0;
-            if (S < 0 || S >= L || (S & (p.bs - 1))) {
-                if (S != 0 && blockIdx.x == 0) pa::record_error(p.err, PA_DEVERR_BAD_BLOCK);
-                S = 0;
-            }
-            lens[b] = L;
-            starts[b] = S;
-            nt = (L - S + C::TT - 1) / C::TT;
-        }
+        int nt = b < p.B ? (lens[b] - starts[b] + C::TT - 1) / C::TT : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(pa::kFull, nt, o);
